@@ -1,0 +1,157 @@
+"""ctypes binding of libgemm_f32.so (argument marshalling only).
+
+Every step of the multiply runs in the library's CUDA kernels.  This module
+turns torch CUDA tensors into the pointers, sizes, leading dimensions and
+stream handle that ``include/gemm_f32.h`` declares, checks the returned
+status, and raises ``GemmError`` on failure.  PyTorch serves only as the
+owner of device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+ALGO_AUTO, ALGO_SIMT, ALGO_TMA, ALGO_TF32X3 = 0, 1, 2, 3
+ALGO_NAMES = {ALGO_AUTO: "auto", ALGO_SIMT: "simt", ALGO_TMA: "tma",
+              ALGO_TF32X3: "tf32x3"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def library_path() -> str:
+    return os.environ.get("GEMM_F32_LIBRARY",
+                          os.path.join(_HERE, "libgemm_f32.so"))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libgemm_f32.so not found at {path}: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(path)
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        args = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
+        L.gemm_f32.restype = ci
+        L.gemm_f32.argtypes = args
+        L.gemm_f32_ex.restype = ci
+        L.gemm_f32_ex.argtypes = args + [ci]
+        L.gemm_f32_select_algo.restype = ci
+        L.gemm_f32_select_algo.argtypes = args[:-1]
+        L.gemm_f32_status_string.restype = ctypes.c_char_p
+        L.gemm_f32_status_string.argtypes = [ci]
+        L.gemm_f32_last_cuda_error.restype = ci
+        L.gemm_f32_last_cuda_error.argtypes = []
+        L.gemm_f32_device_status.restype = ci
+        L.gemm_f32_device_status.argtypes = [vp]
+        L.gemm_f32_set_wait_limit.restype = i64
+        L.gemm_f32_set_wait_limit.argtypes = [i64]
+        L.gemm_f32_version.restype = ci
+        L.gemm_f32_version.argtypes = []
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().gemm_f32_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        L = lib()
+        msg = f"{what}: {status_string(status)}"
+        if status == 3:
+            msg += f" (cudaError {L.gemm_f32_last_cuda_error()})"
+        raise GemmError(status, msg)
+
+
+def gemm_f32_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream=0,
+                 algo=ALGO_AUTO):
+    """Raw-pointer call; device addresses and the stream handle as ints."""
+    st = lib().gemm_f32_ex(int(M), int(N), int(K), a_ptr or None, int(lda),
+                           b_ptr or None, int(ldb), c_ptr or None, int(ldc),
+                           stream or None, int(algo))
+    _check(st, "gemm_f32")
+
+
+def _matrix_args(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a float32 torch tensor")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    rows, cols = t.shape
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+    ld = t.stride(0) if rows > 1 else max(cols, 1)
+    return rows, cols, t.data_ptr() if t.numel() else 0, max(ld, cols)
+
+
+def gemm_f32_ex(a, b, c=None, algo=ALGO_AUTO, stream=None):
+    """C = A·B on torch CUDA tensors; returns C (allocated if not given)."""
+    import torch
+    M, K, ap, lda = _matrix_args(a, "a")
+    K2, N, bp, ldb = _matrix_args(b, "b")
+    if K != K2:
+        raise ValueError(f"inner sizes differ: {tuple(a.shape)} x "
+                         f"{tuple(b.shape)}")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    Mc, Nc, cp, ldc = _matrix_args(c, "c")
+    if (Mc, Nc) != (M, N):
+        raise ValueError(f"c has shape {tuple(c.shape)}, want {(M, N)}")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    with torch.cuda.device(a.device):
+        gemm_f32_ptr(M, N, K, ap, lda, bp, ldb, cp, ldc, handle, algo)
+    return c
+
+
+def gemm_f32(a, b, c=None, stream=None):
+    """C = A·B with the automatically selected kernel."""
+    return gemm_f32_ex(a, b, c, ALGO_AUTO, stream)
+
+
+def select_algo(M, N, K, a_ptr=0, lda=None, b_ptr=0, ldb=None, c_ptr=0,
+                ldc=None) -> int:
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return int(lib().gemm_f32_select_algo(M, N, K, a_ptr or None, lda,
+                                          b_ptr or None, ldb, c_ptr or None,
+                                          ldc))
+
+
+def device_status(stream=None) -> int:
+    """Waits for the stream, returns and clears the kernels' status word."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    return int(lib().gemm_f32_device_status(handle or None))
+
+
+def set_wait_limit(polls: int) -> int:
+    return int(lib().gemm_f32_set_wait_limit(int(polls)))
+
+
+def version() -> int:
+    return int(lib().gemm_f32_version())

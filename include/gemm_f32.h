@@ -1,0 +1,123 @@
+/*
+ * gemm_f32 — single-precision matrix multiply C = A·B for NVIDIA GB300
+ * (sm_103a), row-major, behind a plain C ABI.
+ *
+ * The operation (the pages this library implements):
+ *   "3 · La mémoire partagée", §3.1 "Le problème que ça résout" defines the
+ *   product: every output C[i][j] is the sum over k of A[i][k]·B[k][j],
+ *   one multiply and one add per term (2·M·N·K operations), accumulated in
+ *   single precision, and written over C (no scaling, no accumulation into
+ *   the old C).  "共享内存与同步", section "SharedArray —— 静态共享内存"
+ *   (tiled_sgemm) gives the general m, n, k form with row-major float
+ *   operands.  §3.3-§3.4 of the first page describe the shared-memory tile
+ *   and register micro-tile that the kernels here are built on.
+ *
+ * Layout: all three matrices are row-major float32 in device memory.
+ *   A is M×K with row stride lda (elements), B is K×N with row stride ldb,
+ *   C is M×N with row stride ldc.  Element (i, j) of C lives at
+ *   C[i*ldc + j].  Only C[i*ldc + j] for i < M, j < N is written; the
+ *   padding between N and ldc is left untouched.
+ *
+ * Ownership: the caller owns A, B and C.  The library never allocates or
+ * frees device memory on these calls, never synchronizes the stream and
+ * keeps no pointer after the call returns.  Work is queued on `stream`
+ * (NULL = the legacy default stream) and is complete when the stream is.
+ * C must not overlap A or B (not checked).
+ *
+ * Errors: every entry point returns a gemm_f32_status and never throws.
+ * Nothing is launched unless the call returns GEMM_F32_OK.
+ *
+ * Thread safety: calls from several host threads are safe; per-device
+ * one-time set-up is guarded internally.
+ */
+#ifndef GEMM_F32_H
+#define GEMM_F32_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream; binary compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st *gemm_f32_stream_t;
+
+typedef enum {
+    GEMM_F32_OK = 0,
+    /* M, N or K < 0; lda < K, ldb < N or ldc < N; a NULL pointer for a
+     * matrix with at least one element; an unknown algo value. */
+    GEMM_F32_ERR_INVALID_ARG = 1,
+    /* A forced algorithm whose preconditions do not hold (alignment, sizes,
+     * device architecture).  GEMM_F32_ALGO_AUTO never returns this. */
+    GEMM_F32_ERR_UNSUPPORTED = 2,
+    /* A CUDA runtime error while setting up or launching; the code is
+     * available from gemm_f32_last_cuda_error(). */
+    GEMM_F32_ERR_CUDA = 3,
+    /* A kernel's bounded wait gave up (reported by gemm_f32_device_status). */
+    GEMM_F32_ERR_TIMEOUT = 4
+} gemm_f32_status;
+
+typedef enum {
+    /* Pick the fastest kernel whose preconditions hold. */
+    GEMM_F32_ALGO_AUTO = 0,
+    /* FP32 FFMA register-tiled kernel, operands staged by cp.async into a
+     * multi-stage swizzled shared-memory ring.  Any pointer alignment and
+     * any leading dimension. */
+    GEMM_F32_ALGO_SIMT = 1,
+    /* FP32 FFMA register-tiled kernel fed by a TMA producer warp through an
+     * mbarrier full/empty ring.  Needs A and B 16-byte aligned and lda, ldb
+     * multiples of 4. */
+    GEMM_F32_ALGO_TMA = 2,
+    /* Tensor-core kernel (tcgen05, TMEM accumulator) computing each product
+     * as three TF32 products of a big/small operand split, accumulated in
+     * fp32.  Same alignment needs as GEMM_F32_ALGO_TMA. */
+    GEMM_F32_ALGO_TF32X3 = 3
+} gemm_f32_algo;
+
+/*
+ * C = A·B.  M, N, K >= 0.  M == 0 or N == 0: returns OK and launches
+ * nothing.  K == 0: C[0:M, 0:N] is set to 0 (the empty sum).
+ */
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+             const float *B, int64_t ldb, float *C, int64_t ldc,
+             gemm_f32_stream_t stream);
+
+/* As gemm_f32, with the kernel family forced by `algo` (gemm_f32_algo). */
+int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                const float *B, int64_t ldb, float *C, int64_t ldc,
+                gemm_f32_stream_t stream, int algo);
+
+/* The algorithm gemm_f32 with GEMM_F32_ALGO_AUTO would run for these
+ * arguments on the current device (no launch).  Negative on bad args. */
+int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float *A,
+                         int64_t lda, const float *B, int64_t ldb, float *C,
+                         int64_t ldc);
+
+/* Static description of a status code. */
+const char *gemm_f32_status_string(int status);
+
+/* cudaError_t of the most recent GEMM_F32_ERR_CUDA on this host thread. */
+int gemm_f32_last_cuda_error(void);
+
+/*
+ * Waits for `stream`, then reads and clears the current device's kernel
+ * status word.  Returns GEMM_F32_OK, GEMM_F32_ERR_TIMEOUT if a kernel's
+ * bounded mbarrier wait gave up since the last call, or
+ * GEMM_F32_ERR_CUDA.  This is the only entry point that synchronizes.
+ */
+int gemm_f32_device_status(gemm_f32_stream_t stream);
+
+/* Test hook: the number of polls after which the pipelined kernels' mbarrier
+ * waits give up (0 restores the default).  Returns the previous value.  A
+ * kernel that gives up sets the status word and stops the CTA without
+ * writing its tile. */
+int64_t gemm_f32_set_wait_limit(int64_t polls);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int gemm_f32_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F32_H */

@@ -1,0 +1,177 @@
+/*
+ * Float64 CPU oracle for the FP32 matrix multiply C = A·B.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code with the CUDA path.
+ *
+ * What it computes, from the pages' definition of the product:
+ *   "3 · La mémoire partagée", §3.1 "Le problème que ça résout": each output
+ *   C[lig][col] is the sum over k of A[lig][k]·B[k][col], one multiply and
+ *   one add per k, 2N³ operations for N×N; and "共享内存与同步" (cuda-oxide),
+ *   section "SharedArray —— 静态共享内存" (tiled_sgemm): general m×k times
+ *   k×n with A read as a[row*k + i] and B as b[i*n + col], row-major.
+ * Every kernel on those pages overwrites C (no alpha, no beta).
+ *
+ *   C_ref[i][j]  = sum_{k=0}^{K-1} (double)A[i][k] * (double)B[k][j]
+ *   bound[i][j]  = sum_{k=0}^{K-1} |A[i][k]| * |B[k][j]|     (float64)
+ *
+ * The k sum runs in ascending k for every element.  The loop nest is i-k-j
+ * with a float64 row accumulator; that changes no element's summation order
+ * relative to the i-j-k triple loop, it only walks B by rows.
+ * K = 0 gives the empty sum, 0.  M = 0 or N = 0 writes nothing.
+ *
+ * Build with -O2 -fno-fast-math -ffp-contract=off so no multiply-add is
+ * fused: the x86 host and the aarch64 GPU host then give identical bits.
+ *
+ * ORACLE_MUTANT (compile-time, tests only) plants one plausible mistake so
+ * the tests can show their pins catch it; 0 (the default) is the oracle.
+ *   1 drops the last k term, 2 reads B transposed (B[j][k], the flat index
+ *   wrapped into B's extent so the mistake stays in bounds),
+ *   3 subtracts odd-k terms, 4 reads A one row too high (wraps at M-1),
+ *   5 accumulates in float32 instead of float64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+#if ORACLE_MUTANT == 5
+typedef float acc_t;
+#else
+typedef double acc_t;
+#endif
+
+/* Element (i, k) of A and (k, j) of B as the definition reads them.  The
+ * mutants change only these reads, the range of k or the sign. */
+static inline double a_at(const float *A, int64_t lda, int64_t M, int64_t i,
+                          int64_t k) {
+#if ORACLE_MUTANT == 4
+    int64_t r = (i + 1 < M) ? i + 1 : i;
+    return (double)A[r * lda + k];
+#else
+    (void)M;
+    return (double)A[i * lda + k];
+#endif
+}
+
+static inline double b_at(const float *B, int64_t ldb, int64_t K, int64_t k,
+                          int64_t j) {
+#if ORACLE_MUTANT == 2
+    return (double)B[(j * ldb + k) % (K * ldb)];
+#else
+    (void)K;
+    return (double)B[k * ldb + j];
+#endif
+}
+
+static inline int64_t k_end(int64_t K) {
+#if ORACLE_MUTANT == 1
+    return K > 0 ? K - 1 : 0;
+#else
+    return K;
+#endif
+}
+
+static inline double term_sign(int64_t k) {
+#if ORACLE_MUTANT == 3
+    return (k & 1) ? -1.0 : 1.0;
+#else
+    (void)k;
+    return 1.0;
+#endif
+}
+
+/*
+ * Full product.  C (M×N, leading dimension ldc) receives C_ref; bound, when
+ * not NULL, receives the matching sum of magnitudes with the same ldc.
+ * nthreads <= 0 uses the OpenMP default.  Returns the number of
+ * multiply-adds performed (M·N·K for the oracle), or -1 on bad arguments.
+ */
+int64_t oracle_gemm_f64(int64_t M, int64_t N, int64_t K, const float *A,
+                        int64_t lda, const float *B, int64_t ldb, double *C,
+                        int64_t ldc, double *bound, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || ldc < N) return -1;
+    if (M == 0 || N == 0) return 0;
+    int64_t fmas = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel reduction(+ : fmas)
+    {
+        acc_t *row = (acc_t *)malloc(sizeof(acc_t) * (size_t)N);
+        double *mag = (double *)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(static)
+        for (int64_t i = 0; i < M; ++i) {
+            for (int64_t j = 0; j < N; ++j) {
+                row[j] = 0;
+                mag[j] = 0.0;
+            }
+            const int64_t kend = k_end(K);
+            for (int64_t k = 0; k < kend; ++k) {
+                const double a = a_at(A, lda, M, i, k) * term_sign(k);
+                for (int64_t j = 0; j < N; ++j) {
+                    const double b = b_at(B, ldb, K, k, j);
+                    row[j] += (acc_t)(a * b);
+                    mag[j] += fabs(a) * fabs(b);
+                }
+                fmas += N;
+            }
+            for (int64_t j = 0; j < N; ++j) C[i * ldc + j] = (double)row[j];
+            if (bound)
+                for (int64_t j = 0; j < N; ++j) bound[i * ldc + j] = mag[j];
+        }
+        free(row);
+        free(mag);
+    }
+    return fmas;
+}
+
+/*
+ * Selected elements only: out[t] = C_ref[rows[t]][cols[t]] (and its bound),
+ * for checking a few outputs of a product too large to compute whole.
+ * Returns the number of multiply-adds, or -1 on bad arguments.
+ */
+int64_t oracle_gemm_f64_entries(int64_t M, int64_t N, int64_t K,
+                                const float *A, int64_t lda, const float *B,
+                                int64_t ldb, int64_t count, const int64_t *rows,
+                                const int64_t *cols, double *out,
+                                double *bound) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || count < 0) return -1;
+    int64_t fmas = 0;
+    for (int64_t t = 0; t < count; ++t) {
+        const int64_t i = rows[t], j = cols[t];
+        if (i < 0 || i >= M || j < 0 || j >= N) return -1;
+        acc_t s = 0;
+        double m = 0.0;
+        const int64_t kend = k_end(K);
+        for (int64_t k = 0; k < kend; ++k) {
+            const double a = a_at(A, lda, M, i, k) * term_sign(k);
+            const double b = b_at(B, ldb, K, k, j);
+            s += (acc_t)(a * b);
+            m += fabs(a) * fabs(b);
+            ++fmas;
+        }
+        out[t] = (double)s;
+        if (bound) bound[t] = m;
+    }
+    return fmas;
+}
+
+/* Threads OpenMP would use for oracle_gemm_f64 with nthreads <= 0. */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

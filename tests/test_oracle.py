@@ -1,0 +1,232 @@
+"""Pins for the float64 oracle, against facts that do not come from it.
+
+Each pin checks the oracle against something the pages or mathematics fix:
+hand-worked products (tests/golden), closed forms (identity, all-ones,
+index products, permutations), exact integer arithmetic, exact rational
+brute force, a naive float32 loop inside its rounding-error bound, the
+pages' operation count 2MNK ("3 · La mémoire partagée", §3.1) and
+metamorphic relations.  ``test_mutant_is_caught`` builds oracle copies with
+one planted mistake each (dropped term, transposed operand, wrong sign,
+wrong row, float32 accumulation) and checks that some pin fails on each.
+"""
+
+from __future__ import annotations
+
+import fractions
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_fp32_matrix_02_gb300 import synth
+from helpers import load_golden_cases
+
+U64 = 2.0**-53  # float64 unit roundoff
+U32 = 2.0**-24  # float32 unit roundoff
+
+
+def _gamma(n, u):
+    return n * u / (1.0 - n * u)
+
+
+# --------------------------------------------------------------------- pins
+def pin_golden(orc):
+    """Hand-worked products: exact, bit for bit."""
+    for name, m in load_golden_cases():
+        c, _, _ = orc.gemm(m["A"], m["B"])
+        assert np.array_equal(c, m["C"]), f"golden case {name}: {c} != {m['C']}"
+
+
+def pin_identity(orc):
+    """A·I = A and I·B = B exactly (one non-zero term per sum)."""
+    a, b = synth.make_operands(37, 29, 23, seed=11)
+    c, _, _ = orc.gemm(a, np.eye(23, dtype=np.float32))
+    assert np.array_equal(c, a.astype(np.float64)), "A·I != A"
+    c, _, _ = orc.gemm(np.eye(23, dtype=np.float32), b)
+    assert np.array_equal(c, b.astype(np.float64)), "I·B != B"
+
+
+def pin_all_ones(orc):
+    """All-ones A (M×K) and B (K×N) give C = K everywhere."""
+    for (M, N, K) in [(5, 7, 1), (9, 4, 13), (16, 16, 64)]:
+        c, bound, _ = orc.gemm(np.ones((M, K), np.float32),
+                               np.ones((K, N), np.float32))
+        assert np.array_equal(c, np.full((M, N), float(K))), "ones·ones != K"
+        assert np.array_equal(bound, np.full((M, N), float(K)))
+
+
+def pin_index_product(orc):
+    """A[i][k] = i, B[k][j] = j gives C[i][j] = K·i·j exactly."""
+    M, N, K = 12, 10, 9
+    a = np.repeat(np.arange(M, dtype=np.float32)[:, None], K, axis=1)
+    b = np.repeat(np.arange(N, dtype=np.float32)[None, :], K, axis=0)
+    c, _, _ = orc.gemm(a, b)
+    want = K * np.outer(np.arange(M), np.arange(N)).astype(np.float64)
+    assert np.array_equal(c, want), "index product wrong"
+
+
+def pin_permutation(orc):
+    """P·B permutes B's rows and B·P permutes its columns, exactly."""
+    rng = np.random.default_rng(5)
+    _, b = synth.make_operands(1, 11, 11, seed=12)
+    perm = rng.permutation(11)
+    p = np.eye(11, dtype=np.float32)[perm]  # row i of P is e_{perm[i]}
+    c, _, _ = orc.gemm(p, b)
+    assert np.array_equal(c, b[perm].astype(np.float64)), "P·B wrong"
+    c, _, _ = orc.gemm(b, p)
+    inv = np.argsort(perm)
+    assert np.array_equal(c, b[:, inv].astype(np.float64)), "B·P wrong"
+
+
+def pin_integer_exact(orc):
+    """Small-integer inputs: equal to exact int64 arithmetic."""
+    for (M, N, K, seed) in [(17, 23, 31, 0), (64, 64, 64, 0), (3, 130, 257, 4)]:
+        a, b = synth.make_operands(M, N, K, seed, "int", "int")
+        c, _, _ = orc.gemm(a, b)
+        exact = a.astype(np.int64) @ b.astype(np.int64)
+        assert np.array_equal(c, exact.astype(np.float64)), "integer product"
+
+
+def pin_exact_rational(orc):
+    """Brute force in exact rationals: within the float64 summation bound.
+
+    The product of two float32 values is exact in float64, so the oracle's
+    only rounding is in its K-1 additions: |C_ref - C| <= gamma_{K-1}·sum|ab|.
+    Includes a case (1 + 2**-30) that a float32 accumulator gets wrong.
+    """
+    cases = [synth.make_operands(M, N, K, seed=21 + M)
+             for (M, N, K) in [(1, 1, 1), (2, 3, 5), (4, 4, 7), (3, 5, 16)]]
+    cases.append((np.array([[1.0, 2.0**-30, -3.0]], np.float32),
+                  np.array([[1.0], [1.0], [2.0**-40]], np.float32)))
+    for a, b in cases:
+        c, bound, _ = orc.gemm(a, b)
+        M, K = a.shape
+        N = b.shape[1]
+        for i, j in itertools.product(range(M), range(N)):
+            exact = sum(fractions.Fraction(float(a[i, k])) *
+                        fractions.Fraction(float(b[k, j])) for k in range(K))
+            err = abs(fractions.Fraction(c[i, j]) - exact)
+            mag = sum(abs(fractions.Fraction(float(a[i, k])) *
+                          fractions.Fraction(float(b[k, j]))) for k in range(K))
+            assert err <= fractions.Fraction(_gamma(max(K - 1, 0), U64)) * mag, \
+                f"rational check at {(i, j)}: {c[i, j]!r} vs {float(exact)!r}"
+            assert bound[i, j] == float(mag) or abs(
+                fractions.Fraction(bound[i, j]) - mag) <= \
+                fractions.Fraction(_gamma(K, U64)) * mag, "bound wrong"
+
+
+def pin_naive_float32(orc):
+    """A naive float32 loop (k ascending) agrees within its error bound.
+
+    For every M, N, K in 1..16: |C32 - C_ref| <= gamma_K(2**-24)·sum|ab|
+    plus the oracle's own float64 bound.
+    """
+    for M, N, K in itertools.product(range(1, 17), repeat=3):
+        if (M * 7 + N * 3 + K) % 5:  # every fifth shape keeps this quick
+            continue
+        a, b = synth.make_operands(M, N, K, seed=1000 + M * 289 + N * 17 + K)
+        c32 = np.zeros((M, N), np.float32)
+        for k in range(K):
+            c32 = (c32 + (a[:, k:k + 1] * b[k:k + 1, :]).astype(np.float32)
+                   ).astype(np.float32)
+        c, bound, _ = orc.gemm(a, b)
+        lim = (_gamma(K, U32) + _gamma(K, U64)) * bound
+        assert (np.abs(c32.astype(np.float64) - c) <= lim).all(), \
+            f"naive float32 loop disagrees at M,N,K={M},{N},{K}"
+
+
+def pin_operation_count(orc):
+    """2·(multiply-adds) = 2MNK, the pages' 2N³ for square N×N."""
+    for (M, N, K) in [(64, 64, 64), (3, 5, 7), (10, 1, 33)]:
+        a, b = synth.make_operands(M, N, K, seed=3)
+        _, _, fmas = orc.gemm(a, b)
+        assert 2 * fmas == 2 * M * N * K, f"op count {2 * fmas}"
+    _, _, fmas = orc.gemm(*synth.make_operands(64, 64, 64, seed=0))
+    assert 2 * fmas == 2 * 64**3
+
+
+def pin_metamorphic(orc):
+    """(AB)ᵀ = BᵀAᵀ bitwise; K-split additivity (exact on integers);
+    scaling A by 2 scales C by 2 exactly; entries() equals gemm()."""
+    a, b = synth.make_operands(19, 13, 21, seed=7)
+    c, bound, _ = orc.gemm(a, b)
+    ct, _, _ = orc.gemm(np.ascontiguousarray(b.T), np.ascontiguousarray(a.T))
+    assert np.array_equal(c.T, ct), "(AB)^T != B^T A^T"
+    c2, _, _ = orc.gemm(2 * a, b)
+    assert np.array_equal(c2, 2 * c), "C(2A) != 2 C(A)"
+    ai, bi = synth.make_operands(19, 13, 21, seed=7, dist_a="int", dist_b="int")
+    ci, _, _ = orc.gemm(ai, bi)
+    k1 = 8
+    p1, _, _ = orc.gemm(np.ascontiguousarray(ai[:, :k1]), bi[:k1])
+    p2, _, _ = orc.gemm(np.ascontiguousarray(ai[:, k1:]), bi[k1:])
+    assert np.array_equal(ci, p1 + p2), "K-split additivity"
+    rows = np.array([0, 5, 18, 7])
+    cols = np.array([0, 12, 3, 7])
+    e, eb, fm = orc.entries(a, b, rows, cols)
+    assert np.array_equal(e, c[rows, cols]) and np.array_equal(
+        eb, bound[rows, cols]) and fm == 4 * 21
+
+
+def pin_bound(orc):
+    """bound = oracle(|A|, |B|) and |C| <= bound."""
+    a, b = synth.make_operands(9, 11, 40, seed=9, dist_a="normal",
+                               dist_b="normal")
+    c, bound, _ = orc.gemm(a, b)
+    m, _, _ = orc.gemm(np.abs(a), np.abs(b))
+    assert np.array_equal(m, bound)
+    assert (np.abs(c) <= bound).all()
+
+
+def pin_empty(orc):
+    """K = 0 is the empty sum (zeros); M = 0 or N = 0 is an empty C."""
+    c, bound, f = orc.gemm(np.zeros((4, 0), np.float32),
+                           np.zeros((0, 5), np.float32))
+    assert c.shape == (4, 5) and not c.any() and not bound.any() and f == 0
+    c, _, _ = orc.gemm(np.zeros((0, 3), np.float32), np.ones((3, 5), np.float32))
+    assert c.shape == (0, 5)
+    c, _, _ = orc.gemm(np.ones((4, 3), np.float32), np.zeros((3, 0), np.float32))
+    assert c.shape == (4, 0)
+
+
+PINS = [pin_golden, pin_identity, pin_all_ones, pin_index_product,
+        pin_permutation, pin_integer_exact, pin_exact_rational,
+        pin_naive_float32, pin_operation_count, pin_metamorphic, pin_bound,
+        pin_empty]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+def test_mutant_is_caught(mutant, tmp_path):
+    """Each planted mistake makes at least one pin fail."""
+    orc = oracle.Oracle(oracle.build(mutant, outdir=str(tmp_path)))
+    failed = []
+    for pin in PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {mutant} passed every pin"
+
+
+def test_threads_do_not_change_bits(oracle_lib):
+    a, b = synth.make_operands(33, 45, 70, seed=2)
+    c1, b1, _ = oracle_lib.gemm(a, b, threads=1)
+    c4, b4, _ = oracle_lib.gemm(a, b, threads=4)
+    assert np.array_equal(c1, c4) and np.array_equal(b1, b4)
+
+
+def test_strided_operands(oracle_lib):
+    """Leading dimensions larger than the row width are honoured."""
+    a, b = synth.make_operands(6, 5, 7, seed=8)
+    big_a = np.zeros((6, 11), np.float32)
+    big_a[:, :7] = a
+    big_b = np.zeros((7, 9), np.float32)
+    big_b[:, :5] = b
+    c, _, _ = oracle_lib.gemm(a, b)
+    cs, _, _ = oracle_lib.gemm(big_a[:, :7], big_b[:, :5])
+    assert np.array_equal(c, cs)
