@@ -1,0 +1,390 @@
+"""Benchmark of the FP32 GEMM C = A·B (libgemm_f32, one JSON line on stdout).
+
+Default workload: M = N = K = 4096, row-major float32, entries uniform in
+[-1, 1) from SplitMix64 seed 2.  A step is one gemm_f32 call over the whole
+problem.  Inputs sit in HBM before the timed region; consecutive steps
+rotate over three input/output sets (3 × 192 MB, well over the 129 MB L2),
+so no step finds its operands left in L2 by the step before.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank multiplies its own full problem on its own
+GPU (independent problems, no collective on the data path: weak scaling);
+the value is all ranks' flops over the slowest rank's time.
+
+``--impl reference`` times the float64 CPU oracle on this machine's host
+cores instead (rank 0 only), each step a bounded block of rows of the same
+workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("FP32 GEMM TFLOPS at M=N=K=4096 and % of GB300 FP32 roofline, "
+          "1 GPU")
+ALGOS = {"auto": 0, "simt": 1, "tma": 2, "tf32x3": 3}
+FP32_LANES_PER_SM = 128  # FFMA lanes per SM on GB300 (4 SMSPs x 32)
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="sq4096")
+    p.add_argument("--algo", default="auto", choices=list(ALGOS))
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp32_matrix_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.proc = None
+        self.error = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.error = str(e)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "error": self.error or "nvidia-smi unavailable"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------- reference (oracle)
+def oracle_rows_timing(a, b, rows, threads=0):
+    import oracle
+    t = time.perf_counter()
+    oracle.gemm(a[:rows], b, threads=threads)
+    return time.perf_counter() - t
+
+
+def calibrate_rows(a, b, target_s):
+    """Rows of A whose oracle product takes about target_s seconds."""
+    M = a.shape[0]
+    rows = min(M, 8)
+    t = oracle_rows_timing(a, b, rows)
+    while t < 0.2 and rows < M:
+        rows = min(M, rows * 4)
+        t = oracle_rows_timing(a, b, rows)
+    return max(1, min(M, int(rows * target_s / max(t, 1e-6))))
+
+
+def cpu_baseline(w, a, b, target_s):
+    import oracle
+    rows = calibrate_rows(a, b, target_s)
+    t = oracle_rows_timing(a, b, rows)
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.load().max_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of A times all of B "
+                      f"({rows}x{w.N}x{w.K}, float64 accumulation, "
+                      f"{t:.1f} s)"}
+
+
+def run_reference(args, w, config):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    a, b = w.operands()
+    nthreads = oracle.load().max_threads()
+    per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = calibrate_rows(a, b, per_step)
+    for _ in range(args.warmup):
+        oracle_rows_timing(a, b, rows)
+    times = [oracle_rows_timing(a, b, rows) for _ in range(args.steps)]
+    total = sum(times)
+    flops = 2.0 * rows * w.N * w.K
+    value = flops * args.steps / total / 1e12
+    sample = (f"rows 0..{rows - 1} of A times all of B per step "
+              f"({rows}x{w.N}x{w.K}, float64 accumulation)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": config,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, w, config):
+    import torch
+    import torch.distributed as dist
+
+    from dense_fp32_matrix_02_gb300 import gemm as G
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    algo = ALGOS[args.algo]
+    a, b = w.operands()
+    nsets = 3
+    ta0 = torch.from_numpy(a).to(dev)
+    tb0 = torch.from_numpy(b).to(dev)
+    sets = [(ta0, tb0, torch.empty(w.M, w.N, device=dev))]
+    for _ in range(nsets - 1):
+        sets.append((ta0.clone(), tb0.clone(), torch.empty(w.M, w.N,
+                                                           device=dev)))
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    ran = G.select_algo(w.M, w.N, w.K, ta0.data_ptr(), w.K, tb0.data_ptr(),
+                        w.N, sets[0][2].data_ptr(), w.N) if algo == 0 else algo
+
+    def step(i):
+        ta, tb, tc = sets[i % nsets]
+        G.gemm_f32_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K, tb.data_ptr(), w.N,
+                       tc.data_ptr(), w.N, handle, algo)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if G.device_status() != 0:
+        raise SystemExit("kernel status word set during warm-up")
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001 - older torch
+        gpu_uuid = None
+    sampler = ClockSampler(gpu_uuid)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = start.elapsed_time(end)
+    t_ms = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
+    ms_max = float(t_ms.item())
+    if G.device_status() != 0:
+        raise SystemExit("kernel status word set during the timed region")
+
+    flops = float(w.flops)
+    value = flops * args.steps * world / (ms_max / 1e3) / 1e12
+    kernel_ms = ms / args.steps  # one launch per step, gaps included
+
+    # ---- end to end: pinned host buffers through the public API
+    ha = torch.from_numpy(a).pin_memory()
+    hb = torch.from_numpy(b).pin_memory()
+    hc = torch.empty(w.M, w.N, dtype=torch.float32).pin_memory()
+    ea, eb, ec = sets[0]
+    e_steps = max(1, args.e2e_steps)
+
+    def e2e_step():
+        ea.copy_(ha, non_blocking=True)
+        eb.copy_(hb, non_blocking=True)
+        G.gemm_f32(ea, eb, ec, stream=stream)
+        hc.copy_(ec, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    s2 = torch.cuda.Event(enable_timing=True)
+    e2 = torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e_ms = torch.tensor([s2.elapsed_time(e2)], device=dev)
+    if world > 1:
+        dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = flops * e_steps * world / (float(e_ms.item()) / 1e3) / 1e12
+
+    # ---- roofline of the (only) kernel
+    peaks, peaks_src = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    smax = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    fp32_peak = 2.0 * sms * FP32_LANES_PER_SM * smax * 1e6 / 1e12
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    algo_name = G.ALGO_NAMES.get(ran, str(ran))
+    if algo_name == "tf32x3":
+        # three TF32 tensor products per algorithmic multiply-add; TF32
+        # dense rate = bf16 rate x (1.1 / 2.25), the nominal ratio
+        tf32 = peaks["bf16_tflops"] * (1.1 / 2.25)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf32 / 3.0,
+                "unit": "TFLOP/s", "frac": achieved / (tf32 / 3.0),
+                "peak_source": f"{peaks_src} bf16 burst {peaks['bf16_tflops']}"
+                               " x 1.1/2.25 (nominal TF32/bf16), / 3 products"}
+    else:
+        roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak,
+                "unit": "TFLOP/s", "frac": achieved / fp32_peak,
+                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes "
+                               f"x 2 flop x {smax:.0f} MHz (max SM clock)"}
+    roof["traffic"] = recorded_traffic(f"{algo_name}:{w.name}")
+    roof["algorithmic_bytes"] = w.bytes
+    roof["kernel_ms"] = kernel_ms
+
+    fp32_roof = min(fp32_peak, (flops / w.bytes) * peaks["hbm_gbs"] / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config,
+        "kernel": algo_name,
+        "pct_fp32_roofline": 100.0 * (value / world) / fp32_roof,
+        "fp32_roofline_tflops": fp32_roof,
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
+                "d2h_bytes_per_step": 4 * w.M * w.N},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, a, b, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    from dense_fp32_matrix_02_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    dist_txt = {"uniform": "uniform [-1,1)", "normal": "normal",
+                "int": "integers {-2..2}"}
+    config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+              "layout": "row-major, ld = row width",
+              "inputs": f"A {dist_txt[w.dist_a]} (sigma {w.sigma_a}), "
+                        f"B {dist_txt[w.dist_b]} (sigma {w.sigma_b}), "
+                        f"SplitMix64 seed {w.seed}",
+              "l2": "3 rotating input/output sets (3 x "
+                    f"{w.bytes / 2**20:.0f} MiB) between timed steps",
+              "parallelism": f"independent problem per GPU x {args.gpus}"}
+    if args.impl == "reference":
+        run_reference(args, w, config)
+    else:
+        run_ours(args, w, config)
+
+
+if __name__ == "__main__":
+    main()

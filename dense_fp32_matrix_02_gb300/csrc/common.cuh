@@ -1,0 +1,166 @@
+// Shared device helpers for the gemm_f32 kernels: inline-PTX wrappers for
+// cp.async, mbarrier and TMA, the kernel status word and the launch-side
+// description of one GEMM problem.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gemm_f32_impl {
+
+// Status word bits written by kernels (read and cleared by the host).
+enum : unsigned int {
+  kStatusTimeoutFull = 1u,   // a consumer gave up waiting for a full stage
+  kStatusTimeoutEmpty = 2u,  // the producer gave up waiting for an empty stage
+  kStatusTimeoutDrain = 4u,  // copies still in flight when giving up
+  kStatusTimeoutMma = 8u,    // tensor-core completion wait gave up
+};
+
+// Debug flags passed to the pipelined kernels (tests only).
+enum : unsigned int {
+  kDebugStallProducer = 1u,  // producer issues no copies: consumers time out
+};
+
+// One problem as the kernels see it.  Leading dimensions in elements.
+struct Problem {
+  int M, N, K;
+  const float* A;
+  long long lda;
+  const float* B;
+  long long ldb;
+  float* C;
+  long long ldc;
+};
+
+// Bounded-wait configuration shared by all pipelined kernels.
+struct WaitCfg {
+  long long limit;        // polls before a wait gives up
+  unsigned int debug;     // kDebug* bits
+  unsigned int* status;   // device status word
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- cp.async
+// 16-byte copy global -> shared; bytes beyond src_bytes (0..16) are zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src,
+                                           int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// 4-byte copy global -> shared; src_bytes 0 writes a zero.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src,
+                                          int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- shared loads
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar),
+               "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(
+          bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .b64 st;\n"
+      " mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+
+// One non-blocking probe of phase `parity`; true once that phase completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: polls up to `limit` times; false if the phase never came.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
+                                                  uint32_t parity,
+                                                  long long limit) {
+  for (long long i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------- TMA
+// 2-D tiled bulk tensor load into shared memory, completion counted on the
+// mbarrier in transaction bytes.  c0 is the innermost coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap,
+                                            uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4}], [%2];\n" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
+}
+
+__device__ __forceinline__ void record_status(unsigned int* status,
+                                              unsigned int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Tile order: walks GROUP tile-rows at a time so concurrently running CTAs
+// share A row-panels and B column-panels in L2.
+template <int GROUP>
+__device__ __forceinline__ void tile_coords(int linear, int tiles_m,
+                                            int tiles_n, int& tm, int& tn) {
+  const int per_group = GROUP * tiles_n;
+  const int g = linear / per_group;
+  const int first_m = g * GROUP;
+  const int rows = min(tiles_m - first_m, GROUP);
+  const int in_group = linear - g * per_group;
+  tm = first_m + in_group % rows;
+  tn = in_group / rows;
+}
+
+}  // namespace gemm_f32_impl

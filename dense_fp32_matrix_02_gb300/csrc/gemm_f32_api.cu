@@ -1,0 +1,259 @@
+// C ABI of libgemm_f32: argument checks, kernel selection and launch.
+//
+// The ABI is declared in include/gemm_f32.h.  Every entry point returns a
+// status and never throws; only gemm_f32_device_status synchronizes.
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "gemm_f32.h"
+#include "kernels.h"
+
+using namespace gemm_f32_impl;
+
+// Kernel status word (kStatus* bits), one per device; read and cleared by
+// gemm_f32_device_status.
+__device__ unsigned int g_kernel_status;
+
+namespace {
+
+constexpr long long kDefaultWaitLimit = 1LL << 26;
+constexpr int kMaxDevices = 64;
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+std::atomic<unsigned int> g_debug_flags{0};
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_devices[kMaxDevices];
+std::set<std::pair<int, const void*>> g_smem_attr_done;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return GEMM_F32_ERR_CUDA;
+}
+
+// Per-device facts, fetched once with that device current.
+cudaError_t device_info(const DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return e;
+    void* status = nullptr;
+    if ((e = cudaGetSymbolAddress(&status, g_kernel_status)) != cudaSuccess)
+      return e;
+    d.sm_count = prop.multiProcessorCount;
+    d.cc_major = prop.major;
+    d.cc_minor = prop.minor;
+    d.status = static_cast<unsigned int*>(status);
+    d.ready = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return fallback;
+  return std::atoi(v);
+}
+
+struct Plan {
+  int algo;      // gemm_f32_algo actually run
+  int simt_cfg;  // for ALGO_SIMT
+  bool vec;      // 16-byte operand copies
+  bool c_vec;    // 16-byte C stores
+};
+
+int check_args(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+               const float* B, int64_t ldb, const float* C, int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return GEMM_F32_ERR_INVALID_ARG;
+  if (lda < K || ldb < N || ldc < N) return GEMM_F32_ERR_INVALID_ARG;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
+    return GEMM_F32_ERR_UNSUPPORTED;
+  if (M > 0 && N > 0) {
+    if (!C) return GEMM_F32_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B)) return GEMM_F32_ERR_INVALID_ARG;
+  }
+  return GEMM_F32_OK;
+}
+
+int choose_simt_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
+  const int forced = env_int("GEMM_F32_SIMT_CFG", -1);
+  if (forced >= 0 && forced < kSimtCfgCount) return forced;
+  if (N <= 64) return kSimt128x64x16;
+  const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+  if (tiles < d.sm_count) return kSimt128x64x16;
+  return kSimt128x128x16;
+}
+
+// Decides which kernel runs.  Returns a status; fills *plan on success.
+int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+              const float* B, int64_t ldb, const float* C, int64_t ldc,
+              int algo, const DeviceInfo& d, Plan* plan) {
+  const bool vec = aligned16(A) && aligned16(B) && lda % 4 == 0 &&
+                   ldb % 4 == 0;
+  plan->vec = vec;
+  plan->c_vec = aligned16(C) && ldc % 4 == 0;
+  plan->simt_cfg = choose_simt_cfg(M, N, d);
+  switch (algo) {
+    case GEMM_F32_ALGO_AUTO:
+    case GEMM_F32_ALGO_SIMT:
+      plan->algo = GEMM_F32_ALGO_SIMT;
+      return GEMM_F32_OK;
+    case GEMM_F32_ALGO_TMA:
+    case GEMM_F32_ALGO_TF32X3:
+      return GEMM_F32_ERR_UNSUPPORTED;
+    default:
+      return GEMM_F32_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace
+
+namespace gemm_f32_impl {
+
+cudaError_t ensure_smem_attr(const void* fn, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto key = std::make_pair(dev, fn);
+  if (g_smem_attr_done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e == cudaSuccess) g_smem_attr_done.insert(key);
+  return e;
+}
+
+}  // namespace gemm_f32_impl
+
+extern "C" {
+
+int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                const float* B, int64_t ldb, float* C, int64_t ldc,
+                gemm_f32_stream_t stream, int algo) {
+  if (algo < GEMM_F32_ALGO_AUTO || algo > GEMM_F32_ALGO_TF32X3)
+    return GEMM_F32_ERR_INVALID_ARG;
+  int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM_F32_OK) return st;
+  if (M == 0 || N == 0) return GEMM_F32_OK;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  Plan plan;
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, *d, &plan);
+  if (st != GEMM_F32_OK) return st;
+
+  Problem p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (plan.algo) {
+    case GEMM_F32_ALGO_SIMT:
+      e = launch_simt(p, plan.simt_cfg, plan.vec, plan.c_vec, s);
+      break;
+    default:
+      return GEMM_F32_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return fail_cuda(e);
+  return GEMM_F32_OK;
+}
+
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+             const float* B, int64_t ldb, float* C, int64_t ldc,
+             gemm_f32_stream_t stream) {
+  return gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, stream,
+                     GEMM_F32_ALGO_AUTO);
+}
+
+int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float* A,
+                         int64_t lda, const float* B, int64_t ldb, float* C,
+                         int64_t ldc) {
+  int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM_F32_OK) return -st;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) {
+    t_last_cuda_error = static_cast<int>(e);
+    return -GEMM_F32_ERR_CUDA;
+  }
+  Plan plan;
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, GEMM_F32_ALGO_AUTO, *d,
+                 &plan);
+  if (st != GEMM_F32_OK) return -st;
+  return plan.algo;
+}
+
+const char* gemm_f32_status_string(int status) {
+  switch (status) {
+    case GEMM_F32_OK:
+      return "ok";
+    case GEMM_F32_ERR_INVALID_ARG:
+      return "invalid argument";
+    case GEMM_F32_ERR_UNSUPPORTED:
+      return "unsupported: the forced algorithm's preconditions do not hold";
+    case GEMM_F32_ERR_CUDA:
+      return "CUDA runtime error";
+    case GEMM_F32_ERR_TIMEOUT:
+      return "a kernel's bounded wait gave up";
+    default:
+      return "unknown status";
+  }
+}
+
+int gemm_f32_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gemm_f32_device_status(gemm_f32_stream_t stream) {
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail_cuda(e);
+  unsigned int word = 0;
+  if ((e = cudaMemcpyFromSymbol(&word, g_kernel_status, sizeof(word))) !=
+      cudaSuccess)
+    return fail_cuda(e);
+  if (word) {
+    const unsigned int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_kernel_status, &zero, sizeof(zero))) !=
+        cudaSuccess)
+      return fail_cuda(e);
+    return GEMM_F32_ERR_TIMEOUT;
+  }
+  return GEMM_F32_OK;
+}
+
+int64_t gemm_f32_set_wait_limit(int64_t polls) {
+  return g_wait_limit.exchange(polls > 0 ? polls : kDefaultWaitLimit);
+}
+
+int gemm_f32_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// Internal interface between the C-ABI dispatcher (gemm_f32_api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gemm_f32_impl {
+
+// SIMT tile configurations (BM x BN x BK); "Occ1" variants let a thread use
+// up to 255 registers at one CTA per SM instead of 128 at two.
+enum SimtCfg {
+  kSimt128x128x16 = 0,
+  kSimt128x64x16 = 1,
+  kSimt128x128x32 = 2,
+  kSimt64x64x16 = 3,
+  kSimt128x128x16Occ1 = 4,
+  kSimt128x128x8 = 5,
+  kSimt128x128x32Occ1 = 6,
+  kSimtCfgCount = 7
+};
+
+// Sets cudaFuncAttributeMaxDynamicSharedMemorySize for `fn` on the current
+// device once (a launch asking for more than 48 KB fails without it).
+cudaError_t ensure_smem_attr(const void* fn, int bytes);
+
+cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
+                        cudaStream_t stream);
+
+}  // namespace gemm_f32_impl

@@ -1,0 +1,181 @@
+// FP32 GEMM on the FFMA pipe, operands staged by cp.async.
+//
+// One CTA computes a BM×BN tile of C.  The k loop walks BK-deep stages of a
+// STAGES-deep shared-memory ring: while the CTA multiplies stage kt, the
+// copies for stage kt + STAGES − 1 are already in flight.  This replaces
+// the two __syncthreads of "3 · La mémoire partagée", §3.2-§3.3 (one after
+// the cooperative load, one before the tile is overwritten) with a single
+// barrier per stage: it both publishes stage kt and proves every thread has
+// finished reading the stage that the next copies overwrite.
+//
+// Edges ("3 · La mémoire partagée", §3.3 assumes N % T == 0 and the
+// cuda-oxide tiled_sgemm drops the K remainder; here every size is exact):
+// copies of chunks that fall past M, N or K read only the bytes that exist
+// and fill the rest with zeros, and the epilogue stores only elements inside
+// M×N.
+//
+// A is copied one float at a time so it can land transposed (As[BK][BM],
+// as in §3.4 of the same page); B is copied in 16-byte chunks when VEC is
+// true (B 16-byte aligned, ldb a multiple of 4) and one float at a time
+// otherwise, so any alignment and any leading dimension work.
+#include "ffma_tile.cuh"
+#include "kernels.h"
+
+namespace gemm_f32_impl {
+
+template <int BM, int BN, int BK, int STAGES, bool VEC>
+struct SimtKernel {
+  using Tile = FfmaTileT<BM, BN, BK>;
+  static constexpr int kThreads = Tile::kThreads;
+  static constexpr int kSmemBytes = STAGES * Tile::kStageBytes + 1024;
+
+  // Issues this thread's share of the copies for k-stage `kt` into the ring
+  // slot whose A and B parts start at As and Bs.
+  static __device__ __forceinline__ void load_stage(const Problem& p, float* As,
+                                                    float* Bs, int bm, int bn,
+                                                    int kt, int tid) {
+    const int k0 = kt * BK;
+    // A, transposed on the way in: single-float copies, a warp covering 4
+    // rows × 8 consecutive k (whole 32-byte sectors of each row).
+    constexpr int kElemsA = BM * BK;
+#pragma unroll
+    for (int id = tid; id < kElemsA; id += kThreads) {
+      const int kl = id & 7, ml = (id >> 3) & 3, rest = id >> 5;
+      const int k = (rest % (BK / 8)) * 8 + kl;
+      const int m = (rest / (BK / 8)) * 4 + ml;
+      const int gm = bm + m, gk = k0 + k;
+      const bool ok = gm < p.M && gk < p.K;
+      const float* src = ok ? p.A + (long long)gm * p.lda + gk : p.A;
+      cp_async4(smem_u32(As + Tile::a_index(k, m)), src, ok ? 4 : 0);
+    }
+    if (VEC) {
+      constexpr int kChunksB = BK * BN / 4;
+#pragma unroll
+      for (int id = tid; id < kChunksB; id += kThreads) {
+        const int k = id / (BN / 4), c = id % (BN / 4);
+        const int gk = k0 + k, gn = bn + 4 * c;
+        int bytes = 0;
+        const float* src = p.B;
+        if (gk < p.K && gn < p.N) {
+          bytes = 4 * min(4, p.N - gn);
+          src = p.B + (long long)gk * p.ldb + gn;
+        }
+        cp_async16(smem_u32(Bs + k * BN + 4 * c), src, bytes);
+      }
+    } else {
+      constexpr int kElemsB = BK * BN;
+#pragma unroll 4
+      for (int id = tid; id < kElemsB; id += kThreads) {
+        const int k = id / BN, n = id % BN;
+        const int gk = k0 + k, gn = bn + n;
+        const bool ok = gk < p.K && gn < p.N;
+        const float* src = ok ? p.B + (long long)gk * p.ldb + gn : p.B;
+        cp_async4(smem_u32(Bs + k * BN + n), src, ok ? 4 : 0);
+      }
+    }
+  }
+
+  static __device__ __forceinline__ void run(const Problem& p, int tiles_m,
+                                             int tiles_n, int c_vec) {
+    extern __shared__ unsigned char smem_raw[];
+    float* smem = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* As = smem;
+    float* Bs = smem + STAGES * Tile::kStageFloatsA;
+
+    int tm, tn;
+    tile_coords<8>(blockIdx.x, tiles_m, tiles_n, tm, tn);
+    const int bm = tm * BM, bn = tn * BN;
+    const int tid = threadIdx.x;
+
+    Tile tile;
+    tile.init(tid);
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    const int kt_count = (p.K + BK - 1) / BK;
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+      if (s < kt_count)
+        load_stage(p, As + s * Tile::kStageFloatsA, Bs + s * Tile::kStageFloatsB,
+                   bm, bn, s, tid);
+      cp_async_commit();
+    }
+    for (int kt = 0; kt < kt_count; ++kt) {
+      cp_async_wait<STAGES - 2>();
+      __syncthreads();
+      const int next = kt + STAGES - 1;
+      if (next < kt_count) {
+        const int slot = next % STAGES;
+        load_stage(p, As + slot * Tile::kStageFloatsA,
+                   Bs + slot * Tile::kStageFloatsB, bm, bn, next, tid);
+      }
+      cp_async_commit();
+      const int slot = kt % STAGES;
+      tile.compute(As + slot * Tile::kStageFloatsA,
+                   Bs + slot * Tile::kStageFloatsB, acc);
+    }
+    cp_async_wait<0>();
+    tile.store(p, bm, bn, c_vec != 0, acc);
+  }
+};
+
+template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB>
+__global__ void __launch_bounds__(FfmaTileT<BM, BN, BK>::kThreads, MINB)
+    simt_gemm_kernel(Problem p, int tiles_m, int tiles_n, int c_vec) {
+  SimtKernel<BM, BN, BK, STAGES, VEC>::run(p, tiles_m, tiles_n, c_vec);
+}
+
+namespace {
+
+template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB>
+cudaError_t launch_cfg(const Problem& p, bool c_vec, cudaStream_t stream) {
+  using K = SimtKernel<BM, BN, BK, STAGES, VEC>;
+  auto fn = simt_gemm_kernel<BM, BN, BK, STAGES, VEC, MINB>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn),
+                                   K::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
+  const long long grid = (long long)tiles_m * tiles_n;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  fn<<<(unsigned)grid, K::kThreads, K::kSmemBytes, stream>>>(p, tiles_m,
+                                                             tiles_n, c_vec);
+  return cudaGetLastError();
+}
+
+template <bool VEC>
+cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
+                       cudaStream_t stream) {
+  switch (cfg) {
+    case kSimt128x128x16:
+      return launch_cfg<128, 128, 16, 4, VEC, 2>(p, c_vec, stream);
+    case kSimt128x64x16:
+      return launch_cfg<128, 64, 16, 4, VEC, 3>(p, c_vec, stream);
+    case kSimt128x128x32:
+      return launch_cfg<128, 128, 32, 3, VEC, 2>(p, c_vec, stream);
+    case kSimt64x64x16:
+      return launch_cfg<64, 64, 16, 4, VEC, 4>(p, c_vec, stream);
+    case kSimt128x128x16Occ1:
+      return launch_cfg<128, 128, 16, 4, VEC, 1>(p, c_vec, stream);
+    case kSimt128x128x8:
+      return launch_cfg<128, 128, 8, 6, VEC, 2>(p, c_vec, stream);
+    case kSimt128x128x32Occ1:
+      return launch_cfg<128, 128, 32, 4, VEC, 1>(p, c_vec, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+
+cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
+                        cudaStream_t stream) {
+  return vec ? launch_vec<true>(p, cfg, c_vec, stream)
+             : launch_vec<false>(p, cfg, c_vec, stream);
+}
+
+}  // namespace gemm_f32_impl

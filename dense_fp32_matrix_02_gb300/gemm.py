@@ -98,6 +98,8 @@ def _matrix_args(t, name):
     if not t.is_cuda:
         raise ValueError(f"{name} must live on a CUDA device")
     rows, cols = t.shape
+    if t.numel() == 0:
+        return rows, cols, 0, max(cols, 1)
     if cols > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must be row-major (unit column stride)")
     ld = t.stride(0) if rows > 1 else max(cols, 1)

@@ -39,6 +39,12 @@
 extern "C" {
 #endif
 
+#if defined(__GNUC__)
+#define GEMM_F32_API __attribute__((visibility("default")))
+#else
+#define GEMM_F32_API
+#endif
+
 /* A CUDA stream; binary compatible with cudaStream_t / CUstream. */
 typedef struct CUstream_st *gemm_f32_stream_t;
 
@@ -78,26 +84,26 @@ typedef enum {
  * C = A·B.  M, N, K >= 0.  M == 0 or N == 0: returns OK and launches
  * nothing.  K == 0: C[0:M, 0:N] is set to 0 (the empty sum).
  */
-int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+GEMM_F32_API int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
              const float *B, int64_t ldb, float *C, int64_t ldc,
              gemm_f32_stream_t stream);
 
 /* As gemm_f32, with the kernel family forced by `algo` (gemm_f32_algo). */
-int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+GEMM_F32_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                 const float *B, int64_t ldb, float *C, int64_t ldc,
                 gemm_f32_stream_t stream, int algo);
 
 /* The algorithm gemm_f32 with GEMM_F32_ALGO_AUTO would run for these
  * arguments on the current device (no launch).  Negative on bad args. */
-int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float *A,
+GEMM_F32_API int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float *A,
                          int64_t lda, const float *B, int64_t ldb, float *C,
                          int64_t ldc);
 
 /* Static description of a status code. */
-const char *gemm_f32_status_string(int status);
+GEMM_F32_API const char *gemm_f32_status_string(int status);
 
 /* cudaError_t of the most recent GEMM_F32_ERR_CUDA on this host thread. */
-int gemm_f32_last_cuda_error(void);
+GEMM_F32_API int gemm_f32_last_cuda_error(void);
 
 /*
  * Waits for `stream`, then reads and clears the current device's kernel
@@ -105,16 +111,16 @@ int gemm_f32_last_cuda_error(void);
  * bounded mbarrier wait gave up since the last call, or
  * GEMM_F32_ERR_CUDA.  This is the only entry point that synchronizes.
  */
-int gemm_f32_device_status(gemm_f32_stream_t stream);
+GEMM_F32_API int gemm_f32_device_status(gemm_f32_stream_t stream);
 
 /* Test hook: the number of polls after which the pipelined kernels' mbarrier
  * waits give up (0 restores the default).  Returns the previous value.  A
  * kernel that gives up sets the status word and stops the CTA without
  * writing its tile. */
-int64_t gemm_f32_set_wait_limit(int64_t polls);
+GEMM_F32_API int64_t gemm_f32_set_wait_limit(int64_t polls);
 
 /* Library version, major*10000 + minor*100 + patch. */
-int gemm_f32_version(void);
+GEMM_F32_API int gemm_f32_version(void);
 
 #ifdef __cplusplus
 }

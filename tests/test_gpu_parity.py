@@ -1,0 +1,272 @@
+"""GPU parity: every kernel of libgemm_f32 against the float64 oracle.
+
+All calls go through the C ABI (ctypes binding).  Acceptance per element:
+|C - C_ref| <= 1e-5·sqrt(K)·(|A|·|B|)_ij + 1e-30; on small-integer inputs
+the result must equal the oracle bit for bit.  Full-size cases compare
+sampled elements with the oracle one by one and check every row sum of C
+against A·(B·1) computed by the oracle.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_fp32_matrix_02_gb300 import synth
+from helpers import assert_bitexact, assert_within_tolerance
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from dense_fp32_matrix_02_gb300 import gemm as G  # noqa: E402
+
+DEV = torch.device("cuda:0")
+SIMT_CFGS = list(range(7))
+
+
+def _forced(algo, cfg=None):
+    """Context: forces the algorithm and (for SIMT) the tile config."""
+    import contextlib
+    import os
+
+    @contextlib.contextmanager
+    def ctx():
+        old = os.environ.get("GEMM_F32_SIMT_CFG")
+        if cfg is not None:
+            os.environ["GEMM_F32_SIMT_CFG"] = str(cfg)
+        try:
+            yield algo
+        finally:
+            if old is None:
+                os.environ.pop("GEMM_F32_SIMT_CFG", None)
+            else:
+                os.environ["GEMM_F32_SIMT_CFG"] = old
+    return ctx()
+
+
+def run_gpu(a, b, algo=G.ALGO_AUTO, c_fill=float("nan")):
+    ta = torch.from_numpy(a).to(DEV)
+    tb = torch.from_numpy(b).to(DEV)
+    tc = torch.full((a.shape[0], b.shape[1]), c_fill, dtype=torch.float32,
+                    device=DEV)
+    G.gemm_f32_ex(ta, tb, tc, algo=algo)
+    torch.cuda.synchronize()
+    return tc.cpu().numpy()
+
+
+def check_full(a, b, c, exact=False, what=""):
+    ref, bound, _ = oracle.gemm(a, b)
+    if exact:
+        assert_bitexact(c, ref, what)
+    else:
+        assert_within_tolerance(c, ref, bound, a.shape[1], what)
+
+
+def sample_positions(M, N, count=1024, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = list(rng.integers(0, M, count))
+    cols = list(rng.integers(0, N, count))
+    # corners and tile edges
+    for r in {0, M - 1, min(M - 1, 127), min(M - 1, 128), M // 2}:
+        for c in {0, N - 1, min(N - 1, 127), min(N - 1, 128), N // 2}:
+            rows.append(r)
+            cols.append(c)
+    return np.array(rows), np.array(cols)
+
+
+def check_sampled_and_rowsums(a, b, c, exact=False, what=""):
+    M, K = a.shape
+    N = b.shape[1]
+    rows, cols = sample_positions(M, N)
+    ref, bound, _ = oracle.entries(a, b, rows, cols)
+    got = c[rows, cols]
+    if exact:
+        assert_bitexact(got, ref, what + " (sampled)")
+    else:
+        assert_within_tolerance(got, ref, bound, K, what + " (sampled)")
+    # every row: sum_j C[i, j] = (A·(B·1))_i
+    ones = np.ones((N, 1), np.float32)
+    b1, b1bound, _ = oracle.gemm(b, ones)          # exact for these inputs?
+    b1_32 = b1.astype(np.float32)
+    arow, _, _ = oracle.gemm(a, b1_32)
+    absrow, _, _ = oracle.gemm(np.abs(a), b1bound.astype(np.float32))
+    rs = c.astype(np.float64).sum(axis=1)
+    if exact:
+        assert np.array_equal(rs, arow[:, 0]), what + " row sums"
+    else:
+        # rounding B·1 to float32 and summing C in float64 both add a little
+        tol = (1e-5 * np.sqrt(K) + N * 2.0**-52 + 2.0**-23) * absrow[:, 0] \
+            + 1e-30
+        err = np.abs(rs - arow[:, 0])
+        assert (err <= tol).all(), what + f" row sums, worst {err.max():.3e}"
+
+
+# ------------------------------------------------------------- workloads
+SMALL = ["sq64", "sq1024", "rag1000", "skinny"]
+LARGE = ["sq4096", "mlp"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_auto(name):
+    w = synth.WORKLOADS[name]
+    a, b = w.operands()
+    check_full(a, b, run_gpu(a, b), what=name)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_integer_bitexact(name):
+    w = synth.WORKLOADS[name].integer_variant()
+    a, b = w.operands()
+    check_full(a, b, run_gpu(a, b), exact=True, what=w.name)
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_workload_large_sampled(name):
+    w = synth.WORKLOADS[name]
+    a, b = w.operands()
+    check_sampled_and_rowsums(a, b, run_gpu(a, b), what=name)
+
+
+def test_large_integer_bitexact_sampled():
+    w = synth.WORKLOADS["sq4096"].integer_variant()
+    a, b = w.operands()
+    check_sampled_and_rowsums(a, b, run_gpu(a, b), exact=True, what=w.name)
+
+
+# ------------------------------------------------------------- every kernel
+@pytest.mark.parametrize("cfg", SIMT_CFGS)
+@pytest.mark.parametrize("shape", [(64, 64, 64), (1000, 1000, 1000),
+                                   (300, 260, 77), (129, 65, 33)])
+def test_simt_configs(cfg, shape):
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=M + N + K)
+    with _forced(G.ALGO_SIMT, cfg):
+        check_full(a, b, run_gpu(a, b, G.ALGO_SIMT), what=f"simt{cfg}{shape}")
+    ai, bi = synth.make_operands(M, N, K, seed=M + N + K, dist_a="int",
+                                 dist_b="int")
+    with _forced(G.ALGO_SIMT, cfg):
+        check_full(ai, bi, run_gpu(ai, bi, G.ALGO_SIMT), exact=True,
+                   what=f"simt{cfg}{shape} int")
+
+
+# ------------------------------------------------------------- edges
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (2, 3, 5), (17, 13, 11),
+                                   (7, 1, 200), (1, 300, 9), (131, 127, 129),
+                                   (16, 16, 1), (3, 517, 2)])
+def test_small_and_prime_shapes(M, N, K):
+    a, b = synth.make_operands(M, N, K, seed=5)
+    check_full(a, b, run_gpu(a, b), what=f"{M}x{N}x{K}")
+
+
+def test_sweep_1_to_17():
+    for M in (1, 5, 16, 17):
+        for N in range(1, 18):
+            for K in (1, 4, 7, 16, 17):
+                a, b = synth.make_operands(M, N, K, seed=M * 1000 + N * 10 + K,
+                                           dist_a="int", dist_b="int")
+                check_full(a, b, run_gpu(a, b), exact=True,
+                           what=f"{M}x{N}x{K}")
+
+
+def test_k_zero_writes_zeros():
+    a = np.zeros((37, 0), np.float32)
+    b = np.zeros((0, 45), np.float32)
+    c = run_gpu(a, b)
+    assert c.shape == (37, 45) and (c == 0).all()
+
+
+def test_empty_c_is_noop():
+    ta = torch.ones(0, 5, device=DEV)
+    tb = torch.ones(5, 3, device=DEV)
+    tc = torch.empty(0, 3, device=DEV)
+    G.gemm_f32(ta, tb, tc)
+    ta = torch.ones(4, 5, device=DEV)
+    tb = torch.ones(5, 0, device=DEV)
+    G.gemm_f32(ta, tb, torch.empty(4, 0, device=DEV))
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_unaligned_pointers_and_odd_leading_dims(offset):
+    """Operands that start off a 16-byte boundary, with odd strides."""
+    M, N, K = 150, 133, 97
+    a, b = synth.make_operands(M, N, K, seed=offset)
+    lda, ldb, ldc = K + offset, N + 2 * offset + 1, N + 3
+    ta = torch.zeros(M * lda + offset, device=DEV)
+    tb = torch.zeros(K * ldb + offset, device=DEV)
+    tc = torch.full((M * ldc + offset + 64,), 7.0, device=DEV)
+    ta[offset:offset + M * lda].view(M, lda)[:, :K] = torch.from_numpy(a).to(DEV)
+    tb[offset:offset + K * ldb].view(K, ldb)[:, :N] = torch.from_numpy(b).to(DEV)
+    G.gemm_f32_ptr(M, N, K, ta.data_ptr() + 4 * offset, lda,
+                   tb.data_ptr() + 4 * offset, ldb,
+                   tc.data_ptr() + 4 * offset, ldc,
+                   torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    host = tc.cpu().numpy()
+    c = host[offset:offset + M * ldc].reshape(M, ldc)
+    check_full(a, b, c[:, :N], what=f"offset {offset}")
+    # padding columns and the guard region after C are untouched
+    assert (c[:, N:] == 7.0).all()
+    assert (host[:offset] == 7.0).all() and (host[offset + M * ldc:] == 7.0).all()
+
+
+def test_aligned_padded_leading_dims_and_guard():
+    M, N, K = 200, 136, 72
+    a, b = synth.make_operands(M, N, K, seed=9)
+    ldc = 160
+    ta = torch.from_numpy(np.pad(a, ((0, 0), (0, 8)))).to(DEV)[:, :K]
+    tb = torch.from_numpy(np.pad(b, ((0, 0), (0, 24)))).to(DEV)[:, :N]
+    store = torch.full((M + 2, ldc), -3.0, device=DEV)
+    tc = store[:M, :N]
+    G.gemm_f32(ta, tb, tc)
+    torch.cuda.synchronize()
+    host = store.cpu().numpy()
+    check_full(a, b, host[:M, :N], what="padded")
+    assert (host[:M, N:] == -3.0).all() and (host[M:] == -3.0).all()
+
+
+def test_deterministic_repeat():
+    w = synth.WORKLOADS["rag1000"]
+    a, b = w.operands()
+    c1 = run_gpu(a, b)
+    c2 = run_gpu(a, b)
+    assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+
+
+def test_nan_and_inf_propagate():
+    a, b = synth.make_operands(64, 64, 64, seed=3)
+    a[5, 7] = np.nan
+    b[9, 11] = np.inf
+    c = run_gpu(a, b)
+    ref, bound, _ = oracle.gemm(a, b)
+    assert np.array_equal(np.isnan(c), np.isnan(ref))
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isinf(c), np.isinf(ref))
+    assert_within_tolerance(c[fin], ref[fin], bound[fin], 64, "finite part")
+
+
+def test_stream_ordering_on_side_stream():
+    """Work is queued on the given stream, not the default one."""
+    a, b = synth.make_operands(512, 512, 512, seed=1)
+    ta, tb = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        tc = G.gemm_f32(ta, tb)
+    s.synchronize()
+    check_full(a, b, tc.cpu().numpy(), what="side stream")
+
+
+def test_device_status_clean():
+    run_gpu(*synth.make_operands(64, 64, 64, seed=0))
+    assert G.device_status() == 0
+
+
+def test_select_algo_reports_a_kernel():
+    ta = torch.zeros(256, 256, device=DEV)
+    algo = G.select_algo(256, 256, 256, ta.data_ptr(), 256, ta.data_ptr(), 256,
+                         ta.data_ptr(), 256)
+    assert algo in (G.ALGO_SIMT, G.ALGO_TMA, G.ALGO_TF32X3)
