@@ -295,7 +295,7 @@ def run_ours(args, w, config):
     def e2e_step():
         ea.copy_(ha, non_blocking=True)
         eb.copy_(hb, non_blocking=True)
-        G.gemm_f32(ea, eb, ec, stream=stream)
+        G.gemm_f32_ex(ea, eb, ec, algo=algo, stream=stream)
         hc.copy_(ec, non_blocking=True)
 
     for _ in range(3):

@@ -34,7 +34,7 @@ struct Problem {
 
 // Bounded-wait configuration shared by all pipelined kernels.
 struct WaitCfg {
-  long long limit;        // polls before a wait gives up
+  long long limit;        // ns of %globaltimer before a wait gives up
   unsigned int debug;     // kDebug* bits
   unsigned int* status;   // device status word
 };
@@ -116,16 +116,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-// Bounded wait: polls up to `limit` times; false if the phase never came.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
-                                                  uint32_t parity,
-                                                  long long limit) {
-  for (long long i = 0; i < limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-  }
-  return false;
 }
 
 // ---------------------------------------------------------------- TMA

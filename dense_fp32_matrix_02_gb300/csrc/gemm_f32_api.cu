@@ -20,11 +20,11 @@ __device__ unsigned int g_kernel_status;
 
 namespace {
 
-constexpr long long kDefaultWaitLimit = 1LL << 26;
+constexpr long long kDefaultWaitNs = 2000000000LL;  // 2 s
 constexpr int kMaxDevices = 64;
 
 thread_local int t_last_cuda_error = 0;
-std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+std::atomic<long long> g_wait_ns{kDefaultWaitNs};
 std::atomic<unsigned int> g_debug_flags{0};
 
 struct DeviceInfo {
@@ -103,7 +103,7 @@ int choose_simt_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   if (N <= 64) return kSimt128x64x16;
   const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
   if (tiles < d.sm_count) return kSimt128x64x16;
-  return kSimt128x128x16;
+  return kSimt128x128x32Occ1;
 }
 
 // Decides which kernel runs.  Returns a status; fills *plan on success.
@@ -115,13 +115,21 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   plan->vec = vec;
   plan->c_vec = aligned16(C) && ldc % 4 == 0;
   plan->simt_cfg = choose_simt_cfg(M, N, d);
+  const bool tcgen05_ok = d.cc_major == 10 && vec && K >= 1;
   switch (algo) {
     case GEMM_F32_ALGO_AUTO:
+      plan->algo = (tcgen05_ok && env_int("GEMM_F32_AUTO_SIMT", 0) == 0)
+                       ? GEMM_F32_ALGO_TF32X3
+                       : GEMM_F32_ALGO_SIMT;
+      return GEMM_F32_OK;
     case GEMM_F32_ALGO_SIMT:
       plan->algo = GEMM_F32_ALGO_SIMT;
       return GEMM_F32_OK;
-    case GEMM_F32_ALGO_TMA:
     case GEMM_F32_ALGO_TF32X3:
+      if (!tcgen05_ok) return GEMM_F32_ERR_UNSUPPORTED;
+      plan->algo = GEMM_F32_ALGO_TF32X3;
+      return GEMM_F32_OK;
+    case GEMM_F32_ALGO_TMA:
       return GEMM_F32_ERR_UNSUPPORTED;
     default:
       return GEMM_F32_ERR_INVALID_ARG;
@@ -179,6 +187,14 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     case GEMM_F32_ALGO_SIMT:
       e = launch_simt(p, plan.simt_cfg, plan.vec, plan.c_vec, s);
       break;
+    case GEMM_F32_ALGO_TF32X3: {
+      WaitCfg wc;
+      wc.limit = g_wait_ns.load();
+      wc.debug = g_debug_flags.load();
+      wc.status = d->status;
+      e = launch_tf32x3(p, wc, s);
+      break;
+    }
     default:
       return GEMM_F32_ERR_UNSUPPORTED;
   }
@@ -250,8 +266,12 @@ int gemm_f32_device_status(gemm_f32_stream_t stream) {
   return GEMM_F32_OK;
 }
 
-int64_t gemm_f32_set_wait_limit(int64_t polls) {
-  return g_wait_limit.exchange(polls > 0 ? polls : kDefaultWaitLimit);
+int64_t gemm_f32_set_wait_timeout_ns(int64_t ns) {
+  return g_wait_ns.exchange(ns > 0 ? ns : kDefaultWaitNs);
+}
+
+unsigned int gemm_f32_set_debug_flags(unsigned int flags) {
+  return g_debug_flags.exchange(flags);
 }
 
 int gemm_f32_version(void) { return 100; }

@@ -28,4 +28,9 @@ cudaError_t ensure_smem_attr(const void* fn, int bytes);
 cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
                         cudaStream_t stream);
 
+// 3xTF32 tcgen05 kernel.  Needs A, B 16-byte aligned, lda and ldb multiples
+// of 4, K >= 1 and an sm_100-family device.
+cudaError_t launch_tf32x3(const Problem& p, const WaitCfg& wc,
+                          cudaStream_t stream);
+
 }  // namespace gemm_f32_impl

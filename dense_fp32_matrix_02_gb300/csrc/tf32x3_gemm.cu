@@ -1,0 +1,363 @@
+// FP32 GEMM on the tcgen05 tensor cores by three TF32 products per term.
+//
+// The pages' own tensor-core path ("Rendre le GPU rapide", section "Les
+// Tensor Cores") rounds operands to 16 bits and keeps the sums in f32; that
+// cannot hold single-precision accuracy.  Here every fp32 value x is split
+// into big = x rounded to the nearest TF32 value (10 fraction bits; the
+// round-half-to-even by integer add that the same section uses for bf16) and
+// small = x − big, which fp32 holds exactly.  Then
+//     a·b ≈ a_big·b_big + a_big·b_small + a_small·b_big
+// drops only a_small·b_small and the TF32 rounding of small (≈ 2^-21 |a b|
+// per term), far inside the single-precision tolerance, and the sums run in
+// the tensor core's fp32 accumulator in Tensor Memory (TMEM).
+//
+// The kernel computes the tile of C transposed, Cᵀ = Bᵀ·Aᵀ, so that neither
+// operand needs a transpose in shared memory:
+//   * the MMA's A operand is Bᵀ (128 columns of C × k), written into TMEM by
+//     converter threads: TMEM lane n takes column n of the B tile, which the
+//     32 threads of a warp read as contiguous rows of B in shared memory;
+//   * the MMA's B operand is the A tile (256 rows of C × k), K-major as TMA
+//     copies it from row-major A, 64-byte swizzled.
+// The fp32 accumulator D (TMEM lane = column n of C, TMEM column = row m of
+// C) is read back by the same converter warps, whose 32 lanes then store 32
+// consecutive columns of one row of C.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0     TMA producer (one thread): A tile 256×16, B tile 16×128 per
+//              stage into a 5-stage ring, completion counted on full[s];
+//   warp 1     TMEM allocator and MMA issuer (one thread): waits conv[s],
+//              issues 2 k-steps × 3 TF32 MMAs (M=128, N=256, K=8), commits
+//              the stage's release to empty[s];
+//   warps 2-5  converters: split Bᵀ into TMEM and A in shared memory (big
+//              written back in place, small into its own buffer), then the
+//              epilogue.
+// Every mbarrier wait is bounded by a %globaltimer deadline; a wait that
+// runs out sets the status word and a CTA-wide abort flag, the roles drain
+// their copies and MMAs in flight, TMEM is freed, and the CTA ends without
+// writing C.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gemm_f32_impl {
+namespace tf32x3 {
+
+constexpr int kTileM = 256;  // rows of C per CTA = MMA N
+constexpr int kTileN = 128;  // columns of C per CTA = MMA M = TMEM lanes
+constexpr int kBK = 16;      // k per stage: 64-byte rows
+constexpr int kStages = 5;
+constexpr int kThreads = 192;
+constexpr int kAccCols = kTileM;  // TMEM columns of the accumulator
+constexpr int kTmemCols = 512;
+constexpr int kStageBytesA = kTileM * kBK * 4;  // 16 KB
+constexpr int kStageBytesB = kBK * kTileN * 4;  // 8 KB
+constexpr uint32_t kIdesc = idesc_tf32(kTileN, kTileM);
+constexpr long long kDrainNs = 2000000000LL;
+
+static_assert(kAccCols + kStages * 2 * kBK <= kTmemCols, "TMEM budget");
+
+struct __align__(8) Control {
+  uint64_t full[kStages];   // TMA -> converters (tx bytes)
+  uint64_t conv[kStages];   // converters -> MMA (4 warp arrivals)
+  uint64_t empty[kStages];  // MMA completion -> producer
+  uint64_t accum;           // last MMA completion -> epilogue
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr int kOffASmall = kStages * kStageBytesA;
+constexpr int kOffB = 2 * kStages * kStageBytesA;
+constexpr int kOffCtl = kOffB + kStages * kStageBytesB;
+constexpr int kSmemBytes = kOffCtl + (int)sizeof(Control) + 1024;
+
+// Rounds x to the nearest TF32 value (ties to even) and returns the exact
+// remainder.  Exact values (and ±Inf) give small = 0; NaN stays NaN.
+__device__ __forceinline__ void tf32_split(float x, uint32_t& big,
+                                           uint32_t& small) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t b = (u + 0xFFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
+  const float bf = __uint_as_float(b);
+  const float s = (bf == x) ? 0.0f : __fsub_rn(x, bf);
+  big = b;
+  small = __float_as_uint(s);
+}
+
+// Bounded wait on one phase of an mbarrier.  Gives up (false) when the CTA
+// abort flag is raised or `limit_ns` of %globaltimer time pass.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           long long limit_ns,
+                                           volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (abort && *abort) return false;
+      if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
+    }
+  }
+}
+
+// The same for all 32 lanes of a warp: every lane waits, and the warp goes
+// on only if all of them saw the phase (tcgen05.ld/st need the whole warp).
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
+                                                long long limit_ns,
+                                                volatile int* abort) {
+  const bool ok = wait_phase(bar, parity, limit_ns, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                       const __grid_constant__ CUtensorMap tmap_b, float* C,
+                       long long ldc, int M, int N, int K, int tiles_m,
+                       int tiles_n, WaitCfg wc) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Control* ctl = reinterpret_cast<Control*>(smem + kOffCtl);
+  volatile int* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int tm, tn;
+  tile_coords<8>(blockIdx.x, tiles_m, tiles_n, tm, tn);
+  const int bm = tm * kTileM, bn = tn * kTileN;
+  const int nk = (K + kBK - 1) / kBK;
+
+  auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
+  auto conv = [&](int s) { return smem_u32(&ctl->conv[s]); };
+  auto empty = [&](int s) { return smem_u32(&ctl->empty[s]); };
+  const uint32_t accum = smem_u32(&ctl->accum);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(conv(s), 4);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(accum, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      if (!(wc.debug & kDebugStallProducer)) {
+        for (int kb = 0; kb < nk; ++kb) {
+          const int s = kb % kStages;
+          const uint32_t use = kb / kStages;
+          if (kb >= kStages &&
+              !wait_phase(empty(s), (use - 1) & 1, wc.limit, abort)) {
+            *abort = 1;
+            record_status(wc.status, kStatusTimeoutEmpty);
+            break;
+          }
+          mbar_arrive_expect_tx(full(s), kStageBytesA + kStageBytesB);
+          tma_load_2d(sbase + s * kStageBytesA, &tmap_a, full(s), kb * kBK,
+                      bm);
+          tma_load_2d(sbase + kOffB + s * kStageBytesB, &tmap_b, full(s), bn,
+                      kb * kBK);
+          ++issued;
+        }
+      }
+      if (*abort) {  // let the copies still in flight land before leaving
+        for (int kb = issued > kStages ? issued - kStages : 0; kb < issued;
+             ++kb) {
+          if (!wait_phase(full(kb % kStages), (kb / kStages) & 1, kDrainNs,
+                          nullptr))
+            record_status(wc.status, kStatusTimeoutDrain);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages;
+        if (!wait_phase(conv(s), (kb / kStages) & 1, wc.limit, abort)) {
+          *abort = 1;
+          record_status(wc.status, kStatusTimeoutFull);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t bt_big = tmem + kAccCols + s * 2 * kBK;
+        const uint32_t bt_small = bt_big + kBK;
+        const uint32_t a_big = sbase + s * kStageBytesA;
+        const uint32_t a_small = sbase + kOffASmall + s * kStageBytesA;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 8; ++kk) {
+          const uint64_t d_big = smem_desc_kmajor_sw64(a_big + 32 * kk);
+          const uint64_t d_small = smem_desc_kmajor_sw64(a_small + 32 * kk);
+          mma_tf32_ts(tmem, bt_small + 8 * kk, d_big, kIdesc,
+                      (kb | kk) != 0);
+          mma_tf32_ts(tmem, bt_big + 8 * kk, d_small, kIdesc, 1);
+          mma_tf32_ts(tmem, bt_big + 8 * kk, d_big, kIdesc, 1);
+        }
+        tc_commit(empty(s));
+      }
+      tc_commit(accum);
+      // no MMA may still run when TMEM is freed at the end
+      if (!wait_phase(accum, 0, kDrainNs, nullptr))
+        record_status(wc.status, kStatusTimeoutDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ converters
+    const int q = warp & 3;           // TMEM lane quarter of this warp
+    const int n_loc = q * 32 + lane;  // column of the C tile = TMEM lane
+    const int t = threadIdx.x - 64;   // 0..127
+    const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages;
+      if (!warp_wait_phase(full(s), (kb / kStages) & 1, wc.limit, abort)) {
+        *abort = 1;
+        if (lane == 0) record_status(wc.status, kStatusTimeoutFull);
+        ok = false;
+        break;
+      }
+      // Bᵀ: column n_loc of the B tile (k rows) -> TMEM lane n_loc
+      const float* bcol =
+          reinterpret_cast<const float*>(smem + kOffB + s * kStageBytesB) +
+          n_loc;
+      uint32_t big[kBK], small[kBK];
+#pragma unroll
+      for (int k = 0; k < kBK; ++k) tf32_split(bcol[k * kTileN], big[k], small[k]);
+      const uint32_t tcol = tmem + lane_bits + kAccCols + s * 2 * kBK;
+      tmem_st16(tcol, big);
+      tmem_st16(tcol + kBK, small);
+      // A: element-wise, position for position (the swizzle is untouched)
+      float4* araw = reinterpret_cast<float4*>(smem + s * kStageBytesA);
+      float4* asml =
+          reinterpret_cast<float4*>(smem + kOffASmall + s * kStageBytesA);
+#pragma unroll
+      for (int j = 0; j < kStageBytesA / 16 / 128; ++j) {
+        const int c = t + 128 * j;
+        const float4 v = araw[c];
+        uint32_t b0, b1, b2, b3, s0, s1, s2, s3;
+        tf32_split(v.x, b0, s0);
+        tf32_split(v.y, b1, s1);
+        tf32_split(v.z, b2, s2);
+        tf32_split(v.w, b3, s3);
+        araw[c] = make_float4(__uint_as_float(b0), __uint_as_float(b1),
+                              __uint_as_float(b2), __uint_as_float(b3));
+        asml[c] = make_float4(__uint_as_float(s0), __uint_as_float(s1),
+                              __uint_as_float(s2), __uint_as_float(s3));
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(conv(s));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (__all_sync(0xffffffffu, ok && !*abort)) {
+      if (!warp_wait_phase(accum, 0, wc.limit, abort)) {
+        *abort = 1;
+        if (lane == 0) record_status(wc.status, kStatusTimeoutMma);
+      } else {
+        tc_fence_after_sync();
+        const int n = bn + n_loc;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kAccCols; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_bits + c0, v);
+          tmem_ld_wait();
+          if (n < N) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int m = bm + c0 + i;
+              if (m < M) C[(long long)m * ldc + n] = __uint_as_float(v[i]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace tf32x3
+
+cudaError_t launch_tf32x3(const Problem& p, const WaitCfg& wc,
+                          cudaStream_t stream) {
+  using namespace tf32x3;
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.lda * 4};
+    const cuuint32_t box[2] = {kBK, kTileM};
+    if (encode(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<float*>(p.A), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.K};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.ldb * 4};
+    const cuuint32_t box[2] = {kTileN, kBK};
+    if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<float*>(p.B), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = ensure_smem_attr(
+      reinterpret_cast<const void*>(tf32x3_gemm_kernel), kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int tiles_m = (p.M + kTileM - 1) / kTileM;
+  const int tiles_n = (p.N + kTileN - 1) / kTileN;
+  const long long grid = (long long)tiles_m * tiles_n;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  tf32x3_gemm_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(
+      ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, wc);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm_f32_impl

@@ -59,8 +59,10 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_last_cuda_error.argtypes = []
         L.gemm_f32_device_status.restype = ci
         L.gemm_f32_device_status.argtypes = [vp]
-        L.gemm_f32_set_wait_limit.restype = i64
-        L.gemm_f32_set_wait_limit.argtypes = [i64]
+        L.gemm_f32_set_wait_timeout_ns.restype = i64
+        L.gemm_f32_set_wait_timeout_ns.argtypes = [i64]
+        L.gemm_f32_set_debug_flags.restype = ctypes.c_uint
+        L.gemm_f32_set_debug_flags.argtypes = [ctypes.c_uint]
         L.gemm_f32_version.restype = ci
         L.gemm_f32_version.argtypes = []
         _lib = L
@@ -102,8 +104,9 @@ def _matrix_args(t, name):
         return rows, cols, 0, max(cols, 1)
     if cols > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must be row-major (unit column stride)")
-    ld = t.stride(0) if rows > 1 else max(cols, 1)
-    return rows, cols, t.data_ptr() if t.numel() else 0, max(ld, cols)
+    # a single row has no meaningful row stride unless it spans the width
+    ld = t.stride(0) if (rows > 1 or t.stride(0) >= cols) else cols
+    return rows, cols, t.data_ptr(), max(ld, cols, 1)
 
 
 def gemm_f32_ex(a, b, c=None, algo=ALGO_AUTO, stream=None):
@@ -151,8 +154,15 @@ def device_status(stream=None) -> int:
     return int(lib().gemm_f32_device_status(handle or None))
 
 
-def set_wait_limit(polls: int) -> int:
-    return int(lib().gemm_f32_set_wait_limit(int(polls)))
+def set_wait_timeout_ns(ns: int) -> int:
+    return int(lib().gemm_f32_set_wait_timeout_ns(int(ns)))
+
+
+def set_debug_flags(flags: int) -> int:
+    return int(lib().gemm_f32_set_debug_flags(int(flags)))
+
+
+DEBUG_STALL_PRODUCER = 1
 
 
 def version() -> int:

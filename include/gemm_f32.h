@@ -113,11 +113,19 @@ GEMM_F32_API int gemm_f32_last_cuda_error(void);
  */
 GEMM_F32_API int gemm_f32_device_status(gemm_f32_stream_t stream);
 
-/* Test hook: the number of polls after which the pipelined kernels' mbarrier
- * waits give up (0 restores the default).  Returns the previous value.  A
- * kernel that gives up sets the status word and stops the CTA without
- * writing its tile. */
-GEMM_F32_API int64_t gemm_f32_set_wait_limit(int64_t polls);
+/* The deadline, in nanoseconds of the GPU's global timer, after which an
+ * mbarrier wait in the pipelined kernels gives up (<= 0 restores the
+ * default of 2 s).  Applies to later launches; returns the previous value.
+ * A kernel that gives up sets the status word read by
+ * gemm_f32_device_status, releases what it holds and ends without writing
+ * its tile of C.  Process-wide setting. */
+GEMM_F32_API int64_t gemm_f32_set_wait_timeout_ns(int64_t ns);
+
+/* Test hook, process-wide, for later launches: bit 0 makes the copy
+ * producer of the pipelined kernels issue no copies, so that their waits run
+ * out and the timeout path can be checked.  0 (the default) disables every
+ * hook.  Returns the previous flags. */
+GEMM_F32_API unsigned int gemm_f32_set_debug_flags(unsigned int flags);
 
 /* Library version, major*10000 + minor*100 + patch. */
 GEMM_F32_API int gemm_f32_version(void);

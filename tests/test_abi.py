@@ -86,11 +86,13 @@ def test_argument_checks_need_no_gpu(built_lib):
         gemm.gemm_f32_ptr(-1, 1, 1, 8, 1, 8, 1, 8, 1)
 
 
-def test_wait_limit_roundtrip(built_lib):
+def test_test_hooks_roundtrip(built_lib):
     from dense_fp32_matrix_02_gb300 import gemm
-    old = gemm.set_wait_limit(1000)
-    assert gemm.set_wait_limit(0) == 1000
-    assert gemm.set_wait_limit(old) > 0
+    old = gemm.set_wait_timeout_ns(1000)
+    assert gemm.set_wait_timeout_ns(0) == 1000
+    assert gemm.set_wait_timeout_ns(old) == 2_000_000_000
+    assert gemm.set_debug_flags(1) == 0
+    assert gemm.set_debug_flags(0) == 1
 
 
 def test_binding_rejects_bad_tensors(built_lib):

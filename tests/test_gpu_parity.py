@@ -48,11 +48,26 @@ def _forced(algo, cfg=None):
     return ctx()
 
 
-def run_gpu(a, b, algo=G.ALGO_AUTO, c_fill=float("nan")):
-    ta = torch.from_numpy(a).to(DEV)
-    tb = torch.from_numpy(b).to(DEV)
-    tc = torch.full((a.shape[0], b.shape[1]), c_fill, dtype=torch.float32,
-                    device=DEV)
+def _padded(x):
+    """Device copy of x whose row stride is a multiple of 4 elements."""
+    rows, cols = x.shape
+    ld = max(4, (cols + 3) // 4 * 4)
+    store = torch.zeros(max(rows, 1), ld, device=DEV)
+    store[:rows, :cols] = torch.from_numpy(x).to(DEV)
+    return store[:rows, :cols]
+
+
+def run_gpu(a, b, algo=G.ALGO_AUTO, c_fill=float("nan"), pad=False):
+    """C = A·B on the GPU; pad=True gives every matrix a row stride that is
+    a multiple of 4 (what the TMA-fed kernels need) whatever its width."""
+    if pad:
+        ta, tb = _padded(a), _padded(b)
+        tc = _padded(np.full((a.shape[0], b.shape[1]), c_fill, np.float32))
+    else:
+        ta = torch.from_numpy(a).to(DEV)
+        tb = torch.from_numpy(b).to(DEV)
+        tc = torch.full((a.shape[0], b.shape[1]), c_fill, dtype=torch.float32,
+                        device=DEV)
     G.gemm_f32_ex(ta, tb, tc, algo=algo)
     torch.cuda.synchronize()
     return tc.cpu().numpy()
@@ -237,15 +252,31 @@ def test_deterministic_repeat():
     assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
 
 
-def test_nan_and_inf_propagate():
+def test_nan_and_inf_propagate_simt():
+    """The FFMA kernel follows IEEE arithmetic for NaN and Inf inputs."""
     a, b = synth.make_operands(64, 64, 64, seed=3)
     a[5, 7] = np.nan
     b[9, 11] = np.inf
-    c = run_gpu(a, b)
+    c = run_gpu(a, b, G.ALGO_SIMT)
     ref, bound, _ = oracle.gemm(a, b)
     assert np.array_equal(np.isnan(c), np.isnan(ref))
     fin = np.isfinite(ref)
     assert np.array_equal(np.isinf(c), np.isinf(ref))
+    assert_within_tolerance(c[fin], ref[fin], bound[fin], 64, "finite part")
+
+
+def test_nan_and_inf_tf32x3():
+    """3xTF32: NaN propagates; an Inf input makes its outputs non-finite
+    (NaN where IEEE gives ±Inf, from Inf·0 in a cross term); the outputs
+    that no non-finite input reaches stay within tolerance."""
+    a, b = synth.make_operands(64, 64, 64, seed=3)
+    a[5, 7] = np.nan
+    b[9, 11] = np.inf
+    c = run_gpu(a, b, G.ALGO_TF32X3)
+    ref, bound, _ = oracle.gemm(a, b)
+    assert np.array_equal(np.isfinite(c), np.isfinite(ref))
+    assert np.isnan(c[np.isnan(ref)]).all()
+    fin = np.isfinite(ref)
     assert_within_tolerance(c[fin], ref[fin], bound[fin], 64, "finite part")
 
 
@@ -267,6 +298,69 @@ def test_device_status_clean():
 
 def test_select_algo_reports_a_kernel():
     ta = torch.zeros(256, 256, device=DEV)
-    algo = G.select_algo(256, 256, 256, ta.data_ptr(), 256, ta.data_ptr(), 256,
-                         ta.data_ptr(), 256)
-    assert algo in (G.ALGO_SIMT, G.ALGO_TMA, G.ALGO_TF32X3)
+    p = ta.data_ptr()
+    assert G.select_algo(256, 256, 256, p, 256, p, 256, p, 256) == G.ALGO_TF32X3
+    # misaligned operand or odd leading dimension: the FFMA kernel
+    assert G.select_algo(256, 256, 256, p + 4, 256, p, 256, p, 256) == \
+        G.ALGO_SIMT
+    assert G.select_algo(256, 255, 256, p, 256, p, 255, p, 255) == G.ALGO_SIMT
+    # K = 0 is a zero fill, done by the FFMA kernel
+    assert G.select_algo(256, 256, 0, p, 0, p, 256, p, 256) == G.ALGO_SIMT
+
+
+# ------------------------------------------------------------- 3xTF32
+@pytest.mark.parametrize("shape", [(128, 128, 16), (256, 128, 32),
+                                   (64, 64, 64), (1000, 1000, 1000),
+                                   (300, 260, 77), (129, 65, 33),
+                                   (517, 3, 260), (8, 1000, 8), (1, 1, 1)])
+def test_tf32x3_shapes(shape):
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=M * 3 + N * 5 + K)
+    check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
+               what=f"tf32x3{shape}")
+    ai, bi = synth.make_operands(M, N, K, seed=M + N + K, dist_a="int",
+                                 dist_b="int")
+    check_full(ai, bi, run_gpu(ai, bi, G.ALGO_TF32X3, pad=True), exact=True,
+               what=f"tf32x3{shape} int")
+    assert G.device_status() == 0
+
+
+def test_tf32x3_wide_dynamic_range():
+    """Operands spanning many binades keep the per-element tolerance."""
+    rng = np.random.default_rng(17)
+    M, N, K = 200, 190, 300
+    a = (rng.standard_normal((M, K)) * 2.0 ** rng.integers(-20, 20, (M, K))
+         ).astype(np.float32)
+    b = (rng.standard_normal((K, N)) * 2.0 ** rng.integers(-20, 20, (K, N))
+         ).astype(np.float32)
+    check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
+               what="wide range")
+
+
+def test_tf32x3_unsupported_when_misaligned():
+    ta = torch.zeros(64 * 64 + 1, device=DEV)
+    p = ta.data_ptr()
+    with pytest.raises(G.GemmError) as e:
+        G.gemm_f32_ptr(8, 8, 8, p + 4, 8, p, 8, p, 8, 0, G.ALGO_TF32X3)
+    assert e.value.status == 2
+    with pytest.raises(G.GemmError):
+        G.gemm_f32_ptr(8, 7, 8, p, 8, p, 7, p, 7, 0, G.ALGO_TF32X3)
+
+
+def test_tf32x3_timeout_path_reports_and_recovers():
+    """A producer that issues no copies makes every wait run out: the
+    kernel frees TMEM, leaves, and the status word says TIMEOUT; the next
+    call works."""
+    a, b = synth.make_operands(300, 200, 100, seed=2)
+    old_t = G.set_wait_timeout_ns(2_000_000)
+    old_f = G.set_debug_flags(G.DEBUG_STALL_PRODUCER)
+    try:
+        run_gpu(a, b, G.ALGO_TF32X3, pad=True)
+        assert G.device_status() == 4
+    finally:
+        G.set_debug_flags(old_f)
+        G.set_wait_timeout_ns(old_t)
+    assert G.device_status() == 0
+    check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
+               what="after timeout")
+    assert G.device_status() == 0
