@@ -62,27 +62,34 @@ def load_peaks():
             "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, "fallback"
 
 
-def kernel_source_hash():
+# sources each kernel is built from (its counters go stale when one changes)
+KERNEL_SOURCES = {
+    "tf32x3": ["tf32x3_gemm.cu", "tcgen05.cuh", "common.cuh", "kernels.h"],
+    "simt": ["simt_gemm.cu", "ffma_tile.cuh", "common.cuh", "kernels.h"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp32_matrix_02_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES.get(kernel, []):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, if it was taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel_key)
+            rec = json.load(f).get(f"{kernel}:{workload}")
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -336,7 +343,7 @@ def run_ours(args, w, config):
                 "unit": "TFLOP/s", "frac": achieved / fp32_peak,
                 "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes "
                                f"x 2 flop x {smax:.0f} MHz (max SM clock)"}
-    roof["traffic"] = recorded_traffic(f"{algo_name}:{w.name}")
+    roof["traffic"] = recorded_traffic(algo_name, w.name)
     roof["algorithmic_bytes"] = w.bytes
     roof["kernel_ms"] = kernel_ms
 

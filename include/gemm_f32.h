@@ -70,13 +70,16 @@ typedef enum {
      * multi-stage swizzled shared-memory ring.  Any pointer alignment and
      * any leading dimension. */
     GEMM_F32_ALGO_SIMT = 1,
-    /* FP32 FFMA register-tiled kernel fed by a TMA producer warp through an
-     * mbarrier full/empty ring.  Needs A and B 16-byte aligned and lda, ldb
-     * multiples of 4. */
+    /* Reserved for an FP32 FFMA kernel fed by a TMA producer warp through an
+     * mbarrier full/empty ring; this version returns
+     * GEMM_F32_ERR_UNSUPPORTED for it. */
     GEMM_F32_ALGO_TMA = 2,
     /* Tensor-core kernel (tcgen05, TMEM accumulator) computing each product
      * as three TF32 products of a big/small operand split, accumulated in
-     * fp32.  Same alignment needs as GEMM_F32_ALGO_TMA. */
+     * fp32; within the single-precision tolerance for finite inputs (an Inf
+     * input may yield NaN where IEEE arithmetic gives ±Inf).  Needs A and B
+     * 16-byte aligned, lda and ldb multiples of 4, K >= 1 and an sm_10x GPU.
+     * GEMM_F32_ALGO_AUTO picks it whenever these hold. */
     GEMM_F32_ALGO_TF32X3 = 3
 } gemm_f32_algo;
 
