@@ -22,15 +22,18 @@
 // C) is read back by the same converter warps, whose 32 lanes then store 32
 // consecutive columns of one row of C.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (320 threads, one CTA per SM):
 //   warp 0     TMA producer (one thread): A tile 256×16, B tile 16×128 per
 //              stage into a 5-stage ring, completion counted on full[s];
 //   warp 1     TMEM allocator and MMA issuer (one thread): waits conv[s],
 //              issues 2 k-steps × 3 TF32 MMAs (M=128, N=256, K=8), commits
 //              the stage's release to empty[s];
-//   warps 2-5  converters: split Bᵀ into TMEM and A in shared memory (big
-//              written back in place, small into its own buffer), then the
-//              epilogue.
+//   warps 2-9  converters, two per TMEM lane quarter (a warp may only touch
+//              the 32 lanes of quarter warp % 4): each splits half of the
+//              stage's k range of Bᵀ into TMEM and a quarter of the A tile
+//              in shared memory (big written back in place, small into its
+//              own buffer), then stores half of its quarter's columns of D
+//              in the epilogue.
 // Every mbarrier wait is bounded by a %globaltimer deadline; a wait that
 // runs out sets the status word and a CTA-wide abort flag, the roles drain
 // their copies and MMAs in flight, TMEM is freed, and the CTA ends without
@@ -50,7 +53,8 @@ constexpr int kTileM = 256;  // rows of C per CTA = MMA N
 constexpr int kTileN = 128;  // columns of C per CTA = MMA M = TMEM lanes
 constexpr int kBK = 16;      // k per stage: 64-byte rows
 constexpr int kStages = 5;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kConvWarps = 8;
 constexpr int kAccCols = kTileM;  // TMEM columns of the accumulator
 constexpr int kTmemCols = 512;
 constexpr int kStageBytesA = kTileM * kBK * 4;  // 16 KB
@@ -62,7 +66,7 @@ static_assert(kAccCols + kStages * 2 * kBK <= kTmemCols, "TMEM budget");
 
 struct __align__(8) Control {
   uint64_t full[kStages];   // TMA -> converters (tx bytes)
-  uint64_t conv[kStages];   // converters -> MMA (4 warp arrivals)
+  uint64_t conv[kStages];   // converters -> MMA (one arrival per warp)
   uint64_t empty[kStages];  // MMA completion -> producer
   uint64_t accum;           // last MMA completion -> epilogue
   uint32_t tmem_base;
@@ -75,15 +79,14 @@ constexpr int kOffCtl = kOffB + kStages * kStageBytesB;
 constexpr int kSmemBytes = kOffCtl + (int)sizeof(Control) + 1024;
 
 // Rounds x to the nearest TF32 value (ties to even) and returns the exact
-// remainder.  Exact values (and ±Inf) give small = 0; NaN stays NaN.
+// remainder x - big.  Values TF32 holds exactly give small = 0; NaN stays
+// NaN; ±Inf gives small = NaN (so an Inf input yields non-finite outputs).
 __device__ __forceinline__ void tf32_split(float x, uint32_t& big,
                                            uint32_t& small) {
   const uint32_t u = __float_as_uint(x);
   const uint32_t b = (u + 0xFFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
-  const float bf = __uint_as_float(b);
-  const float s = (bf == x) ? 0.0f : __fsub_rn(x, bf);
   big = b;
-  small = __float_as_uint(s);
+  small = __float_as_uint(__fsub_rn(x, __uint_as_float(b)));
 }
 
 // Bounded wait on one phase of an mbarrier.  Gives up (false) when the CTA
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(conv(s), 4);
+      mbar_init(conv(s), kConvWarps);
       mbar_init(empty(s), 1);
     }
     mbar_init(accum, 1);
@@ -222,8 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ converters
     const int q = warp & 3;           // TMEM lane quarter of this warp
+    const int h = (warp - 2) >> 2;    // which half of k (Bᵀ) / of D columns
     const int n_loc = q * 32 + lane;  // column of the C tile = TMEM lane
-    const int t = threadIdx.x - 64;   // 0..127
+    const int t = threadIdx.x - 64;   // 0..255
     const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
     bool ok = true;
     for (int kb = 0; kb < nk; ++kb) {
@@ -234,23 +238,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      // Bᵀ: column n_loc of the B tile (k rows) -> TMEM lane n_loc
+      // Bᵀ: column n_loc of the B tile, k in [8h, 8h + 8) -> TMEM lane n_loc
       const float* bcol =
           reinterpret_cast<const float*>(smem + kOffB + s * kStageBytesB) +
-          n_loc;
-      uint32_t big[kBK], small[kBK];
+          n_loc + 8 * h * kTileN;
+      uint32_t big[8], small[8];
 #pragma unroll
-      for (int k = 0; k < kBK; ++k) tf32_split(bcol[k * kTileN], big[k], small[k]);
-      const uint32_t tcol = tmem + lane_bits + kAccCols + s * 2 * kBK;
-      tmem_st16(tcol, big);
-      tmem_st16(tcol + kBK, small);
+      for (int k = 0; k < 8; ++k) tf32_split(bcol[k * kTileN], big[k], small[k]);
+      const uint32_t tcol = tmem + lane_bits + kAccCols + s * 2 * kBK + 8 * h;
+      tmem_st8(tcol, big);
+      tmem_st8(tcol + kBK, small);
       // A: element-wise, position for position (the swizzle is untouched)
       float4* araw = reinterpret_cast<float4*>(smem + s * kStageBytesA);
       float4* asml =
           reinterpret_cast<float4*>(smem + kOffASmall + s * kStageBytesA);
 #pragma unroll
-      for (int j = 0; j < kStageBytesA / 16 / 128; ++j) {
-        const int c = t + 128 * j;
+      for (int j = 0; j < kStageBytesA / 16 / (32 * kConvWarps); ++j) {
+        const int c = t + 32 * kConvWarps * j;
         const float4 v = araw[c];
         uint32_t b0, b1, b2, b3, s0, s1, s2, s3;
         tf32_split(v.x, b0, s0);
@@ -276,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         tc_fence_after_sync();
         const int n = bn + n_loc;
+        const int c_begin = h * (kAccCols / 2);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kAccCols; c0 += 16) {
+        for (int c0 = c_begin; c0 < c_begin + kAccCols / 2; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tmem + lane_bits + c0, v);
           tmem_ld_wait();
