@@ -80,6 +80,7 @@ int env_int(const char* name, int fallback) {
 struct Plan {
   int algo;      // gemm_f32_algo actually run
   int simt_cfg;  // for ALGO_SIMT
+  int tc_cfg;    // for ALGO_TF32X3
   bool vec;      // 16-byte operand copies
   bool c_vec;    // 16-byte C stores
 };
@@ -106,6 +107,18 @@ int choose_simt_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   return kSimt128x128x32Occ1;
 }
 
+int choose_tc_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
+  const int forced = env_int("GEMM_F32_TC_CFG", -1);
+  if (forced >= 0 && forced < kTcCfgCount) return forced;
+  (void)M;
+  (void)N;
+  (void)d;
+  // 128 x 128 tiles at two CTAs per SM beat 256 x 128 at one on every
+  // measured shape (finer scheduling grain, one CTA's epilogue overlapping
+  // the other's main loop).
+  return kTc128;
+}
+
 // Decides which kernel runs.  Returns a status; fills *plan on success.
 int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
               const float* B, int64_t ldb, const float* C, int64_t ldc,
@@ -115,6 +128,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   plan->vec = vec;
   plan->c_vec = aligned16(C) && ldc % 4 == 0;
   plan->simt_cfg = choose_simt_cfg(M, N, d);
+  plan->tc_cfg = choose_tc_cfg(M, N, d);
   const bool tcgen05_ok = d.cc_major == 10 && vec && K >= 1;
   switch (algo) {
     case GEMM_F32_ALGO_AUTO:
@@ -192,7 +206,7 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       wc.limit = g_wait_ns.load();
       wc.debug = g_debug_flags.load();
       wc.status = d->status;
-      e = launch_tf32x3(p, wc, s);
+      e = launch_tf32x3(p, plan.tc_cfg, wc, s);
       break;
     }
     default:

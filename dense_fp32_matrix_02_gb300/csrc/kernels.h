@@ -28,9 +28,14 @@ cudaError_t ensure_smem_attr(const void* fn, int bytes);
 cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
                         cudaStream_t stream);
 
+// 3xTF32 tcgen05 kernel configurations: 256 x 128 tiles at one CTA per SM,
+// or 128 x 128 tiles at two.
+enum TcCfg { kTc256 = 0, kTc128 = 1, kTcCfgCount = 2 };
+int tf32x3_tile_m(int cfg);
+
 // 3xTF32 tcgen05 kernel.  Needs A, B 16-byte aligned, lda and ldb multiples
 // of 4, K >= 1 and an sm_100-family device.
-cudaError_t launch_tf32x3(const Problem& p, const WaitCfg& wc,
+cudaError_t launch_tf32x3(const Problem& p, int cfg, const WaitCfg& wc,
                           cudaStream_t stream);
 
 }  // namespace gemm_f32_impl

@@ -49,34 +49,47 @@
 namespace gemm_f32_impl {
 namespace tf32x3 {
 
-constexpr int kTileM = 256;  // rows of C per CTA = MMA N
-constexpr int kTileN = 128;  // columns of C per CTA = MMA M = TMEM lanes
-constexpr int kBK = 16;      // k per stage: 64-byte rows
-constexpr int kStages = 5;
-constexpr int kThreads = 320;
-constexpr int kConvWarps = 8;
-constexpr int kAccCols = kTileM;  // TMEM columns of the accumulator
-constexpr int kTmemCols = 512;
-constexpr int kStageBytesA = kTileM * kBK * 4;  // 16 KB
-constexpr int kStageBytesB = kBK * kTileN * 4;  // 8 KB
-constexpr uint32_t kIdesc = idesc_tf32(kTileN, kTileM);
+// Tile configuration.  TILE_M rows of C per CTA (the MMA's N), always 128
+// columns (the MMA's M = TMEM lanes), STAGES-deep ring of 16-deep k stages.
+template <int TILE_M, int STAGES>
+struct Cfg {
+  static constexpr int kTileM = TILE_M;
+  static constexpr int kTileN = 128;
+  static constexpr int kBK = 16;  // k per stage: 64-byte rows
+  static constexpr int kStages = STAGES;
+  static constexpr int kThreads = 320;
+  static constexpr int kConvWarps = 8;
+  static constexpr int kAccCols = kTileM;  // TMEM columns of the accumulator
+  static constexpr int kTmemNeed = kAccCols + kStages * 2 * kBK;
+  static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kStageBytesA = kTileM * kBK * 4;
+  static constexpr int kStageBytesB = kBK * kTileN * 4;
+  static constexpr uint32_t kIdesc = idesc_tf32(kTileN, kTileM);
+  static constexpr int kOffASmall = kStages * kStageBytesA;
+  static constexpr int kOffB = 2 * kStages * kStageBytesA;
+  static constexpr int kOffCtl = kOffB + kStages * kStageBytesB;
+  static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
+  static_assert(kTmemNeed <= kTmemCols, "TMEM budget");
+  static_assert(TILE_M % 16 == 0 && TILE_M >= 64 && TILE_M <= 256,
+                "MMA N in [64, 256], multiple of 16");
+};
+
+constexpr int kMaxStages = 8;
 constexpr long long kDrainNs = 2000000000LL;
 
-static_assert(kAccCols + kStages * 2 * kBK <= kTmemCols, "TMEM budget");
-
 struct __align__(8) Control {
-  uint64_t full[kStages];   // TMA -> converters (tx bytes)
-  uint64_t conv[kStages];   // converters -> MMA (one arrival per warp)
-  uint64_t empty[kStages];  // MMA completion -> producer
-  uint64_t accum;           // last MMA completion -> epilogue
+  uint64_t full[kMaxStages];   // TMA -> converters (tx bytes)
+  uint64_t conv[kMaxStages];   // converters -> MMA (one arrival per warp)
+  uint64_t empty[kMaxStages];  // MMA completion -> producer
+  uint64_t accum;              // last MMA completion -> epilogue
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr int kOffASmall = kStages * kStageBytesA;
-constexpr int kOffB = 2 * kStages * kStageBytesA;
-constexpr int kOffCtl = kOffB + kStages * kStageBytesB;
-constexpr int kSmemBytes = kOffCtl + (int)sizeof(Control) + 1024;
+template <class C>
+constexpr int smem_bytes() {
+  return C::kOffCtl + (int)sizeof(Control) + 1024;
+}
 
 // Rounds x to the nearest TF32 value (ties to even) and returns the exact
 // remainder x - big.  Values TF32 holds exactly give small = 0; NaN stays
@@ -114,16 +127,24 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <class Cf>
+__global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, float* C,
                        long long ldc, int M, int N, int K, int tiles_m,
                        int tiles_n, WaitCfg wc) {
+  constexpr int kTileM = Cf::kTileM, kTileN = Cf::kTileN, kBK = Cf::kBK;
+  constexpr int kStages = Cf::kStages, kConvWarps = Cf::kConvWarps;
+  constexpr int kAccCols = Cf::kAccCols, kTmemCols = Cf::kTmemCols;
+  constexpr int kStageBytesA = Cf::kStageBytesA;
+  constexpr int kStageBytesB = Cf::kStageBytesB;
+  constexpr int kOffASmall = Cf::kOffASmall, kOffB = Cf::kOffB;
+  constexpr uint32_t kIdesc = Cf::kIdesc;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  Control* ctl = reinterpret_cast<Control*>(smem + kOffCtl);
+  Control* ctl = reinterpret_cast<Control*>(smem + Cf::kOffCtl);
   volatile int* abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -324,8 +345,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace tf32x3
 
-cudaError_t launch_tf32x3(const Problem& p, const WaitCfg& wc,
-                          cudaStream_t stream) {
+namespace {
+
+template <class Cf>
+cudaError_t launch_cfg(const Problem& p, const WaitCfg& wc,
+                       cudaStream_t stream) {
   using namespace tf32x3;
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
@@ -334,7 +358,7 @@ cudaError_t launch_tf32x3(const Problem& p, const WaitCfg& wc,
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.lda * 4};
-    const cuuint32_t box[2] = {kBK, kTileM};
+    const cuuint32_t box[2] = {(cuuint32_t)Cf::kBK, (cuuint32_t)Cf::kTileM};
     if (encode(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                const_cast<float*>(p.A), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -345,7 +369,7 @@ cudaError_t launch_tf32x3(const Problem& p, const WaitCfg& wc,
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.K};
     const cuuint64_t strides[1] = {(cuuint64_t)p.ldb * 4};
-    const cuuint32_t box[2] = {kTileN, kBK};
+    const cuuint32_t box[2] = {(cuuint32_t)Cf::kTileN, (cuuint32_t)Cf::kBK};
     if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                const_cast<float*>(p.B), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -353,16 +377,35 @@ cudaError_t launch_tf32x3(const Problem& p, const WaitCfg& wc,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = ensure_smem_attr(
-      reinterpret_cast<const void*>(tf32x3_gemm_kernel), kSmemBytes);
+  auto fn = tf32x3_gemm_kernel<Cf>;
+  constexpr int kSmem = smem_bytes<Cf>();
+  cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(fn), kSmem);
   if (e != cudaSuccess) return e;
-  const int tiles_m = (p.M + kTileM - 1) / kTileM;
-  const int tiles_n = (p.N + kTileN - 1) / kTileN;
+  const int tiles_m = (p.M + Cf::kTileM - 1) / Cf::kTileM;
+  const int tiles_n = (p.N + Cf::kTileN - 1) / Cf::kTileN;
   const long long grid = (long long)tiles_m * tiles_n;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tf32x3_gemm_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(
+  fn<<<(unsigned)grid, Cf::kThreads, kSmem, stream>>>(
       ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, wc);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int tf32x3_tile_m(int cfg) { return cfg == kTc256 ? 256 : 128; }
+
+cudaError_t launch_tf32x3(const Problem& p, int cfg, const WaitCfg& wc,
+                          cudaStream_t stream) {
+  using namespace tf32x3;
+  switch (cfg) {
+    case kTc256:
+      return launch_cfg<Cfg<256, 5>>(p, wc, stream);
+    case kTc128:
+      return launch_cfg<Cfg<128, 4>>(p, wc, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace gemm_f32_impl

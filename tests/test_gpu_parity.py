@@ -28,24 +28,32 @@ DEV = torch.device("cuda:0")
 SIMT_CFGS = list(range(7))
 
 
-def _forced(algo, cfg=None):
-    """Context: forces the algorithm and (for SIMT) the tile config."""
+def _env(name, value):
+    """Context: sets one environment variable the library reads per call."""
     import contextlib
     import os
 
     @contextlib.contextmanager
     def ctx():
-        old = os.environ.get("GEMM_F32_SIMT_CFG")
-        if cfg is not None:
-            os.environ["GEMM_F32_SIMT_CFG"] = str(cfg)
+        old = os.environ.get(name)
+        if value is not None:
+            os.environ[name] = str(value)
         try:
-            yield algo
+            yield
         finally:
             if old is None:
-                os.environ.pop("GEMM_F32_SIMT_CFG", None)
+                os.environ.pop(name, None)
             else:
-                os.environ["GEMM_F32_SIMT_CFG"] = old
+                os.environ[name] = old
     return ctx()
+
+
+def _forced(algo, cfg=None):
+    """Context: forces the SIMT tile config."""
+    return _env("GEMM_F32_SIMT_CFG", cfg)
+
+
+TC_CFGS = [0, 1]
 
 
 def _padded(x):
@@ -309,19 +317,22 @@ def test_select_algo_reports_a_kernel():
 
 
 # ------------------------------------------------------------- 3xTF32
+@pytest.mark.parametrize("tc_cfg", TC_CFGS)
 @pytest.mark.parametrize("shape", [(128, 128, 16), (256, 128, 32),
                                    (64, 64, 64), (1000, 1000, 1000),
                                    (300, 260, 77), (129, 65, 33),
-                                   (517, 3, 260), (8, 1000, 8), (1, 1, 1)])
-def test_tf32x3_shapes(shape):
+                                   (517, 3, 260), (8, 1000, 8), (1, 1, 1),
+                                   (700, 520, 2000)])
+def test_tf32x3_shapes(shape, tc_cfg):
     M, N, K = shape
     a, b = synth.make_operands(M, N, K, seed=M * 3 + N * 5 + K)
-    check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
-               what=f"tf32x3{shape}")
-    ai, bi = synth.make_operands(M, N, K, seed=M + N + K, dist_a="int",
-                                 dist_b="int")
-    check_full(ai, bi, run_gpu(ai, bi, G.ALGO_TF32X3, pad=True), exact=True,
-               what=f"tf32x3{shape} int")
+    with _env("GEMM_F32_TC_CFG", tc_cfg):
+        check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
+                   what=f"tf32x3 cfg{tc_cfg} {shape}")
+        ai, bi = synth.make_operands(M, N, K, seed=M + N + K, dist_a="int",
+                                     dist_b="int")
+        check_full(ai, bi, run_gpu(ai, bi, G.ALGO_TF32X3, pad=True),
+                   exact=True, what=f"tf32x3 cfg{tc_cfg} {shape} int")
     assert G.device_status() == 0
 
 
@@ -347,20 +358,22 @@ def test_tf32x3_unsupported_when_misaligned():
         G.gemm_f32_ptr(8, 7, 8, p, 8, p, 7, p, 7, 0, G.ALGO_TF32X3)
 
 
-def test_tf32x3_timeout_path_reports_and_recovers():
+@pytest.mark.parametrize("tc_cfg", TC_CFGS)
+def test_tf32x3_timeout_path_reports_and_recovers(tc_cfg):
     """A producer that issues no copies makes every wait run out: the
     kernel frees TMEM, leaves, and the status word says TIMEOUT; the next
     call works."""
     a, b = synth.make_operands(300, 200, 100, seed=2)
-    old_t = G.set_wait_timeout_ns(2_000_000)
-    old_f = G.set_debug_flags(G.DEBUG_STALL_PRODUCER)
-    try:
-        run_gpu(a, b, G.ALGO_TF32X3, pad=True)
-        assert G.device_status() == 4
-    finally:
-        G.set_debug_flags(old_f)
-        G.set_wait_timeout_ns(old_t)
-    assert G.device_status() == 0
-    check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
-               what="after timeout")
+    with _env("GEMM_F32_TC_CFG", tc_cfg):
+        old_t = G.set_wait_timeout_ns(2_000_000)
+        old_f = G.set_debug_flags(G.DEBUG_STALL_PRODUCER)
+        try:
+            run_gpu(a, b, G.ALGO_TF32X3, pad=True)
+            assert G.device_status() == 4
+        finally:
+            G.set_debug_flags(old_f)
+            G.set_wait_timeout_ns(old_t)
+        assert G.device_status() == 0
+        check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
+                   what="after timeout")
     assert G.device_status() == 0
