@@ -115,8 +115,9 @@ int choose_tc_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   (void)d;
   // 128 x 128 tiles at two CTAs per SM beat 256 x 128 at one on every
   // measured shape (finer scheduling grain, one CTA's epilogue overlapping
-  // the other's main loop).
-  return kTc128;
+  // the other's main loop); letting the tensor core truncate the raw
+  // operands to TF32 halves the converters' work.
+  return kTc128Raw;
 }
 
 // Decides which kernel runs.  Returns a status; fills *plan on success.

@@ -29,9 +29,15 @@ cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
                         cudaStream_t stream);
 
 // 3xTF32 tcgen05 kernel configurations: 256 x 128 tiles at one CTA per SM,
-// or 128 x 128 tiles at two.
-enum TcCfg { kTc256 = 0, kTc128 = 1, kTcCfgCount = 2 };
-int tf32x3_tile_m(int cfg);
+// or 128 x 128 tiles at two; "Raw" variants let the tensor core truncate the
+// raw fp32 operands to TF32 for the big part instead of rounding them first.
+enum TcCfg {
+  kTc256 = 0,
+  kTc128 = 1,
+  kTc128Raw = 2,
+  kTc256Raw = 3,
+  kTcCfgCount = 4
+};
 
 // 3xTF32 tcgen05 kernel.  Needs A, B 16-byte aligned, lda and ldb multiples
 // of 4, K >= 1 and an sm_100-family device.

@@ -3,13 +3,19 @@
 // The pages' own tensor-core path ("Rendre le GPU rapide", section "Les
 // Tensor Cores") rounds operands to 16 bits and keeps the sums in f32; that
 // cannot hold single-precision accuracy.  Here every fp32 value x is split
-// into big = x rounded to the nearest TF32 value (10 fraction bits; the
-// round-half-to-even by integer add that the same section uses for bf16) and
-// small = x − big, which fp32 holds exactly.  Then
+// into a TF32 part big and small = x − big, which fp32 holds exactly.  Then
 //     a·b ≈ a_big·b_big + a_big·b_small + a_small·b_big
-// drops only a_small·b_small and the TF32 rounding of small (≈ 2^-21 |a b|
-// per term), far inside the single-precision tolerance, and the sums run in
-// the tensor core's fp32 accumulator in Tensor Memory (TMEM).
+// drops only a_small·b_small and the TF32 truncation of small, and the sums
+// run in the tensor core's fp32 accumulator in Tensor Memory (TMEM).  Two
+// splits are built:
+//   * rounded: big = x rounded to the nearest TF32 value (ties to even, the
+//     integer add-and-cut that the same section uses for bf16), written out
+//     explicitly; per-term error ≈ 2^-21 |a b|;
+//   * raw (the default): the MMAs read x itself and the tensor core keeps
+//     its top 19 bits, so big = x truncated to TF32 and the converters only
+//     write small = x − trunc(x); per-term error ≤ 3·2^-20 |a b|.  A test
+//     (A·I = A bit for bit) pins the truncation this relies on.
+// Both are far inside the single-precision tolerance.
 //
 // The kernel computes the tile of C transposed, Cᵀ = Bᵀ·Aᵀ, so that neither
 // operand needs a transpose in shared memory:
@@ -51,8 +57,13 @@ namespace tf32x3 {
 
 // Tile configuration.  TILE_M rows of C per CTA (the MMA's N), always 128
 // columns (the MMA's M = TMEM lanes), STAGES-deep ring of 16-deep k stages.
-template <int TILE_M, int STAGES>
+template <int TILE_M, int STAGES, bool RAW_BIG>
 struct Cfg {
+  // RAW_BIG: the MMAs read the raw fp32 operands as their "big" part and the
+  // tensor core keeps their top 19 bits (TF32 truncation); converters then
+  // write only small = x - trunc(x).  Otherwise big is rounded to the
+  // nearest TF32 value explicitly and written out as well.
+  static constexpr bool kRawBig = RAW_BIG;
   static constexpr int kTileM = TILE_M;
   static constexpr int kTileN = 128;
   static constexpr int kBK = 16;  // k per stage: 64-byte rows
@@ -100,6 +111,13 @@ __device__ __forceinline__ void tf32_split(float x, uint32_t& big,
   const uint32_t b = (u + 0xFFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
   big = b;
   small = __float_as_uint(__fsub_rn(x, __uint_as_float(b)));
+}
+
+// The split the tensor core sees when it reads x itself: big = x with its
+// 13 low mantissa bits dropped (TF32 truncation), small = x - big (exact).
+__device__ __forceinline__ uint32_t tf32_small_of_truncated(float x) {
+  const float big = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  return __float_as_uint(__fsub_rn(x, big));
 }
 
 // Bounded wait on one phase of an mbarrier.  Gives up (false) when the CTA
@@ -264,28 +282,51 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
           reinterpret_cast<const float*>(smem + kOffB + s * kStageBytesB) +
           n_loc + 8 * h * kTileN;
       uint32_t big[8], small[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) tf32_split(bcol[k * kTileN], big[k], small[k]);
       const uint32_t tcol = tmem + lane_bits + kAccCols + s * 2 * kBK + 8 * h;
-      tmem_st8(tcol, big);
-      tmem_st8(tcol + kBK, small);
-      // A: element-wise, position for position (the swizzle is untouched)
       float4* araw = reinterpret_cast<float4*>(smem + s * kStageBytesA);
       float4* asml =
           reinterpret_cast<float4*>(smem + kOffASmall + s * kStageBytesA);
+      constexpr int kChunksPerThread = kStageBytesA / 16 / (32 * kConvWarps);
+      if constexpr (Cf::kRawBig) {
 #pragma unroll
-      for (int j = 0; j < kStageBytesA / 16 / (32 * kConvWarps); ++j) {
-        const int c = t + 32 * kConvWarps * j;
-        const float4 v = araw[c];
-        uint32_t b0, b1, b2, b3, s0, s1, s2, s3;
-        tf32_split(v.x, b0, s0);
-        tf32_split(v.y, b1, s1);
-        tf32_split(v.z, b2, s2);
-        tf32_split(v.w, b3, s3);
-        araw[c] = make_float4(__uint_as_float(b0), __uint_as_float(b1),
-                              __uint_as_float(b2), __uint_as_float(b3));
-        asml[c] = make_float4(__uint_as_float(s0), __uint_as_float(s1),
-                              __uint_as_float(s2), __uint_as_float(s3));
+        for (int k = 0; k < 8; ++k) {
+          const float x = bcol[k * kTileN];
+          big[k] = __float_as_uint(x);
+          small[k] = tf32_small_of_truncated(x);
+        }
+        tmem_st8(tcol, big);
+        tmem_st8(tcol + kBK, small);
+        // A: the raw tile stays the big part; only small is written
+#pragma unroll
+        for (int j = 0; j < kChunksPerThread; ++j) {
+          const int c = t + 32 * kConvWarps * j;
+          const float4 v = araw[c];
+          asml[c] = make_float4(__uint_as_float(tf32_small_of_truncated(v.x)),
+                                __uint_as_float(tf32_small_of_truncated(v.y)),
+                                __uint_as_float(tf32_small_of_truncated(v.z)),
+                                __uint_as_float(tf32_small_of_truncated(v.w)));
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          tf32_split(bcol[k * kTileN], big[k], small[k]);
+        tmem_st8(tcol, big);
+        tmem_st8(tcol + kBK, small);
+        // A: element-wise, position for position (the swizzle is untouched)
+#pragma unroll
+        for (int j = 0; j < kChunksPerThread; ++j) {
+          const int c = t + 32 * kConvWarps * j;
+          const float4 v = araw[c];
+          uint32_t b0, b1, b2, b3, s0, s1, s2, s3;
+          tf32_split(v.x, b0, s0);
+          tf32_split(v.y, b1, s1);
+          tf32_split(v.z, b2, s2);
+          tf32_split(v.w, b3, s3);
+          araw[c] = make_float4(__uint_as_float(b0), __uint_as_float(b1),
+                                __uint_as_float(b2), __uint_as_float(b3));
+          asml[c] = make_float4(__uint_as_float(s0), __uint_as_float(s1),
+                                __uint_as_float(s2), __uint_as_float(s3));
+        }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -393,16 +434,19 @@ cudaError_t launch_cfg(const Problem& p, const WaitCfg& wc,
 
 }  // namespace
 
-int tf32x3_tile_m(int cfg) { return cfg == kTc256 ? 256 : 128; }
 
 cudaError_t launch_tf32x3(const Problem& p, int cfg, const WaitCfg& wc,
                           cudaStream_t stream) {
   using namespace tf32x3;
   switch (cfg) {
     case kTc256:
-      return launch_cfg<Cfg<256, 5>>(p, wc, stream);
+      return launch_cfg<Cfg<256, 5, false>>(p, wc, stream);
     case kTc128:
-      return launch_cfg<Cfg<128, 4>>(p, wc, stream);
+      return launch_cfg<Cfg<128, 4, false>>(p, wc, stream);
+    case kTc128Raw:
+      return launch_cfg<Cfg<128, 4, true>>(p, wc, stream);
+    case kTc256Raw:
+      return launch_cfg<Cfg<256, 5, true>>(p, wc, stream);
     default:
       return cudaErrorInvalidValue;
   }

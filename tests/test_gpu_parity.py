@@ -53,7 +53,7 @@ def _forced(algo, cfg=None):
     return _env("GEMM_F32_SIMT_CFG", cfg)
 
 
-TC_CFGS = [0, 1]
+TC_CFGS = [0, 1, 2, 3]
 
 
 def _padded(x):
@@ -334,6 +334,26 @@ def test_tf32x3_shapes(shape, tc_cfg):
         check_full(ai, bi, run_gpu(ai, bi, G.ALGO_TF32X3, pad=True),
                    exact=True, what=f"tf32x3 cfg{tc_cfg} {shape} int")
     assert G.device_status() == 0
+
+
+@pytest.mark.parametrize("tc_cfg", TC_CFGS)
+def test_tf32x3_identity_is_exact(tc_cfg):
+    """A·I = A and I·B = B bit for bit when every value's TF32 big/small
+    split is exact (the two lowest mantissa bits clear).  For the raw-operand
+    configurations this pins the tensor core's reading of an fp32 operand to
+    TF32 truncation: rounding it would move about half of the values."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((192, 64)).astype(np.float32)
+    x = (x.view(np.uint32) & np.uint32(0xFFFFFFFC)).view(np.float32)
+    eye = np.eye(64, dtype=np.float32)
+    with _env("GEMM_F32_TC_CFG", tc_cfg):
+        c = run_gpu(x, eye, G.ALGO_TF32X3)
+        assert np.array_equal(c.view(np.uint32), x.view(np.uint32)), \
+            f"A·I != A in {int((c != x).sum())} places"
+        xt = np.ascontiguousarray(x[:64, :])
+        c = run_gpu(eye, xt, G.ALGO_TF32X3)
+        assert np.array_equal(c.view(np.uint32), xt.view(np.uint32)), \
+            f"I·B != B in {int((c != xt).sum())} places"
 
 
 def test_tf32x3_wide_dynamic_range():
