@@ -2,6 +2,7 @@
 //
 // The ABI is declared in include/gemm_f32.h.  Every entry point returns a
 // status and never throws; only gemm_f32_device_status synchronizes.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -81,6 +82,8 @@ struct Plan {
   int algo;      // gemm_f32_algo actually run
   int simt_cfg;  // for ALGO_SIMT
   int tc_cfg;    // for ALGO_TF32X3
+  int splits;    // split-K factor for ALGO_TF32X3 (1 = none)
+  long long ws_bytes;  // scratch the plan needs (0 = none)
   bool vec;      // 16-byte operand copies
   bool c_vec;    // 16-byte C stores
 };
@@ -120,6 +123,20 @@ int choose_tc_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   return kTc128Raw;
 }
 
+// Split-K factor for the tensor path: enough CTAs to fill every slot when
+// the tiles alone leave most SMs idle, at least 8 k stages per split.
+int choose_splits(int64_t M, int64_t N, int64_t K, int tile_m,
+                  const DeviceInfo& d) {
+  const int forced = env_int("GEMM_F32_SPLITS", 0);
+  const int64_t nk = (K + 15) / 16;
+  const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + 127) / 128);
+  const int64_t slots = (tile_m == 128 ? 2 : 1) * (int64_t)d.sm_count;
+  int64_t s = forced > 0 ? forced : (2 * tiles >= slots ? 1 : slots / tiles);
+  if (forced <= 0) s = std::min<int64_t>(s, nk / 8);
+  s = std::min<int64_t>(std::min<int64_t>(s, nk), 16);
+  return (int)std::max<int64_t>(s, 1);
+}
+
 // Decides which kernel runs.  Returns a status; fills *plan on success.
 int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
               const float* B, int64_t ldb, const float* C, int64_t ldc,
@@ -130,25 +147,32 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   plan->c_vec = aligned16(C) && ldc % 4 == 0;
   plan->simt_cfg = choose_simt_cfg(M, N, d);
   plan->tc_cfg = choose_tc_cfg(M, N, d);
+  plan->splits = 1;
+  plan->ws_bytes = 0;
   const bool tcgen05_ok = d.cc_major == 10 && vec && K >= 1;
   switch (algo) {
     case GEMM_F32_ALGO_AUTO:
       plan->algo = (tcgen05_ok && env_int("GEMM_F32_AUTO_SIMT", 0) == 0)
                        ? GEMM_F32_ALGO_TF32X3
                        : GEMM_F32_ALGO_SIMT;
-      return GEMM_F32_OK;
+      break;
     case GEMM_F32_ALGO_SIMT:
       plan->algo = GEMM_F32_ALGO_SIMT;
       return GEMM_F32_OK;
     case GEMM_F32_ALGO_TF32X3:
       if (!tcgen05_ok) return GEMM_F32_ERR_UNSUPPORTED;
       plan->algo = GEMM_F32_ALGO_TF32X3;
-      return GEMM_F32_OK;
+      break;
     case GEMM_F32_ALGO_TMA:
       return GEMM_F32_ERR_UNSUPPORTED;
     default:
       return GEMM_F32_ERR_INVALID_ARG;
   }
+  if (plan->algo == GEMM_F32_ALGO_TF32X3) {
+    plan->splits = choose_splits(M, N, K, tf32x3_tile_m(plan->tc_cfg), d);
+    if (plan->splits > 1) plan->ws_bytes = (long long)plan->splits * M * N * 4;
+  }
+  return GEMM_F32_OK;
 }
 
 }  // namespace
@@ -172,11 +196,18 @@ cudaError_t ensure_smem_attr(const void* fn, int bytes) {
 
 extern "C" {
 
-int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                const float* B, int64_t ldb, float* C, int64_t ldc,
-                gemm_f32_stream_t stream, int algo) {
+}  // extern "C"
+
+namespace {
+
+// One call: checks, plan, launch.  `ws`/`ws_bytes` is optional scratch; a
+// plan that wants more than given runs without split-K.
+int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+             const float* B, int64_t ldb, float* C, int64_t ldc,
+             gemm_f32_stream_t stream, int algo, void* ws, int64_t ws_bytes) {
   if (algo < GEMM_F32_ALGO_AUTO || algo > GEMM_F32_ALGO_TF32X3)
     return GEMM_F32_ERR_INVALID_ARG;
+  if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return GEMM_F32_ERR_INVALID_ARG;
   int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM_F32_OK) return st;
   if (M == 0 || N == 0) return GEMM_F32_OK;
@@ -186,6 +217,11 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   Plan plan;
   st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, *d, &plan);
   if (st != GEMM_F32_OK) return st;
+  if (plan.ws_bytes > 0 &&
+      (plan.ws_bytes > ws_bytes || !aligned16(ws))) {
+    plan.splits = 1;
+    plan.ws_bytes = 0;
+  }
 
   Problem p;
   p.M = static_cast<int>(M);
@@ -207,7 +243,9 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       wc.limit = g_wait_ns.load();
       wc.debug = g_debug_flags.load();
       wc.status = d->status;
-      e = launch_tf32x3(p, plan.tc_cfg, wc, s);
+      e = launch_tf32x3(p, plan.tc_cfg, plan.splits,
+                        plan.splits > 1 ? static_cast<float*>(ws) : nullptr,
+                        wc, s);
       break;
     }
     default:
@@ -215,6 +253,42 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   }
   if (e != cudaSuccess) return fail_cuda(e);
   return GEMM_F32_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                const float* B, int64_t ldb, float* C, int64_t ldc,
+                gemm_f32_stream_t stream, int algo) {
+  return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, stream, algo, nullptr, 0);
+}
+
+int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                const float* B, int64_t ldb, float* C, int64_t ldc,
+                void* workspace, int64_t workspace_bytes,
+                gemm_f32_stream_t stream) {
+  return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, stream,
+                  GEMM_F32_ALGO_AUTO, workspace, workspace_bytes);
+}
+
+int64_t gemm_f32_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) {
+    t_last_cuda_error = static_cast<int>(e);
+    return -GEMM_F32_ERR_CUDA;
+  }
+  Plan plan;
+  // aligned operands: the plan gemm_f32_ws takes for 16-byte aligned
+  // matrices with leading dimensions that are multiples of 4
+  const float* aligned = reinterpret_cast<const float*>(16);
+  const int st = make_plan(M, N, K, aligned, K, aligned, N, aligned, N,
+                           GEMM_F32_ALGO_AUTO, *d, &plan);
+  if (st != GEMM_F32_OK) return -st;
+  return plan.ws_bytes;
 }
 
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,

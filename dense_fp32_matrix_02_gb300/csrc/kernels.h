@@ -39,9 +39,19 @@ enum TcCfg {
   kTcCfgCount = 4
 };
 
+int tf32x3_tile_m(int cfg);
+
+// Bytes of partial tiles a split-K launch with `splits` > 1 writes (and the
+// reduction reads): splits × M × N floats.
+long long tf32x3_partials_bytes(const Problem& p, int splits);
+
 // 3xTF32 tcgen05 kernel.  Needs A, B 16-byte aligned, lda and ldb multiples
-// of 4, K >= 1 and an sm_100-family device.
-cudaError_t launch_tf32x3(const Problem& p, int cfg, const WaitCfg& wc,
+// of 4, K >= 1 and an sm_100-family device.  With splits > 1 and a
+// `partials` buffer of tf32x3_partials_bytes, the K range is split over
+// `splits` CTAs per tile and a second kernel sums the partial tiles into C
+// in split order (deterministic).  splits is reduced so no split is empty.
+cudaError_t launch_tf32x3(const Problem& p, int cfg, int splits,
+                          float* partials, const WaitCfg& wc,
                           cudaStream_t stream);
 
 }  // namespace gemm_f32_impl

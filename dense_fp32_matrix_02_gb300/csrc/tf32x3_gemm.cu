@@ -150,7 +150,8 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, float* C,
                        long long ldc, int M, int N, int K, int tiles_m,
-                       int tiles_n, WaitCfg wc) {
+                       int tiles_n, int splits, int kb_per_split,
+                       float* partials, WaitCfg wc) {
   constexpr int kTileM = Cf::kTileM, kTileN = Cf::kTileN, kBK = Cf::kBK;
   constexpr int kStages = Cf::kStages, kConvWarps = Cf::kConvWarps;
   constexpr int kAccCols = Cf::kAccCols, kTmemCols = Cf::kTmemCols;
@@ -166,10 +167,23 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   volatile int* abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // split-K: the `splits` CTAs of one tile are adjacent in the grid; split
+  // s covers k stages [s·kb_per_split, min(nk, (s+1)·kb_per_split)) and, when
+  // splits > 1, writes its partial tile to partials[s] (an M×N row-major
+  // slice) for the reduction kernel.
+  const int split = blockIdx.x % splits;
   int tm, tn;
-  tile_coords<8>(blockIdx.x, tiles_m, tiles_n, tm, tn);
+  tile_coords<8>(blockIdx.x / splits, tiles_m, tiles_n, tm, tn);
   const int bm = tm * kTileM, bn = tn * kTileN;
-  const int nk = (K + kBK - 1) / kBK;
+  const int nk_total = (K + kBK - 1) / kBK;
+  const int kb0 = split * kb_per_split;
+  const int nk = min(nk_total, kb0 + kb_per_split) - kb0;  // >= 1 (host)
+  float* out = C;
+  long long ldo = ldc;
+  if (splits > 1) {
+    out = partials + (long long)split * M * N;
+    ldo = N;
+  }
 
   auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
   auto conv = [&](int s) { return smem_u32(&ctl->conv[s]); };
@@ -214,10 +228,10 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
             break;
           }
           mbar_arrive_expect_tx(full(s), kStageBytesA + kStageBytesB);
-          tma_load_2d(sbase + s * kStageBytesA, &tmap_a, full(s), kb * kBK,
-                      bm);
+          tma_load_2d(sbase + s * kStageBytesA, &tmap_a, full(s),
+                      (kb0 + kb) * kBK, bm);
           tma_load_2d(sbase + kOffB + s * kStageBytesB, &tmap_b, full(s), bn,
-                      kb * kBK);
+                      (kb0 + kb) * kBK);
           ++issued;
         }
       }
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int m = bm + c0 + i;
-              if (m < M) C[(long long)m * ldc + n] = __uint_as_float(v[i]);
+              if (m < M) out[(long long)m * ldo + n] = __uint_as_float(v[i]);
             }
           }
         }
@@ -365,6 +379,41 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// C[i][j] = sum over s = 0..splits-1, in that order, of partials[s][i][j].
+// Each thread sums four consecutive elements of one row.
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ partials, int splits,
+                         int M, int N, float* __restrict__ C, long long ldc,
+                         int vec) {
+  const long long groups_per_row = (N + 3) / 4;
+  const long long total = (long long)M * groups_per_row;
+  const long long slice = (long long)M * N;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+       g < total; g += (long long)gridDim.x * blockDim.x) {
+    const int i = (int)(g / groups_per_row);
+    const int j = (int)(g % groups_per_row) * 4;
+    const float* src = partials + (long long)i * N + j;
+    float* dst = C + (long long)i * ldc + j;
+    if (vec && j + 3 < N) {
+      float4 acc = *reinterpret_cast<const float4*>(src);
+      for (int s = 1; s < splits; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(src + s * slice);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      *reinterpret_cast<float4*>(dst) = acc;
+    } else {
+      for (int e = 0; e < 4 && j + e < N; ++e) {
+        float acc = src[e];
+        for (int s = 1; s < splits; ++s) acc += src[e + s * slice];
+        dst[e] = acc;
+      }
+    }
   }
 }
 
@@ -389,8 +438,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 namespace {
 
 template <class Cf>
-cudaError_t launch_cfg(const Problem& p, const WaitCfg& wc,
-                       cudaStream_t stream) {
+cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
+                       const WaitCfg& wc, cudaStream_t stream) {
   using namespace tf32x3;
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
@@ -425,28 +474,53 @@ cudaError_t launch_cfg(const Problem& p, const WaitCfg& wc,
   if (e != cudaSuccess) return e;
   const int tiles_m = (p.M + Cf::kTileM - 1) / Cf::kTileM;
   const int tiles_n = (p.N + Cf::kTileN - 1) / Cf::kTileN;
-  const long long grid = (long long)tiles_m * tiles_n;
+  const int nk = (p.K + Cf::kBK - 1) / Cf::kBK;
+  if (splits < 1 || !partials) splits = 1;
+  const int kb_per_split = (nk + splits - 1) / splits;
+  splits = (nk + kb_per_split - 1) / kb_per_split;  // no empty split
+  const long long grid = (long long)tiles_m * tiles_n * splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fn<<<(unsigned)grid, Cf::kThreads, kSmem, stream>>>(
-      ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, wc);
+      ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, splits,
+      kb_per_split, partials, wc);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
+                   p.ldc % 4 == 0 && p.N % 4 == 0)
+                      ? 1
+                      : 0;
+  const long long groups = (long long)p.M * ((p.N + 3) / 4);
+  const int blocks = (int)((groups + 255) / 256 < 4096 ? (groups + 255) / 256
+                                                      : 4096);
+  splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(partials, splits, p.M,
+                                                  p.N, p.C, p.ldc, vec);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 
-cudaError_t launch_tf32x3(const Problem& p, int cfg, const WaitCfg& wc,
+int tf32x3_tile_m(int cfg) {
+  return (cfg == kTc256 || cfg == kTc256Raw) ? 256 : 128;
+}
+
+long long tf32x3_partials_bytes(const Problem& p, int splits) {
+  return splits > 1 ? (long long)splits * p.M * p.N * 4 : 0;
+}
+
+cudaError_t launch_tf32x3(const Problem& p, int cfg, int splits,
+                          float* partials, const WaitCfg& wc,
                           cudaStream_t stream) {
   using namespace tf32x3;
   switch (cfg) {
     case kTc256:
-      return launch_cfg<Cfg<256, 5, false>>(p, wc, stream);
+      return launch_cfg<Cfg<256, 5, false>>(p, splits, partials, wc, stream);
     case kTc128:
-      return launch_cfg<Cfg<128, 4, false>>(p, wc, stream);
+      return launch_cfg<Cfg<128, 4, false>>(p, splits, partials, wc, stream);
     case kTc128Raw:
-      return launch_cfg<Cfg<128, 4, true>>(p, wc, stream);
+      return launch_cfg<Cfg<128, 4, true>>(p, splits, partials, wc, stream);
     case kTc256Raw:
-      return launch_cfg<Cfg<256, 5, true>>(p, wc, stream);
+      return launch_cfg<Cfg<256, 5, true>>(p, splits, partials, wc, stream);
     default:
       return cudaErrorInvalidValue;
   }

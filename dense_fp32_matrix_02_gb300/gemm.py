@@ -51,6 +51,10 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32.argtypes = args
         L.gemm_f32_ex.restype = ci
         L.gemm_f32_ex.argtypes = args + [ci]
+        L.gemm_f32_ws.restype = ci
+        L.gemm_f32_ws.argtypes = args[:-1] + [vp, i64, vp]
+        L.gemm_f32_workspace_size.restype = i64
+        L.gemm_f32_workspace_size.argtypes = [i64, i64, i64]
         L.gemm_f32_select_algo.restype = ci
         L.gemm_f32_select_algo.argtypes = args[:-1]
         L.gemm_f32_status_string.restype = ctypes.c_char_p
@@ -89,6 +93,23 @@ def gemm_f32_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, stream=0,
                            b_ptr or None, int(ldb), c_ptr or None, int(ldc),
                            stream or None, int(algo))
     _check(st, "gemm_f32")
+
+
+def gemm_f32_ws_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, ws_ptr,
+                    ws_bytes, stream=0):
+    """Raw-pointer gemm_f32_ws call (automatic kernel, optional scratch)."""
+    st = lib().gemm_f32_ws(int(M), int(N), int(K), a_ptr or None, int(lda),
+                           b_ptr or None, int(ldb), c_ptr or None, int(ldc),
+                           ws_ptr or None, int(ws_bytes), stream or None)
+    _check(st, "gemm_f32_ws")
+
+
+def workspace_size(M, N, K) -> int:
+    """Scratch bytes gemm_f32_ws would use for aligned M×N×K operands."""
+    n = int(lib().gemm_f32_workspace_size(int(M), int(N), int(K)))
+    if n < 0:
+        _check(-n, "gemm_f32_workspace_size")
+    return n
 
 
 def _matrix_args(t, name):
@@ -130,9 +151,35 @@ def gemm_f32_ex(a, b, c=None, algo=ALGO_AUTO, stream=None):
     return c
 
 
-def gemm_f32(a, b, c=None, stream=None):
-    """C = A·B with the automatically selected kernel."""
-    return gemm_f32_ex(a, b, c, ALGO_AUTO, stream)
+def gemm_f32(a, b, c=None, stream=None, workspace=None):
+    """C = A·B with the automatically selected kernel.
+
+    ``workspace``: optional CUDA tensor used as split-K scratch through
+    gemm_f32_ws (see ``workspace_size``); None runs gemm_f32 without it.
+    """
+    if workspace is None:
+        return gemm_f32_ex(a, b, c, ALGO_AUTO, stream)
+    import torch
+    M, K, ap, lda = _matrix_args(a, "a")
+    K2, N, bp, ldb = _matrix_args(b, "b")
+    if K != K2:
+        raise ValueError(f"inner sizes differ: {tuple(a.shape)} x "
+                         f"{tuple(b.shape)}")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    Mc, Nc, cp, ldc = _matrix_args(c, "c")
+    if (Mc, Nc) != (M, N):
+        raise ValueError(f"c has shape {tuple(c.shape)}, want {(M, N)}")
+    if not workspace.is_cuda:
+        raise ValueError("workspace must live on a CUDA device")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    nbytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(a.device):
+        gemm_f32_ws_ptr(M, N, K, ap, lda, bp, ldb, cp, ldc,
+                        workspace.data_ptr() if nbytes else 0, nbytes, handle)
+    return c
 
 
 def select_algo(M, N, K, a_ptr=0, lda=None, b_ptr=0, ldb=None, c_ptr=0,

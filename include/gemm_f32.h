@@ -96,6 +96,27 @@ GEMM_F32_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, in
                 const float *B, int64_t ldb, float *C, int64_t ldc,
                 gemm_f32_stream_t stream, int algo);
 
+/*
+ * As gemm_f32 (automatic kernel choice), with caller-owned device scratch
+ * that the library may use to split K over several CTAs per tile when the
+ * tiles alone would leave most SMs idle (a second kernel then sums the
+ * partial tiles in a fixed order, so results stay deterministic).
+ * `workspace` must be 16-byte aligned device memory of `workspace_bytes`
+ * bytes (NULL with 0 is allowed); if it is smaller than
+ * gemm_f32_workspace_size(M, N, K) the call runs without splitting.  The
+ * workspace is in use until the stream passes this call: calls that may
+ * overlap on the GPU need separate workspaces.
+ */
+GEMM_F32_API int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A,
+                             int64_t lda, const float *B, int64_t ldb,
+                             float *C, int64_t ldc, void *workspace,
+                             int64_t workspace_bytes,
+                             gemm_f32_stream_t stream);
+
+/* Scratch bytes gemm_f32_ws would use for an M×N×K product with aligned
+ * operands on the current device (0 = none).  Negative status on error. */
+GEMM_F32_API int64_t gemm_f32_workspace_size(int64_t M, int64_t N, int64_t K);
+
 /* The algorithm gemm_f32 with GEMM_F32_ALGO_AUTO would run for these
  * arguments on the current device (no launch).  Negative on bad args. */
 GEMM_F32_API int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float *A,

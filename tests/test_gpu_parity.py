@@ -397,3 +397,70 @@ def test_tf32x3_timeout_path_reports_and_recovers(tc_cfg):
         check_full(a, b, run_gpu(a, b, G.ALGO_TF32X3, pad=True),
                    what="after timeout")
     assert G.device_status() == 0
+
+
+# ------------------------------------------------------------- split-K
+def run_gpu_ws(a, b, ws_bytes=None):
+    """C = A·B through gemm_f32_ws with a workspace of the size it asks."""
+    M, K = a.shape
+    N = b.shape[1]
+    need = G.workspace_size(M, N, K) if ws_bytes is None else ws_bytes
+    ws = torch.empty(max(need // 4, 1), device=DEV) if need else None
+    ta, tb = _padded(a), _padded(b)
+    tc = _padded(np.full((M, N), np.nan, np.float32))
+    G.gemm_f32(ta, tb, tc, workspace=ws if ws is not None else
+               torch.empty(0, device=DEV))
+    torch.cuda.synchronize()
+    return tc.cpu().numpy(), need
+
+
+def test_workspace_size_policy():
+    assert G.workspace_size(1024, 1024, 1024) > 0          # 64 tiles
+    assert G.workspace_size(4096, 4096, 4096) == 0         # 1024 tiles
+    assert G.workspace_size(64, 64, 64) == 0               # K too short
+    assert G.workspace_size(0, 5, 5) == 0
+
+
+@pytest.mark.parametrize("name", ["sq1024", "rag1000"])
+def test_splitk_workloads(name):
+    w = synth.WORKLOADS[name]
+    a, b = w.operands()
+    c, need = run_gpu_ws(a, b)
+    assert need > 0
+    check_full(a, b, c, what=f"{name} split-K")
+    wi = w.integer_variant()
+    ai, bi = wi.operands()
+    ci, _ = run_gpu_ws(ai, bi)
+    check_full(ai, bi, ci, exact=True, what=f"{wi.name} split-K")
+    assert G.device_status() == 0
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5, 16])
+@pytest.mark.parametrize("shape", [(300, 260, 1000), (129, 65, 333),
+                                   (64, 64, 64), (17, 1000, 520)])
+def test_splitk_forced(splits, shape):
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=splits + M)
+    with _env("GEMM_F32_SPLITS", splits):
+        need = G.workspace_size(M, N, K)
+        assert need == min(splits, (K + 15) // 16) * M * N * 4 or need == 0
+        c, _ = run_gpu_ws(a, b)
+        check_full(a, b, c, what=f"split {splits} {shape}")
+        ai, bi = synth.make_operands(M, N, K, seed=splits, dist_a="int",
+                                     dist_b="int")
+        ci, _ = run_gpu_ws(ai, bi)
+        check_full(ai, bi, ci, exact=True, what=f"split {splits} {shape} int")
+
+
+def test_splitk_small_workspace_falls_back():
+    a, b = synth.WORKLOADS["sq1024"].operands()
+    need = G.workspace_size(1024, 1024, 1024)
+    c, _ = run_gpu_ws(a, b, ws_bytes=need - 4)
+    check_full(a, b, c, what="too-small workspace")
+
+
+def test_splitk_deterministic():
+    a, b = synth.WORKLOADS["rag1000"].operands()
+    c1, _ = run_gpu_ws(a, b)
+    c2, _ = run_gpu_ws(a, b)
+    assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
