@@ -257,6 +257,34 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
 
 }  // namespace
 
+namespace gemm_f32_impl {
+
+long long auto_plan_scratch_bytes(int64_t M, int64_t N, int64_t K,
+                                  const float* A, int64_t lda, const float* B,
+                                  int64_t ldb, const float* C, int64_t ldc) {
+  const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM_F32_OK) return -st;
+  if (M == 0 || N == 0) return 0;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return -fail_cuda(e);
+  Plan plan;
+  const int ps = make_plan(M, N, K, A, lda, B, ldb, C, ldc,
+                           GEMM_F32_ALGO_AUTO, *d, &plan);
+  if (ps != GEMM_F32_OK) return -ps;
+  return plan.ws_bytes;
+}
+
+int run_auto_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float* C,
+                          int64_t ldc, void* scratch, int64_t scratch_bytes,
+                          gemm_f32_stream_t stream) {
+  return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, stream, GEMM_F32_ALGO_AUTO,
+                  scratch, scratch_bytes);
+}
+
+}  // namespace gemm_f32_impl
+
 extern "C" {
 
 int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
@@ -328,6 +356,9 @@ const char* gemm_f32_status_string(int status) {
       return "CUDA runtime error";
     case GEMM_F32_ERR_TIMEOUT:
       return "a kernel's bounded wait gave up";
+    case GEMM_F32_ERR_SCRATCH_LIMIT:
+      return "the product needs more split-K scratch than the library's "
+             "static buffer holds (see gemm_f32_noalloc_scratch_bytes)";
     default:
       return "unknown status";
   }

@@ -3,8 +3,10 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "common.cuh"
+#include "gemm_f32.h"
 
 namespace gemm_f32_impl {
 
@@ -53,5 +55,17 @@ long long tf32x3_partials_bytes(const Problem& p, int splits);
 cudaError_t launch_tf32x3(const Problem& p, int cfg, int splits,
                           float* partials, const WaitCfg& wc,
                           cudaStream_t stream);
+
+// Scratch bytes the automatic plan wants for these arguments on the current
+// device (0 = none), or minus a gemm_f32_status.
+long long auto_plan_scratch_bytes(int64_t M, int64_t N, int64_t K,
+                                  const float* A, int64_t lda, const float* B,
+                                  int64_t ldb, const float* C, int64_t ldc);
+
+// gemm_f32_ws's path: automatic plan with the given scratch.
+int run_auto_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float* C,
+                          int64_t ldc, void* scratch, int64_t scratch_bytes,
+                          gemm_f32_stream_t stream);
 
 }  // namespace gemm_f32_impl

@@ -53,6 +53,10 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_ex.argtypes = args + [ci]
         L.gemm_f32_ws.restype = ci
         L.gemm_f32_ws.argtypes = args[:-1] + [vp, i64, vp]
+        L.gemm_f32_noalloc.restype = ci
+        L.gemm_f32_noalloc.argtypes = args
+        L.gemm_f32_noalloc_scratch_bytes.restype = i64
+        L.gemm_f32_noalloc_scratch_bytes.argtypes = []
         L.gemm_f32_workspace_size.restype = i64
         L.gemm_f32_workspace_size.argtypes = [i64, i64, i64]
         L.gemm_f32_select_algo.restype = ci
@@ -102,6 +106,22 @@ def gemm_f32_ws_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, ws_ptr,
                            b_ptr or None, int(ldb), c_ptr or None, int(ldc),
                            ws_ptr or None, int(ws_bytes), stream or None)
     _check(st, "gemm_f32_ws")
+
+
+def gemm_f32_noalloc_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,
+                         stream=0):
+    """Raw-pointer gemm_f32_noalloc call: split-K scratch is the library's
+    own static buffer, so nothing is allocated (for callers that may not
+    allocate device memory)."""
+    st = lib().gemm_f32_noalloc(int(M), int(N), int(K), a_ptr or None,
+                                int(lda), b_ptr or None, int(ldb),
+                                c_ptr or None, int(ldc), stream or None)
+    _check(st, "gemm_f32_noalloc")
+
+
+def noalloc_scratch_bytes() -> int:
+    """Capacity of the static scratch buffer gemm_f32_noalloc uses."""
+    return int(lib().gemm_f32_noalloc_scratch_bytes())
 
 
 def workspace_size(M, N, K) -> int:

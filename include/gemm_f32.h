@@ -60,7 +60,10 @@ typedef enum {
      * available from gemm_f32_last_cuda_error(). */
     GEMM_F32_ERR_CUDA = 3,
     /* A kernel's bounded wait gave up (reported by gemm_f32_device_status). */
-    GEMM_F32_ERR_TIMEOUT = 4
+    GEMM_F32_ERR_TIMEOUT = 4,
+    /* gemm_f32_noalloc: the product needs more split-K scratch than the
+     * library's static buffer holds. */
+    GEMM_F32_ERR_SCRATCH_LIMIT = 5
 } gemm_f32_status;
 
 typedef enum {
@@ -112,6 +115,36 @@ GEMM_F32_API int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A,
                              float *C, int64_t ldc, void *workspace,
                              int64_t workspace_bytes,
                              gemm_f32_stream_t stream);
+
+/*
+ * As gemm_f32_ws, but the split-K scratch is a buffer inside the library
+ * itself, so this call allocates no memory at all.  It is for callers that
+ * must not allocate device memory: code running inside a framework or
+ * server that hands out all device memory from its own pool (a direct
+ * cudaMalloc would go around that pool's budget), and latency-critical
+ * paths where an allocation's implicit synchronisation and unbounded
+ * latency are not acceptable.  The pages have no counterpart to it.
+ *
+ * The buffer is a static device array of gemm_f32_noalloc_scratch_bytes()
+ * (16 MiB) that every GPU holds from the library's first use on it until
+ * the process exits.  The first call on each device looks up the buffer's
+ * device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  A product whose split needs
+ * more scratch than the buffer holds is rejected with
+ * GEMM_F32_ERR_SCRATCH_LIMIT (nothing is launched); products that need no
+ * split run as gemm_f32 would.  All calls on a device share the buffer and
+ * it keeps whatever the last call left there; nothing in it needs to start
+ * at zero (every split writes the whole partial tile it later adds), but
+ * calls that may overlap on the GPU (different streams, or not yet
+ * finished) race on it and must be serialised by the caller.
+ */
+GEMM_F32_API int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
+                                  const float *A, int64_t lda, const float *B,
+                                  int64_t ldb, float *C, int64_t ldc,
+                                  gemm_f32_stream_t stream);
+
+/* Capacity in bytes of the static scratch buffer gemm_f32_noalloc uses. */
+GEMM_F32_API int64_t gemm_f32_noalloc_scratch_bytes(void);
 
 /* Scratch bytes gemm_f32_ws would use for an M×N×K product with aligned
  * operands on the current device (0 = none).  Negative status on error. */
