@@ -310,10 +310,11 @@ int64_t gemm_f32_workspace_size(int64_t M, int64_t N, int64_t K) {
     return -GEMM_F32_ERR_CUDA;
   }
   Plan plan;
-  // aligned operands: the plan gemm_f32_ws takes for 16-byte aligned
-  // matrices with leading dimensions that are multiples of 4
+  // the plan for 16-byte aligned operands whose leading dimensions are the
+  // row widths rounded up to multiples of 4: the layouts that can use it
   const float* aligned = reinterpret_cast<const float*>(16);
-  const int st = make_plan(M, N, K, aligned, K, aligned, N, aligned, N,
+  const int64_t lda = (K + 3) / 4 * 4, ldn = (N + 3) / 4 * 4;
+  const int st = make_plan(M, N, K, aligned, lda, aligned, ldn, aligned, ldn,
                            GEMM_F32_ALGO_AUTO, *d, &plan);
   if (st != GEMM_F32_OK) return -st;
   return plan.ws_bytes;

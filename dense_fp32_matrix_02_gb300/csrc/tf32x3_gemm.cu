@@ -121,18 +121,20 @@ __device__ __forceinline__ uint32_t tf32_small_of_truncated(float x) {
 }
 
 // Bounded wait on one phase of an mbarrier.  Gives up (false) when the CTA
-// abort flag is raised or `limit_ns` of %globaltimer time pass.
+// abort flag is raised or `limit_ns` of %globaltimer time pass.  Each probe
+// lets the thread sleep until the phase completes (up to kSleepNs) instead
+// of polling shared memory.
+constexpr uint32_t kSleepNs = 200000;
+
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            long long limit_ns,
                                            volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0) {
-      if (abort && *abort) return false;
-      if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    if (abort && *abort) return false;
+    if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
   }
 }
 

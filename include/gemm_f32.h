@@ -146,8 +146,10 @@ GEMM_F32_API int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
 /* Capacity in bytes of the static scratch buffer gemm_f32_noalloc uses. */
 GEMM_F32_API int64_t gemm_f32_noalloc_scratch_bytes(void);
 
-/* Scratch bytes gemm_f32_ws would use for an M×N×K product with aligned
- * operands on the current device (0 = none).  Negative status on error. */
+/* Scratch bytes gemm_f32_ws would use for an M×N×K product on the current
+ * device when A, B and C are 16-byte aligned with leading dimensions that
+ * are multiples of 4 (the layouts that can use scratch; others need none).
+ * 0 = none.  Negative status on error. */
 GEMM_F32_API int64_t gemm_f32_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /* The algorithm gemm_f32 with GEMM_F32_ALGO_AUTO would run for these
