@@ -107,7 +107,7 @@ int choose_simt_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   if (N <= 64) return kSimt128x64x16;
   const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
   if (tiles < d.sm_count) return kSimt128x64x16;
-  return kSimt128x128x32Occ1;
+  return kSimtKm128x128x32Occ1;
 }
 
 int choose_tc_cfg(int64_t M, int64_t N, const DeviceInfo& d) {

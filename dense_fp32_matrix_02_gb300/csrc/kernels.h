@@ -20,7 +20,10 @@ enum SimtCfg {
   kSimt128x128x16Occ1 = 4,
   kSimt128x128x8 = 5,
   kSimt128x128x32Occ1 = 6,
-  kSimtCfgCount = 7
+  kSimt128x128x16Occ1S6 = 7,
+  kSimtKm128x128x32Occ1 = 8,  // A kept K-major (16-byte copies)
+  kSimtKm128x128x16Occ1 = 9,
+  kSimtCfgCount = 10
 };
 
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize for `fn` on the current

@@ -18,14 +18,19 @@
 // as in §3.4 of the same page); B is copied in 16-byte chunks when VEC is
 // true (B 16-byte aligned, ldb a multiple of 4) and one float at a time
 // otherwise, so any alignment and any leading dimension work.
+#include <type_traits>
+
 #include "ffma_tile.cuh"
 #include "kernels.h"
 
 namespace gemm_f32_impl {
 
-template <int BM, int BN, int BK, int STAGES, bool VEC>
+// AKM = true keeps A K-major in shared memory (FfmaTile: 16-byte copies of
+// A, read along K); false stores it transposed (FfmaTileT, 4-byte copies).
+template <int BM, int BN, int BK, int STAGES, bool VEC, bool AKM = false>
 struct SimtKernel {
-  using Tile = FfmaTileT<BM, BN, BK>;
+  using Tile = typename std::conditional<AKM, FfmaTile<BM, BN, BK>,
+                                         FfmaTileT<BM, BN, BK>>::type;
   static constexpr int kThreads = Tile::kThreads;
   static constexpr int kSmemBytes = STAGES * Tile::kStageBytes + 1024;
 
@@ -35,8 +40,26 @@ struct SimtKernel {
                                                     float* Bs, int bm, int bn,
                                                     int kt, int tid) {
     const int k0 = kt * BK;
+    if constexpr (AKM) {
+      // A, K-major: 16-byte chunks (zero-filled past M or K), swizzled
+      constexpr int kChunksA = BM * BK / 4;
+#pragma unroll
+      for (int id = tid; id < kChunksA; id += kThreads) {
+        const int m = id / (BK / 4), c = id % (BK / 4);
+        const int gm = bm + m, gk = k0 + 4 * c;
+        int bytes = 0;
+        const float* src = p.A;
+        if (gm < p.M && gk < p.K) {
+          bytes = 4 * min(4, p.K - gk);
+          src = p.A + (long long)gm * p.lda + gk;
+        }
+        cp_async16(smem_u32(As + m * BK + ((c ^ a_swizzle<BK>(m)) * 4)), src,
+                   bytes);
+      }
+    }
     // A, transposed on the way in: single-float copies, a warp covering 4
     // rows × 8 consecutive k (whole 32-byte sectors of each row).
+    if constexpr (!AKM) {
     constexpr int kElemsA = BM * BK;
 #pragma unroll
     for (int id = tid; id < kElemsA; id += kThreads) {
@@ -47,6 +70,7 @@ struct SimtKernel {
       const bool ok = gm < p.M && gk < p.K;
       const float* src = ok ? p.A + (long long)gm * p.lda + gk : p.A;
       cp_async4(smem_u32(As + Tile::a_index(k, m)), src, ok ? 4 : 0);
+    }
     }
     if (VEC) {
       constexpr int kChunksB = BK * BN / 4;
@@ -123,18 +147,19 @@ struct SimtKernel {
   }
 };
 
-template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB>
+template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB, bool AKM>
 __global__ void __launch_bounds__(FfmaTileT<BM, BN, BK>::kThreads, MINB)
     simt_gemm_kernel(Problem p, int tiles_m, int tiles_n, int c_vec) {
-  SimtKernel<BM, BN, BK, STAGES, VEC>::run(p, tiles_m, tiles_n, c_vec);
+  SimtKernel<BM, BN, BK, STAGES, VEC, AKM>::run(p, tiles_m, tiles_n, c_vec);
 }
 
 namespace {
 
-template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB>
+template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB,
+          bool AKM = false>
 cudaError_t launch_cfg(const Problem& p, bool c_vec, cudaStream_t stream) {
-  using K = SimtKernel<BM, BN, BK, STAGES, VEC>;
-  auto fn = simt_gemm_kernel<BM, BN, BK, STAGES, VEC, MINB>;
+  using K = SimtKernel<BM, BN, BK, STAGES, VEC, AKM>;
+  auto fn = simt_gemm_kernel<BM, BN, BK, STAGES, VEC, MINB, AKM>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn),
                                    K::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -164,6 +189,15 @@ cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
       return launch_cfg<128, 128, 8, 6, VEC, 2>(p, c_vec, stream);
     case kSimt128x128x32Occ1:
       return launch_cfg<128, 128, 32, 4, VEC, 1>(p, c_vec, stream);
+    case kSimt128x128x16Occ1S6:
+      return launch_cfg<128, 128, 16, 6, VEC, 1>(p, c_vec, stream);
+    case kSimtKm128x128x32Occ1:
+      // 16-byte copies of A need VEC (aligned A, lda % 4 == 0)
+      return VEC ? launch_cfg<128, 128, 32, 4, true, 1, true>(p, c_vec, stream)
+                 : launch_cfg<128, 128, 32, 4, false, 1>(p, c_vec, stream);
+    case kSimtKm128x128x16Occ1:
+      return VEC ? launch_cfg<128, 128, 16, 6, true, 1, true>(p, c_vec, stream)
+                 : launch_cfg<128, 128, 16, 6, false, 1>(p, c_vec, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -121,20 +121,26 @@ __device__ __forceinline__ uint32_t tf32_small_of_truncated(float x) {
 }
 
 // Bounded wait on one phase of an mbarrier.  Gives up (false) when the CTA
-// abort flag is raised or `limit_ns` of %globaltimer time pass.  Each probe
-// lets the thread sleep until the phase completes (up to kSleepNs) instead
-// of polling shared memory.
+// abort flag is raised or `limit_ns` of %globaltimer time pass.  With
+// `sleep`, each probe lets the thread sleep until the phase completes (up to
+// kSleepNs) instead of polling shared memory; the single-thread roles that
+// feed the pipeline (producer, MMA issuer) poll, to react at once.
 constexpr uint32_t kSleepNs = 200000;
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            long long limit_ns,
-                                           volatile int* abort) {
+                                           volatile int* abort,
+                                           bool sleep = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
-    if (abort && *abort) return false;
-    if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
+  for (uint32_t i = 1;; ++i) {
+    if (sleep ? mbar_try_wait_sleep(bar, parity, kSleepNs)
+              : mbar_try_wait(bar, parity))
+      return true;
+    if (sleep || (i & 15u) == 0) {
+      if (abort && *abort) return false;
+      if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
+    }
   }
 }
 
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
           const int s = kb % kStages;
           const uint32_t use = kb / kStages;
           if (kb >= kStages &&
-              !wait_phase(empty(s), (use - 1) & 1, wc.limit, abort)) {
+              !wait_phase(empty(s), (use - 1) & 1, wc.limit, abort, false)) {
             *abort = 1;
             record_status(wc.status, kStatusTimeoutEmpty);
             break;
@@ -251,7 +257,8 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % kStages;
-        if (!wait_phase(conv(s), (kb / kStages) & 1, wc.limit, abort)) {
+        if (!wait_phase(conv(s), (kb / kStages) & 1, wc.limit, abort,
+                        false)) {
           *abort = 1;
           record_status(wc.status, kStatusTimeoutFull);
           break;

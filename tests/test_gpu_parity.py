@@ -25,7 +25,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 from dense_fp32_matrix_02_gb300 import gemm as G  # noqa: E402
 
 DEV = torch.device("cuda:0")
-SIMT_CFGS = list(range(7))
+SIMT_CFGS = list(range(10))
 
 
 def _env(name, value):
