@@ -259,6 +259,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
 
 namespace gemm_f32_impl {
 
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 long long auto_plan_scratch_bytes(int64_t M, int64_t N, int64_t K,
                                   const float* A, int64_t lda, const float* B,
                                   int64_t ldb, const float* C, int64_t ldc) {

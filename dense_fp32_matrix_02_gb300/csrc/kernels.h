@@ -65,6 +65,10 @@ long long auto_plan_scratch_bytes(int64_t M, int64_t N, int64_t K,
                                   const float* A, int64_t lda, const float* B,
                                   int64_t ldb, const float* C, int64_t ldc);
 
+// Records a CUDA error for gemm_f32_last_cuda_error; returns
+// GEMM_F32_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // gemm_f32_ws's path: automatic plan with the given scratch.
 int run_auto_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
                           int64_t lda, const float* B, int64_t ldb, float* C,

@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_ex.argtypes = args + [ci]
         L.gemm_f32_ws.restype = ci
         L.gemm_f32_ws.argtypes = args[:-1] + [vp, i64, vp]
+        L.gemm_f32_host.restype = ci
+        L.gemm_f32_host.argtypes = args[:-1] + [vp, vp, vp, vp, i64, vp]
         L.gemm_f32_noalloc.restype = ci
         L.gemm_f32_noalloc.argtypes = args
         L.gemm_f32_noalloc_scratch_bytes.restype = i64
@@ -117,6 +119,48 @@ def gemm_f32_noalloc_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,
                                 int(lda), b_ptr or None, int(ldb),
                                 c_ptr or None, int(ldc), stream or None)
     _check(st, "gemm_f32_noalloc")
+
+
+def gemm_f32_host(a, b, c, da, db, dc, workspace=None, stream=None):
+    """C = A·B for CPU tensors a, b, c (pin them for overlapped copies),
+    through caller-lent CUDA buffers da (M×K), db (K×N), dc (M×N),
+    contiguous.  Copies, multiply and copy-back overlap in row chunks."""
+    import torch
+    for t, name in ((a, "a"), (b, "b"), (c, "c")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or \
+                t.dim() != 2 or t.is_cuda:
+            raise TypeError(f"{name} must be a 2-D float32 CPU tensor")
+        if t.numel() and t.shape[1] > 1 and t.stride(1) != 1:
+            raise ValueError(f"{name} must be row-major")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2 or tuple(c.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    for t, shape, name in ((da, (M, K), "da"), (db, (K, N), "db"),
+                           (dc, (M, N), "dc")):
+        if not t.is_cuda or not t.is_contiguous() or \
+                t.numel() < shape[0] * shape[1]:
+            raise ValueError(f"{name} must be a contiguous CUDA buffer of "
+                             f"at least {shape[0]}x{shape[1]} floats")
+    if stream is None:
+        stream = torch.cuda.current_stream(dc.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+    def ld(t, cols):
+        return max(t.stride(0) if t.shape[0] > 1 else cols, cols, 1)
+
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+        ws_ptr = workspace.data_ptr() if ws_bytes else 0
+    with torch.cuda.device(dc.device):
+        st = lib().gemm_f32_host(
+            M, N, K, a.data_ptr() or None, ld(a, K), b.data_ptr() or None,
+            ld(b, N), c.data_ptr() or None, ld(c, N), da.data_ptr() or None,
+            db.data_ptr() or None, dc.data_ptr() or None, ws_ptr or None,
+            ws_bytes, handle or None)
+    _check(st, "gemm_f32_host")
+    return c
 
 
 def noalloc_scratch_bytes() -> int:

@@ -152,6 +152,27 @@ GEMM_F32_API int64_t gemm_f32_noalloc_scratch_bytes(void);
  * 0 = none.  Negative status on error. */
 GEMM_F32_API int64_t gemm_f32_workspace_size(int64_t M, int64_t N, int64_t K);
 
+/*
+ * C = A·B for A, B and C in host memory (row-major, leading dimensions lda,
+ * ldb, ldc); page-locked host memory lets the copies run asynchronously and
+ * at full speed.  The caller lends device buffers dA (M×K), dB (K×N) and dC
+ * (M×N), row-major with leading dimensions K, N and N, and optional split-K
+ * scratch as for gemm_f32_ws; the library allocates no memory.  B is copied
+ * to the GPU first, then A in row chunks: each chunk is multiplied on
+ * `stream` while the next one is being copied, and each finished chunk of C
+ * is copied back while the next one is multiplied.  The work starts after
+ * what is already queued on `stream`, and `stream` completes once C is in
+ * host memory; the host buffers must stay valid until then.  Two copy
+ * streams and a set of events per device are created on first use and kept.
+ * The pages have no counterpart (they keep data on the GPU).
+ */
+GEMM_F32_API int gemm_f32_host(int64_t M, int64_t N, int64_t K,
+                               const float *hA, int64_t lda, const float *hB,
+                               int64_t ldb, float *hC, int64_t ldc, float *dA,
+                               float *dB, float *dC, void *workspace,
+                               int64_t workspace_bytes,
+                               gemm_f32_stream_t stream);
+
 /* The algorithm gemm_f32 with GEMM_F32_ALGO_AUTO would run for these
  * arguments on the current device (no launch).  Negative on bad args. */
 GEMM_F32_API int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float *A,

@@ -464,3 +464,39 @@ def test_splitk_deterministic():
     c1, _ = run_gpu_ws(a, b)
     c2, _ = run_gpu_ws(a, b)
     assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+
+
+# ------------------------------------------------------------- host buffers
+@pytest.mark.parametrize("shape,pinned,pad", [
+    ((1000, 1000, 1000), True, 0), ((2048, 1536, 512), True, 0),
+    ((517, 300, 77), True, 3), ((517, 300, 77), False, 5),
+    ((9, 7, 0), True, 0), ((1, 1, 1), False, 0)])
+def test_host_pipeline(shape, pinned, pad):
+    """gemm_f32_host: host operands (strided or not, pinned or not) through
+    lent device buffers, chunked and overlapped, equal the oracle."""
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=M + N + K)
+    ha = torch.zeros(M, K + pad)
+    hb = torch.zeros(K, N + pad)
+    hc = torch.full((M, N + pad), float("nan"))
+    if pinned:
+        ha, hb, hc = ha.pin_memory(), hb.pin_memory(), hc.pin_memory()
+    ha[:, :K] = torch.from_numpy(a)
+    hb[:, :N] = torch.from_numpy(b)
+    da = torch.empty(max(M * K, 1), device=DEV)
+    db = torch.empty(max(K * N, 1), device=DEV)
+    dc = torch.empty(M * N, device=DEV)
+    need = G.workspace_size(M, N, K)
+    ws = torch.empty(max(need // 4, 1), device=DEV) if need else None
+    s = torch.cuda.Stream()
+    G.gemm_f32_host(ha[:, :K], hb[:, :N], hc[:, :N], da, db, dc,
+                    workspace=ws, stream=s)
+    s.synchronize()
+    c = hc[:, :N].numpy()
+    if K == 0:
+        assert (c == 0).all()
+    else:
+        check_full(a, b, c, what=f"host {shape}")
+    if pad:
+        assert torch.isnan(hc[:, N:]).all()   # padding untouched
+    assert G.device_status() == 0
