@@ -164,7 +164,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       plan->algo = GEMM_F32_ALGO_TF32X3;
       break;
     case GEMM_F32_ALGO_TMA:
-      return GEMM_F32_ERR_UNSUPPORTED;
+      if (!(vec && K >= 1)) return GEMM_F32_ERR_UNSUPPORTED;
+      plan->algo = GEMM_F32_ALGO_TMA;
+      return GEMM_F32_OK;
     default:
       return GEMM_F32_ERR_INVALID_ARG;
   }
@@ -238,6 +240,14 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     case GEMM_F32_ALGO_SIMT:
       e = launch_simt(p, plan.simt_cfg, plan.vec, plan.c_vec, s);
       break;
+    case GEMM_F32_ALGO_TMA: {
+      WaitCfg wc;
+      wc.limit = g_wait_ns.load();
+      wc.debug = g_debug_flags.load();
+      wc.status = d->status;
+      e = launch_tma_ffma(p, plan.c_vec, wc, s);
+      break;
+    }
     case GEMM_F32_ALGO_TF32X3: {
       WaitCfg wc;
       wc.limit = g_wait_ns.load();

@@ -65,6 +65,11 @@ long long auto_plan_scratch_bytes(int64_t M, int64_t N, int64_t K,
                                   const float* A, int64_t lda, const float* B,
                                   int64_t ldb, const float* C, int64_t ldc);
 
+// FFMA kernel fed by TMA under mbarrier phases (128x128x32 tiles, 4
+// stages).  Needs A, B 16-byte aligned, lda and ldb multiples of 4, K >= 1.
+cudaError_t launch_tma_ffma(const Problem& p, bool c_vec, const WaitCfg& wc,
+                            cudaStream_t stream);
+
 // Records a CUDA error for gemm_f32_last_cuda_error; returns
 // GEMM_F32_ERR_CUDA.
 int record_cuda_error(cudaError_t e);

@@ -73,9 +73,10 @@ typedef enum {
      * multi-stage swizzled shared-memory ring.  Any pointer alignment and
      * any leading dimension. */
     GEMM_F32_ALGO_SIMT = 1,
-    /* Reserved for an FP32 FFMA kernel fed by a TMA producer warp through an
-     * mbarrier full/empty ring; this version returns
-     * GEMM_F32_ERR_UNSUPPORTED for it. */
+    /* FP32 FFMA register-tiled kernel whose operand tiles TMA copies into
+     * a 4-stage ring under mbarrier full/empty phases (no per-thread copy
+     * instructions, no __syncthreads in the main loop).  Needs A and B
+     * 16-byte aligned, lda and ldb multiples of 4, and K >= 1. */
     GEMM_F32_ALGO_TMA = 2,
     /* Tensor-core kernel (tcgen05, TMEM accumulator) computing each product
      * as three TF32 products of a big/small operand split, accumulated in

@@ -500,3 +500,48 @@ def test_host_pipeline(shape, pinned, pad):
     if pad:
         assert torch.isnan(hc[:, N:]).all()   # padding untouched
     assert G.device_status() == 0
+
+
+# ------------------------------------------------------------- TMA + FFMA
+@pytest.mark.parametrize("shape", [(128, 128, 32), (64, 64, 64),
+                                   (1000, 1000, 1000), (300, 260, 77),
+                                   (129, 65, 33), (1, 1, 1), (8, 1000, 300),
+                                   (700, 520, 2000)])
+def test_tma_ffma_shapes(shape):
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=M + 7 * N + K)
+    check_full(a, b, run_gpu(a, b, G.ALGO_TMA, pad=True),
+               what=f"tma {shape}")
+    ai, bi = synth.make_operands(M, N, K, seed=K + 1, dist_a="int",
+                                 dist_b="int")
+    check_full(ai, bi, run_gpu(ai, bi, G.ALGO_TMA, pad=True), exact=True,
+               what=f"tma {shape} int")
+    assert G.device_status() == 0
+
+
+def test_tma_ffma_sq4096_sampled():
+    w = synth.WORKLOADS["sq4096"]
+    a, b = w.operands()
+    check_sampled_and_rowsums(a, b, run_gpu(a, b, G.ALGO_TMA), what="tma")
+
+
+def test_tma_ffma_unsupported_when_misaligned():
+    ta = torch.zeros(64 * 64 + 1, device=DEV)
+    p = ta.data_ptr()
+    with pytest.raises(G.GemmError) as e:
+        G.gemm_f32_ptr(8, 8, 8, p + 4, 8, p, 8, p, 8, 0, G.ALGO_TMA)
+    assert e.value.status == 2
+
+
+def test_tma_ffma_timeout_path_reports_and_recovers():
+    a, b = synth.make_operands(300, 200, 100, seed=2)
+    old_t = G.set_wait_timeout_ns(2_000_000)
+    old_f = G.set_debug_flags(G.DEBUG_STALL_PRODUCER)
+    try:
+        run_gpu(a, b, G.ALGO_TMA, pad=True)
+        assert G.device_status() == 4
+    finally:
+        G.set_debug_flags(old_f)
+        G.set_wait_timeout_ns(old_t)
+    check_full(a, b, run_gpu(a, b, G.ALGO_TMA, pad=True), what="tma after")
+    assert G.device_status() == 0
