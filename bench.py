@@ -66,7 +66,9 @@ def load_peaks():
 KERNEL_SOURCES = {
     "tf32x3": ["tf32x3_gemm.cu", "tcgen05.cuh", "common.cuh", "kernels.h"],
     "simt": ["simt_gemm.cu", "ffma_tile.cuh", "common.cuh", "kernels.h"],
+    "tma": ["tma_ffma_gemm.cu", "ffma_tile.cuh", "common.cuh", "kernels.h"],
 }
+TF32_FLOP_PER_CLK_PER_SM = 4096  # tcgen05 kind::tf32 dense (ncu peak rate)
 
 
 def kernel_source_hash(kernel):
@@ -359,6 +361,11 @@ def run_ours(args, w, config):
                 "unit": "TFLOP/s", "frac": achieved / (tf32 / 3.0),
                 "peak_source": f"{peaks_src} bf16 burst {peaks['bf16_tflops']}"
                                " x 1.1/2.25 (nominal TF32/bf16), / 3 products"}
+        # the tensor pipe's own TF32 rate (ncu peak_sustained: 4096 flop per
+        # clock per SM) at the run's maximum clock, / 3 products
+        hw = TF32_FLOP_PER_CLK_PER_SM * sms * smax * 1e6 / 1e12 / 3.0
+        roof["peak_tensor_pipe_at_clock"] = hw
+        roof["frac_tensor_pipe_at_clock"] = achieved / hw
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak,
                 "unit": "TFLOP/s", "frac": achieved / fp32_peak,
