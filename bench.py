@@ -40,8 +40,8 @@ FP32_LANES_PER_SM = 128  # FFMA lanes per SM on GB300 (4 SMSPs x 32)
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="sq4096")
     p.add_argument("--algo", default="auto", choices=list(ALGOS))
@@ -149,6 +149,23 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def reduce_max_over_ranks(value, device=None):
+    """Largest `value` over all ranks of the process group (itself alone
+    when there is no group)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and \
+            dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_rank, steps, world, ms_slowest):
+    """Whole-job TFLOP/s: every rank's flops over the slowest rank's time."""
+    return flops_per_rank * steps * world / (ms_slowest / 1e3) / 1e12
 
 
 def dist_env():
@@ -295,15 +312,12 @@ def run_ours(args, w, config):
         dist.barrier()
     clocks = sampler.stop()
     ms = start.elapsed_time(end)
-    t_ms = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
-    ms_max = float(t_ms.item())
+    ms_max = reduce_max_over_ranks(ms, dev)
     if G.device_status() != 0:
         raise SystemExit("kernel status word set during the timed region")
 
     flops = float(w.flops)
-    value = flops * args.steps * world / (ms_max / 1e3) / 1e12
+    value = weak_scaling_value(flops, args.steps, world, ms_max)
     # one GEMM launch per step (plus the split-K reduction when it splits);
     # launch gaps are included
     kernel_ms = ms / args.steps
@@ -340,10 +354,8 @@ def run_ours(args, w, config):
         e2e_step()
     e2.record(stream)
     torch.cuda.synchronize()
-    e_ms = torch.tensor([s2.elapsed_time(e2)], device=dev)
-    if world > 1:
-        dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = flops * e_steps * world / (float(e_ms.item()) / 1e3) / 1e12
+    e2e_value = weak_scaling_value(
+        flops, e_steps, world, reduce_max_over_ranks(s2.elapsed_time(e2), dev))
 
     # ---- roofline of the (only) kernel
     peaks, peaks_src = load_peaks()
