@@ -22,6 +22,9 @@ enum : unsigned int {
 };
 
 // One problem as the kernels see it.  Leading dimensions in elements.
+// Batched calls add per-matrix element strides; a kernel launched with
+// gridDim.z = batch handles matrix blockIdx.z.  transA / transB: the operand
+// is stored transposed (A as K×M with row stride lda, B as N×K with ldb).
 struct Problem {
   int M, N, K;
   const float* A;
@@ -30,6 +33,9 @@ struct Problem {
   long long ldb;
   float* C;
   long long ldc;
+  long long sA = 0, sB = 0, sC = 0;  // batch strides (elements)
+  int batch = 1;
+  int transA = 0, transB = 0;
 };
 
 // Bounded-wait configuration shared by all pipelined kernels.
@@ -143,6 +149,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::"
       "bytes [%0], [%1, {%3, %4}], [%2];\n" ::"r"(dst),
       "l"(tmap), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// 3-D tiled bulk tensor load (c0 innermost, c2 the batch index).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap,
+                                            uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
 

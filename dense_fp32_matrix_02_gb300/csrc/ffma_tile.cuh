@@ -158,7 +158,11 @@ struct FfmaTile {
 // Thread placement: warps (BM/64) × (BN/32), lanes 8 (M) × 4 (N).  Lane
 // (lm, ln) of warp (wm, wn) owns rows wm·64 + lm·4 + 32h + r (h < 2, r < 4)
 // and columns wn·32 + ln·4 + 16g + j (g < 2, j < 4).
-template <int BM, int BN, int BK>
+//
+// BSWZ = true (B stored transposed in global memory, so its tile arrives
+// one float at a time): B's 16-byte chunk c of row k sits at c ^ (k & 7),
+// the same swizzle as A, and the thread's two B chunks are read from there.
+template <int BM, int BN, int BK, bool BSWZ = false>
 struct FfmaTileT {
   static_assert(BM % 64 == 0 && BN % 32 == 0, "warp tile is 64 x 32");
   static_assert(BK % 8 == 0 && BK <= 32, "BK in {8, 16, 24, 32}");
@@ -170,8 +174,15 @@ struct FfmaTileT {
   static constexpr int kStageBytes = 4 * (kStageFloatsA + kStageFloatsB);
 
   int a_off[8];  // (c ^ g) * 4 for g = 0..7, c = row0 / 4
+  int b_off[BSWZ ? 8 : 1];  // (c ^ g) * 4 for g = 0..7, c = col0 / 4
   int b_col_off;
   int row0, col0;
+
+  // Offset (floats) of element (k, n) in a B stage.
+  static __device__ __forceinline__ int b_index(int k, int n) {
+    if (BSWZ) return k * BN + ((((n >> 2) ^ (k & 7)) << 2) | (n & 3));
+    return k * BN + n;
+  }
 
   // Offset (floats) of element (k, m) in an A stage.
   static __device__ __forceinline__ int a_index(int k, int m) {
@@ -188,6 +199,11 @@ struct FfmaTileT {
 #pragma unroll
     for (int g = 0; g < 8; ++g) a_off[g] = (c ^ g) << 2;
     b_col_off = col0;
+    if (BSWZ) {
+      const int cb = col0 >> 2;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) b_off[g] = (cb ^ g) << 2;
+    }
   }
 
   __device__ __forceinline__ void compute(const float* __restrict__ As,
@@ -199,8 +215,17 @@ struct FfmaTileT {
       const float* a_row = As + k * BM + a_off[k & 7];
       const float4 a0 = *reinterpret_cast<const float4*>(a_row);
       const float4 a1 = *reinterpret_cast<const float4*>(a_row + 32);
-      const float4 b0 = *reinterpret_cast<const float4*>(b_base + k * BN);
-      const float4 b1 = *reinterpret_cast<const float4*>(b_base + k * BN + 16);
+      float4 b0, b1;
+      if (BSWZ) {
+        // col0 / 4 has bit 2 clear, so the second chunk (col0 + 16) sits at
+        // the first one's position with bit 2 flipped: offset ^ 16 floats
+        const float* b_row = Bs + k * BN;
+        b0 = *reinterpret_cast<const float4*>(b_row + b_off[k & 7]);
+        b1 = *reinterpret_cast<const float4*>(b_row + (b_off[k & 7] ^ 16));
+      } else {
+        b0 = *reinterpret_cast<const float4*>(b_base + k * BN);
+        b1 = *reinterpret_cast<const float4*>(b_base + k * BN + 16);
+      }
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll

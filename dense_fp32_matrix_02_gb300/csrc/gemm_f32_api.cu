@@ -297,7 +297,69 @@ int run_auto_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
 
 }  // namespace gemm_f32_impl
 
+namespace {
+
+bool mult4(int64_t x) { return x % 4 == 0; }
+
+int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
+                const float* A, int64_t lda, int64_t sA, const float* B,
+                int64_t ldb, int64_t sB, float* C, int64_t ldc, int64_t sC,
+                int64_t batch, gemm_f32_stream_t stream) {
+  if ((opA != GEMM_F32_OP_N && opA != GEMM_F32_OP_T) ||
+      (opB != GEMM_F32_OP_N && opB != GEMM_F32_OP_T))
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || batch < 0) return GEMM_F32_ERR_INVALID_ARG;
+  const bool ta = opA == GEMM_F32_OP_T, tb = opB == GEMM_F32_OP_T;
+  if (lda < (ta ? M : K) || ldb < (tb ? K : N) || ldc < N)
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (sA < 0 || sB < 0 || sC < 0) return GEMM_F32_ERR_INVALID_ARG;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff || batch > 65535)
+    return GEMM_F32_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0 || batch == 0) return GEMM_F32_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_F32_ERR_INVALID_ARG;
+  if (!ta && !tb && batch == 1)  // the plain product
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, stream,
+                    GEMM_F32_ALGO_AUTO, nullptr, 0);
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  Problem p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  p.sA = sA;
+  p.sB = sB;
+  p.sC = sC;
+  p.batch = static_cast<int>(batch);
+  p.transA = ta ? 1 : 0;
+  p.transB = tb ? 1 : 0;
+  const bool vec = aligned16(A) && aligned16(B) && mult4(lda) && mult4(ldb) &&
+                   mult4(sA) && mult4(sB);
+  const bool c_vec = aligned16(C) && mult4(ldc) && mult4(sC);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  e = launch_simt(p, choose_simt_cfg(M, N, *d), vec, c_vec, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return GEMM_F32_OK;
+}
+
+}  // namespace
+
 extern "C" {
+
+int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
+                     const float* A, int64_t lda, int64_t strideA,
+                     const float* B, int64_t ldb, int64_t strideB, float* C,
+                     int64_t ldc, int64_t strideC, int64_t batch,
+                     gemm_f32_stream_t stream) {
+  return run_batched(opA, opB, M, N, K, A, lda, strideA, B, ldb, strideB, C,
+                     ldc, strideC, batch, stream);
+}
 
 int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                 const float* B, int64_t ldb, float* C, int64_t ldc,

@@ -26,11 +26,17 @@
 namespace gemm_f32_impl {
 
 // AKM = true keeps A K-major in shared memory (FfmaTile: 16-byte copies of
-// A, read along K); false stores it transposed (FfmaTileT, 4-byte copies).
-template <int BM, int BN, int BK, int STAGES, bool VEC, bool AKM = false>
+// A, read along K); false stores it transposed (FfmaTileT).
+// TA / TB: A / B stored transposed in global memory (A as K×M, B as N×K).
+// A transposed in memory is exactly FfmaTileT's [BK][BM] layout (16-byte
+// copies when VEC); B transposed lands one float at a time in a swizzled
+// [BK][BN] layout (FfmaTileT with BSWZ).
+template <int BM, int BN, int BK, int STAGES, bool VEC, bool AKM = false,
+          bool TA = false, bool TB = false>
 struct SimtKernel {
+  static_assert(!(AKM && (TA || TB)), "K-major A only for A untransposed");
   using Tile = typename std::conditional<AKM, FfmaTile<BM, BN, BK>,
-                                         FfmaTileT<BM, BN, BK>>::type;
+                                         FfmaTileT<BM, BN, BK, TB>>::type;
   static constexpr int kThreads = Tile::kThreads;
   static constexpr int kSmemBytes = STAGES * Tile::kStageBytes + 1024;
 
@@ -57,9 +63,36 @@ struct SimtKernel {
                    bytes);
       }
     }
+    if constexpr (TA && VEC) {
+      // A stored K×M: row k of the stage is 4-float chunks of row k0 + k
+      constexpr int kChunksA = BK * BM / 4;
+#pragma unroll
+      for (int id = tid; id < kChunksA; id += kThreads) {
+        const int k = id / (BM / 4), c = id % (BM / 4);
+        const int gk = k0 + k, gm = bm + 4 * c;
+        int bytes = 0;
+        const float* src = p.A;
+        if (gk < p.K && gm < p.M) {
+          bytes = 4 * min(4, p.M - gm);
+          src = p.A + (long long)gk * p.lda + gm;
+        }
+        cp_async16(smem_u32(As + Tile::a_index(k, 4 * c)), src, bytes);
+      }
+    } else if constexpr (TA) {
+      // A stored K×M, any alignment: a warp copies 32 consecutive m of one k
+      constexpr int kElemsA = BK * BM;
+#pragma unroll 4
+      for (int id = tid; id < kElemsA; id += kThreads) {
+        const int k = id / BM, m = id % BM;
+        const int gk = k0 + k, gm = bm + m;
+        const bool ok = gk < p.K && gm < p.M;
+        const float* src = ok ? p.A + (long long)gk * p.lda + gm : p.A;
+        cp_async4(smem_u32(As + Tile::a_index(k, m)), src, ok ? 4 : 0);
+      }
+    }
     // A, transposed on the way in: single-float copies, a warp covering 4
     // rows × 8 consecutive k (whole 32-byte sectors of each row).
-    if constexpr (!AKM) {
+    if constexpr (!AKM && !TA) {
     constexpr int kElemsA = BM * BK;
 #pragma unroll
     for (int id = tid; id < kElemsA; id += kThreads) {
@@ -72,7 +105,21 @@ struct SimtKernel {
       cp_async4(smem_u32(As + Tile::a_index(k, m)), src, ok ? 4 : 0);
     }
     }
-    if (VEC) {
+    if constexpr (TB) {
+      // B stored N×K, transposed on the way in like A above: a warp copies
+      // 4 rows n × 8 consecutive k into eight different swizzled chunks
+      constexpr int kElemsB = BK * BN;
+#pragma unroll
+      for (int id = tid; id < kElemsB; id += kThreads) {
+        const int kl = id & 7, nl = (id >> 3) & 3, rest = id >> 5;
+        const int k = (rest % (BK / 8)) * 8 + kl;
+        const int n = (rest / (BK / 8)) * 4 + nl;
+        const int gn = bn + n, gk = k0 + k;
+        const bool ok = gn < p.N && gk < p.K;
+        const float* src = ok ? p.B + (long long)gn * p.ldb + gk : p.B;
+        cp_async4(smem_u32(Bs + Tile::b_index(k, n)), src, ok ? 4 : 0);
+      }
+    } else if (VEC) {
       constexpr int kChunksB = BK * BN / 4;
 #pragma unroll
       for (int id = tid; id < kChunksB; id += kThreads) {
@@ -99,8 +146,12 @@ struct SimtKernel {
     }
   }
 
-  static __device__ __forceinline__ void run(const Problem& p, int tiles_m,
+  static __device__ __forceinline__ void run(Problem p, int tiles_m,
                                              int tiles_n, int c_vec) {
+    // matrix blockIdx.z of a strided batch
+    p.A += blockIdx.z * p.sA;
+    p.B += blockIdx.z * p.sB;
+    p.C += blockIdx.z * p.sC;
     extern __shared__ unsigned char smem_raw[];
     float* smem = reinterpret_cast<float*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -147,28 +198,44 @@ struct SimtKernel {
   }
 };
 
-template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB, bool AKM>
+template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB, bool AKM,
+          bool TA, bool TB>
 __global__ void __launch_bounds__(FfmaTileT<BM, BN, BK>::kThreads, MINB)
     simt_gemm_kernel(Problem p, int tiles_m, int tiles_n, int c_vec) {
-  SimtKernel<BM, BN, BK, STAGES, VEC, AKM>::run(p, tiles_m, tiles_n, c_vec);
+  SimtKernel<BM, BN, BK, STAGES, VEC, AKM, TA, TB>::run(p, tiles_m, tiles_n,
+                                                        c_vec);
 }
 
 namespace {
 
 template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB,
-          bool AKM = false>
+          bool AKM = false, bool TA = false, bool TB = false>
 cudaError_t launch_cfg(const Problem& p, bool c_vec, cudaStream_t stream) {
-  using K = SimtKernel<BM, BN, BK, STAGES, VEC, AKM>;
-  auto fn = simt_gemm_kernel<BM, BN, BK, STAGES, VEC, MINB, AKM>;
+  using K = SimtKernel<BM, BN, BK, STAGES, VEC, AKM, TA, TB>;
+  auto fn = simt_gemm_kernel<BM, BN, BK, STAGES, VEC, MINB, AKM, TA, TB>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(fn),
                                    K::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
   const long long grid = (long long)tiles_m * tiles_n;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fn<<<(unsigned)grid, K::kThreads, K::kSmemBytes, stream>>>(p, tiles_m,
-                                                             tiles_n, c_vec);
+  if (grid > 0x7fffffffLL || p.batch < 1 || p.batch > 65535)
+    return cudaErrorInvalidConfiguration;
+  fn<<<dim3((unsigned)grid, 1, (unsigned)p.batch), K::kThreads, K::kSmemBytes,
+       stream>>>(p, tiles_m, tiles_n, c_vec);
   return cudaGetLastError();
+}
+
+// Transposed operands: one tile configuration (128 x 128 x 32, 4 stages).
+template <bool VEC>
+cudaError_t launch_trans(const Problem& p, bool c_vec, cudaStream_t stream) {
+  if (p.transA && p.transB)
+    return launch_cfg<128, 128, 32, 4, VEC, 1, false, true, true>(p, c_vec,
+                                                                  stream);
+  if (p.transA)
+    return launch_cfg<128, 128, 32, 4, VEC, 1, false, true, false>(p, c_vec,
+                                                                   stream);
+  return launch_cfg<128, 128, 32, 4, VEC, 1, false, false, true>(p, c_vec,
+                                                                 stream);
 }
 
 template <bool VEC>
@@ -208,6 +275,9 @@ cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
 
 cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
                         cudaStream_t stream) {
+  if (p.transA || p.transB)
+    return vec ? launch_trans<true>(p, c_vec, stream)
+               : launch_trans<false>(p, c_vec, stream);
   return vec ? launch_vec<true>(p, cfg, c_vec, stream)
              : launch_vec<false>(p, cfg, c_vec, stream);
 }

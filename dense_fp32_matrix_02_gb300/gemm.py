@@ -53,6 +53,9 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_ex.argtypes = args + [ci]
         L.gemm_f32_ws.restype = ci
         L.gemm_f32_ws.argtypes = args[:-1] + [vp, i64, vp]
+        L.gemm_f32_batched.restype = ci
+        L.gemm_f32_batched.argtypes = [ci, ci, i64, i64, i64, vp, i64, i64,
+                                       vp, i64, i64, vp, i64, i64, i64, vp]
         L.gemm_f32_host.restype = ci
         L.gemm_f32_host.argtypes = args[:-1] + [vp, vp, vp, vp, i64, vp]
         L.gemm_f32_noalloc.restype = ci
@@ -119,6 +122,72 @@ def gemm_f32_noalloc_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,
                                 int(lda), b_ptr or None, int(ldb),
                                 c_ptr or None, int(ldc), stream or None)
     _check(st, "gemm_f32_noalloc")
+
+
+OP_N, OP_T = 0, 1
+
+
+def gemm_f32_batched_ptr(opA, opB, M, N, K, a_ptr, lda, sA, b_ptr, ldb, sB,
+                         c_ptr, ldc, sC, batch, stream=0):
+    """Raw-pointer gemm_f32_batched call."""
+    st = lib().gemm_f32_batched(int(opA), int(opB), int(M), int(N), int(K),
+                                a_ptr or None, int(lda), int(sA),
+                                b_ptr or None, int(ldb), int(sB),
+                                c_ptr or None, int(ldc), int(sC), int(batch),
+                                stream or None)
+    _check(st, "gemm_f32_batched")
+
+
+def gemm_f32_batched(a, b, c=None, trans_a=False, trans_b=False,
+                     stream=None):
+    """C[i] = op(A[i]) · op(B[i]) for 3-D CUDA tensors (batch, rows, cols).
+
+    op(X) is X or, with trans_*, X transposed (read in place, no copy).  A
+    2-D operand is used for every product (stride 0).
+    """
+    import torch
+
+    def views(t, name):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or \
+                not t.is_cuda:
+            raise TypeError(f"{name} must be a float32 CUDA tensor")
+        if t.dim() == 2:
+            t = t.unsqueeze(0).expand(1, *t.shape)
+            stride0 = 0
+        elif t.dim() == 3:
+            stride0 = t.stride(0) if t.shape[0] > 1 else 0
+        else:
+            raise ValueError(f"{name} must be 2-D or 3-D")
+        rows, cols = t.shape[1], t.shape[2]
+        if cols > 1 and t.stride(2) != 1:
+            raise ValueError(f"{name} must be row-major")
+        ld = t.stride(1) if rows > 1 else max(cols, 1)
+        return t, rows, cols, max(ld, cols, 1), stride0
+
+    a3, ar, ac, lda, sA = views(a, "a")
+    b3, br, bc, ldb, sB = views(b, "b")
+    M, K = (ac, ar) if trans_a else (ar, ac)
+    K2, N = (bc, br) if trans_b else (br, bc)
+    if K != K2:
+        raise ValueError("inner sizes differ")
+    batch = max(a3.shape[0] if a.dim() == 3 else 1,
+                b3.shape[0] if b.dim() == 3 else 1)
+    if c is None:
+        c = torch.empty((batch, M, N), dtype=torch.float32, device=a.device)
+    c3, cr, cc, ldc, sC = views(c, "c")
+    if (cr, cc) != (M, N) or (c.dim() == 3 and c.shape[0] != batch):
+        raise ValueError("c has the wrong shape")
+    if batch > 1 and sC == 0:
+        raise ValueError("c must hold one matrix per product")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    with torch.cuda.device(a.device):
+        gemm_f32_batched_ptr(OP_T if trans_a else OP_N,
+                             OP_T if trans_b else OP_N, M, N, K,
+                             a3.data_ptr(), lda, sA, b3.data_ptr(), ldb, sB,
+                             c3.data_ptr(), ldc, sC, batch, handle)
+    return c
 
 
 def gemm_f32_host(a, b, c, da, db, dc, workspace=None, stream=None):

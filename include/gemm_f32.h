@@ -100,6 +100,33 @@ GEMM_F32_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, in
                 const float *B, int64_t ldb, float *C, int64_t ldc,
                 gemm_f32_stream_t stream, int algo);
 
+/* Operand forms for gemm_f32_batched. */
+typedef enum {
+    GEMM_F32_OP_N = 0, /* the operand as stored */
+    GEMM_F32_OP_T = 1  /* the operand's transpose (no copy is made) */
+} gemm_f32_op;
+
+/*
+ * Strided batch of products with optional transposes, without copies:
+ *   for b in [0, batch):  C_b = op(A_b) · op(B_b)
+ * where X_b = X + b·strideX (elements).  op(A) is M×K: with opA = N, A_b is
+ * stored M×K row-major (lda >= K); with opA = T it is stored K×M (lda >= M)
+ * and used transposed.  op(B) is K×N: stored K×N (ldb >= N) or, with
+ * opB = T, N×K (ldb >= K).  C_b is M×N (ldc >= N).  Strides may be 0 (the
+ * same operand for every product); output matrices must not overlap.
+ * batch = 0, M = 0 or N = 0 launches nothing; batch <= 65535.  Kernel
+ * choice as for gemm_f32: the 3xTF32 tensor kernel where its layouts allow
+ * (16-byte aligned operands, leading dimensions and strides multiples of 4,
+ * forms NN, NT and TT), the FFMA kernel otherwise.  Within the tolerance of
+ * gemm_f32 for every form.
+ */
+GEMM_F32_API int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N,
+                                  int64_t K, const float *A, int64_t lda,
+                                  int64_t strideA, const float *B, int64_t ldb,
+                                  int64_t strideB, float *C, int64_t ldc,
+                                  int64_t strideC, int64_t batch,
+                                  gemm_f32_stream_t stream);
+
 /*
  * As gemm_f32 (automatic kernel choice), with caller-owned device scratch
  * that the library may use to split K over several CTAs per tile when the

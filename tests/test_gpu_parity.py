@@ -545,3 +545,91 @@ def test_tma_ffma_timeout_path_reports_and_recovers():
         G.set_wait_timeout_ns(old_t)
     check_full(a, b, run_gpu(a, b, G.ALGO_TMA, pad=True), what="tma after")
     assert G.device_status() == 0
+
+
+# ------------------------------------------------------------- batched, op
+def _batched_case(form, M, N, K, batch, seed, gap=0, dist="uniform",
+                  broadcast_b=False):
+    """Operands stored as the form says, with `gap` extra floats between
+    rows and matrices; returns (host A list, host B list, device views)."""
+    rng_seed = seed
+    As, Bs = [], []
+    for i in range(batch):
+        a, b = synth.make_operands(M, N, K, seed=rng_seed + i, dist_a=dist,
+                                   dist_b=dist)
+        As.append(a)
+        Bs.append(Bs[0] if (broadcast_b and i) else b)
+    ta, tb = form[0] == "T", form[1] == "T"
+    a_store = [x.T.copy() if ta else x for x in As]      # stored shapes
+    b_store = [x.T.copy() if tb else x for x in Bs]
+    ra, ca = a_store[0].shape
+    rb, cb = b_store[0].shape
+    lda, ldb = ca + gap, cb + gap
+    sA, sB = ra * lda + gap, rb * ldb + gap
+    bufA = torch.full((batch * sA + 1,), float("nan"), device=DEV)
+    nb = 1 if broadcast_b else batch
+    bufB = torch.full((nb * sB + 1,), float("nan"), device=DEV)
+    for i in range(batch):
+        bufA[i * sA:i * sA + ra * lda].view(ra, lda)[:, :ca] = \
+            torch.from_numpy(a_store[i]).to(DEV)
+    for i in range(nb):
+        bufB[i * sB:i * sB + rb * ldb].view(rb, ldb)[:, :cb] = \
+            torch.from_numpy(b_store[i]).to(DEV)
+    ldc, sC = N + gap, M * (N + gap) + gap
+    bufC = torch.full((batch * sC + 1,), -7.0, device=DEV)
+    G.gemm_f32_batched_ptr(int(ta), int(tb), M, N, K, bufA.data_ptr(), lda, sA,
+                           bufB.data_ptr(), ldb, 0 if broadcast_b else sB,
+                           bufC.data_ptr(), ldc, sC, batch,
+                           torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    host = bufC.cpu().numpy()
+    Cs = [host[i * sC:i * sC + M * ldc].reshape(M, ldc) for i in range(batch)]
+    return As, Bs, Cs, host, sC, ldc
+
+
+@pytest.mark.parametrize("form", ["NN", "NT", "TN", "TT"])
+@pytest.mark.parametrize("shape,batch,gap", [((300, 260, 77), 3, 0),
+                                             ((129, 65, 33), 2, 3),
+                                             ((64, 64, 64), 4, 4),
+                                             ((256, 384, 512), 2, 0),
+                                             ((1, 1, 1), 1, 0)])
+def test_batched_forms(form, shape, batch, gap):
+    M, N, K = shape
+    As, Bs, Cs, host, sC, ldc = _batched_case(form, M, N, K, batch, seed=M,
+                                              gap=gap)
+    for i in range(batch):
+        check_full(As[i], Bs[i], Cs[i][:, :N], what=f"{form} b{i} {shape}")
+        assert (Cs[i][:, N:] == -7.0).all()          # row padding untouched
+    if gap:
+        for i in range(batch):                       # gaps between matrices
+            assert (host[i * sC + M * ldc:(i + 1) * sC] == -7.0).all()
+    Ai, Bi, Ci, _, _, _ = _batched_case(form, M, N, K, batch, seed=K,
+                                        gap=gap, dist="int")
+    for i in range(batch):
+        check_full(Ai[i], Bi[i], Ci[i][:, :N], exact=True,
+                   what=f"{form} b{i} {shape} int")
+    assert G.device_status() == 0
+
+
+def test_batched_broadcast_operand():
+    As, Bs, Cs, _, _, _ = _batched_case("NT", 200, 150, 96, 5, seed=1,
+                                        broadcast_b=True)
+    for i in range(5):
+        check_full(As[i], Bs[i], Cs[i][:, :150], what=f"broadcast {i}")
+
+
+def test_batched_binding_and_empty_batch():
+    a = torch.from_numpy(np.stack([synth.make_operands(70, 40, 50, seed=i)[0]
+                                   for i in range(3)])).to(DEV)
+    b = torch.from_numpy(synth.make_operands(1, 60, 50, seed=9)[1].T.copy()
+                         ).to(DEV)                      # 60 x 50, used as B^T
+    c = G.gemm_f32_batched(a, b, trans_b=True)
+    torch.cuda.synchronize()
+    bt = b.cpu().numpy().T.copy()
+    for i in range(3):
+        check_full(a[i].cpu().numpy(), bt, c[i].cpu().numpy(), what=f"bind {i}")
+    G.gemm_f32_batched_ptr(0, 0, 4, 4, 4, 8, 4, 16, 8, 4, 16, 8, 4, 16, 0)
+    with pytest.raises(G.GemmError):
+        G.gemm_f32_batched_ptr(2, 0, 4, 4, 4, 8, 4, 16, 8, 4, 16, 8, 4, 16, 1)
+    with pytest.raises(G.GemmError):                   # lda < M for op T
+        G.gemm_f32_batched_ptr(1, 0, 8, 4, 4, 8, 4, 32, 8, 4, 16, 8, 4, 32, 1)
