@@ -45,6 +45,10 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="sq4096")
     p.add_argument("--algo", default="auto", choices=list(ALGOS))
+    p.add_argument("--op", default="nn", choices=["nn", "nt", "tn", "tt"],
+                   help="operand forms (gemm_f32_batched); nn = plain")
+    p.add_argument("--batch", type=int, default=1,
+                   help="independent products per step (gemm_f32_batched)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -272,7 +276,30 @@ def run_ours(args, w, config):
     ws = torch.empty(max(ws_bytes // 4, 1), device=dev) if ws_bytes else None
     launches_per_step = 2 if ws_bytes else 1
 
+    batched = args.op != "nn" or args.batch > 1
+    if batched:
+        # stored operands: A as K x M when op(A) = T, B as N x K when
+        # op(B) = T; `batch` copies laid out back to back
+        ta_, tb_ = args.op[0] == "t", args.op[1] == "t"
+        sa = torch.from_numpy(a.T.copy() if ta_ else a).to(dev)
+        sb = torch.from_numpy(b.T.copy() if tb_ else b).to(dev)
+        bA = sa.unsqueeze(0).repeat(args.batch, 1, 1)
+        bB = sb.unsqueeze(0).repeat(args.batch, 1, 1)
+        bsets = [(bA, bB, torch.empty(args.batch, w.M, w.N, device=dev))]
+        for _ in range(nsets - 1):
+            bsets.append((bA.clone(), bB.clone(),
+                          torch.empty(args.batch, w.M, w.N, device=dev)))
+        launches_per_step = 1
+
+    if batched:  # the tensor kernel takes NN/NT/TT, the FFMA kernel TN
+        ran = 1 if args.op == "tn" else 3
+
     def step(i):
+        if batched:
+            xa, xb, xc = bsets[i % nsets]
+            G.gemm_f32_batched(xa, xb, xc, trans_a=ta_, trans_b=tb_,
+                               stream=stream)
+            return
         ta, tb, tc = sets[i % nsets]
         if algo == 0:
             G.gemm_f32_ws_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K,
@@ -316,7 +343,7 @@ def run_ours(args, w, config):
     if G.device_status() != 0:
         raise SystemExit("kernel status word set during the timed region")
 
-    flops = float(w.flops)
+    flops = float(w.flops) * args.batch
     value = weak_scaling_value(flops, args.steps, world, ms_max)
     # one GEMM launch per step (plus the split-K reduction when it splits);
     # launch gaps are included
@@ -326,6 +353,10 @@ def run_ours(args, w, config):
     # (gemm_f32_host: B, then row chunks of A copied in while earlier
     # chunks are multiplied and their C copied back; forced kernels go
     # through gemm_f32_ex between plain copies)
+    if batched:
+        hba = bsets[0][0].cpu().pin_memory()
+        hbb = bsets[0][1].cpu().pin_memory()
+        hbc = torch.empty(args.batch, w.M, w.N).pin_memory()
     ha = torch.from_numpy(a).pin_memory()
     hb = torch.from_numpy(b).pin_memory()
     hc = torch.empty(w.M, w.N, dtype=torch.float32).pin_memory()
@@ -333,6 +364,14 @@ def run_ours(args, w, config):
     e_steps = max(1, args.e2e_steps)
 
     def e2e_step():
+        if batched:  # host copies of every operand, then the batched call
+            xa, xb, xc = bsets[0]
+            xa.copy_(hba, non_blocking=True)
+            xb.copy_(hbb, non_blocking=True)
+            G.gemm_f32_batched(xa, xb, xc, trans_a=ta_, trans_b=tb_,
+                               stream=stream)
+            hbc.copy_(xc, non_blocking=True)
+            return
         if algo == 0:
             G.gemm_f32_host(ha, hb, hc, ea, eb, ec, workspace=ws,
                             stream=stream)
@@ -384,7 +423,7 @@ def run_ours(args, w, config):
                 "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes "
                                f"x 2 flop x {smax:.0f} MHz (max SM clock)"}
     roof["traffic"] = recorded_traffic(algo_name, w.name)
-    roof["algorithmic_bytes"] = w.bytes
+    roof["algorithmic_bytes"] = w.bytes * args.batch
     roof["kernel_ms"] = kernel_ms
 
     fp32_roof = min(fp32_peak, (flops / w.bytes) * peaks["hbm_gbs"] / 1e3)
@@ -399,8 +438,8 @@ def run_ours(args, w, config):
         "fp32_roofline_tflops": fp32_roof,
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
-                "d2h_bytes_per_step": 4 * w.M * w.N},
+                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N) * args.batch,
+                "d2h_bytes_per_step": 4 * w.M * w.N * args.batch},
         "gpu_launches": args.steps * launches_per_step,
         "split_k_workspace_bytes": ws_bytes,
         "clocks": clocks,
@@ -421,6 +460,7 @@ def main():
     dist_txt = {"uniform": "uniform [-1,1)", "normal": "normal",
                 "int": "integers {-2..2}"}
     config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+              "op": args.op, "batch": args.batch,
               "layout": "row-major, ld = row width",
               "inputs": f"A {dist_txt[w.dist_a]} (sigma {w.sigma_a}), "
                         f"B {dist_txt[w.dist_b]} (sigma {w.sigma_b}), "

@@ -343,7 +343,36 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
                    mult4(sA) && mult4(sB);
   const bool c_vec = aligned16(C) && mult4(ldc) && mult4(sC);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  e = launch_simt(p, choose_simt_cfg(M, N, *d), vec, c_vec, s);
+  // The tensor kernel takes NN, NT and TT (TN has no copy-free mapping onto
+  // its operand layouts) when TMA can describe every operand: aligned, and
+  // batch strides 0 or at least one whole stored matrix.
+  const int64_t rows_a = ta ? K : M, rows_b = tb ? N : K;
+  const bool strides_ok = (batch == 1) ||
+                          ((sA == 0 || sA >= rows_a * lda) &&
+                           (sB == 0 || sB >= rows_b * ldb));
+  if (d->cc_major == 10 && vec && K >= 1 && !(ta && !tb) && strides_ok &&
+      env_int("GEMM_F32_AUTO_SIMT", 0) == 0) {
+    Problem q = p;
+    if (ta && tb) {  // C = (B·A)ᵀ: swap the operands, store the transpose
+      q.M = p.N;
+      q.N = p.M;
+      q.A = B;
+      q.lda = ldb;
+      q.sA = sB;
+      q.B = A;
+      q.ldb = lda;
+      q.sB = sA;
+      q.transA = 1;  // marks the swapped form
+      q.transB = 0;
+    }
+    WaitCfg wc;
+    wc.limit = g_wait_ns.load();
+    wc.debug = g_debug_flags.load();
+    wc.status = d->status;
+    e = launch_tf32x3(q, kTc128Raw, 1, nullptr, wc, s);
+  } else {
+    e = launch_simt(p, choose_simt_cfg(M, N, *d), vec, c_vec, s);
+  }
   if (e != cudaSuccess) return fail_cuda(e);
   return GEMM_F32_OK;
 }

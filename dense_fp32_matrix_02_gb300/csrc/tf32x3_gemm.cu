@@ -57,8 +57,15 @@ namespace tf32x3 {
 
 // Tile configuration.  TILE_M rows of C per CTA (the MMA's N), always 128
 // columns (the MMA's M = TMEM lanes), STAGES-deep ring of 16-deep k stages.
-template <int TILE_M, int STAGES, bool RAW_BIG>
+// TB: B is stored transposed (N×K, K-contiguous); its tile arrives as
+// 128 rows n of 16 k (64-byte swizzle) and a converter lane reads its own
+// row instead of a column.  TSTORE: the product computed is Cᵀ and is
+// stored transposed (used for op(A)ᵀ·op(B)ᵀ = (B·A)ᵀ with A, B swapped).
+template <int TILE_M, int STAGES, bool RAW_BIG, bool TB = false,
+          bool TSTORE = false>
 struct Cfg {
+  static constexpr bool kTB = TB;
+  static constexpr bool kTStore = TSTORE;
   // RAW_BIG: the MMAs read the raw fp32 operands as their "big" part and the
   // tensor core keeps their top 19 bits (TF32 truncation); converters then
   // write only small = x - trunc(x).  Otherwise big is rounded to the
@@ -83,6 +90,7 @@ struct Cfg {
   static_assert(kTmemNeed <= kTmemCols, "TMEM budget");
   static_assert(TILE_M % 16 == 0 && TILE_M >= 64 && TILE_M <= 256,
                 "MMA N in [64, 256], multiple of 16");
+  static_assert(!TB || RAW_BIG, "transposed B only with the raw split");
 };
 
 constexpr int kMaxStages = 8;
@@ -159,7 +167,11 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                        const __grid_constant__ CUtensorMap tmap_b, float* C,
                        long long ldc, int M, int N, int K, int tiles_m,
                        int tiles_n, int splits, int kb_per_split,
-                       float* partials, WaitCfg wc) {
+                       float* partials, long long sC, int batched_ab,
+                       WaitCfg wc) {
+  // batch: matrix blockIdx.z; tensor-map batch coordinates are z for a
+  // batched operand and 0 for one shared by every product (batched_ab bits
+  // 0 = A, 1 = B); C advances by sC per product.
   constexpr int kTileM = Cf::kTileM, kTileN = Cf::kTileN, kBK = Cf::kBK;
   constexpr int kStages = Cf::kStages, kConvWarps = Cf::kConvWarps;
   constexpr int kAccCols = Cf::kAccCols, kTmemCols = Cf::kTmemCols;
@@ -186,7 +198,9 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   const int nk_total = (K + kBK - 1) / kBK;
   const int kb0 = split * kb_per_split;
   const int nk = min(nk_total, kb0 + kb_per_split) - kb0;  // >= 1 (host)
-  float* out = C;
+  const int z = blockIdx.z;
+  const int za = (batched_ab & 1) ? z : 0, zb = (batched_ab & 2) ? z : 0;
+  float* out = C + z * sC;
   long long ldo = ldc;
   if (splits > 1) {
     out = partials + (long long)split * M * N;
@@ -236,10 +250,14 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
             break;
           }
           mbar_arrive_expect_tx(full(s), kStageBytesA + kStageBytesB);
-          tma_load_2d(sbase + s * kStageBytesA, &tmap_a, full(s),
-                      (kb0 + kb) * kBK, bm);
-          tma_load_2d(sbase + kOffB + s * kStageBytesB, &tmap_b, full(s), bn,
-                      (kb0 + kb) * kBK);
+          tma_load_3d(sbase + s * kStageBytesA, &tmap_a, full(s),
+                      (kb0 + kb) * kBK, bm, za);
+          if constexpr (Cf::kTB)
+            tma_load_3d(sbase + kOffB + s * kStageBytesB, &tmap_b, full(s),
+                        (kb0 + kb) * kBK, bn, zb);
+          else
+            tma_load_3d(sbase + kOffB + s * kStageBytesB, &tmap_b, full(s),
+                        bn, (kb0 + kb) * kBK, zb);
           ++issued;
         }
       }
@@ -311,11 +329,27 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
           reinterpret_cast<float4*>(smem + kOffASmall + s * kStageBytesA);
       constexpr int kChunksPerThread = kStageBytesA / 16 / (32 * kConvWarps);
       if constexpr (Cf::kRawBig) {
+        float x[8];
+        if constexpr (Cf::kTB) {
+          // row n_loc of the stored Bᵀ tile: 64-byte rows, 16-byte chunk c
+          // at c ^ ((row >> 1) & 3); this warp's k-slice is chunks 2h, 2h+1
+          const unsigned char* brow =
+              smem + kOffB + s * kStageBytesB + n_loc * 64;
+          const int sw = (n_loc >> 1) & 3;
+          const float4 v0 = *reinterpret_cast<const float4*>(
+              brow + (((2 * h) ^ sw) << 4));
+          const float4 v1 = *reinterpret_cast<const float4*>(
+              brow + (((2 * h + 1) ^ sw) << 4));
+          x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+          x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[k] = bcol[k * kTileN];
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float x = bcol[k * kTileN];
-          big[k] = __float_as_uint(x);
-          small[k] = tf32_small_of_truncated(x);
+          big[k] = __float_as_uint(x[k]);
+          small[k] = tf32_small_of_truncated(x[k]);
         }
         tmem_st8(tcol, big);
         tmem_st8(tcol + kBK, small);
@@ -371,7 +405,25 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
           uint32_t v[16];
           tmem_ld16(tmem + lane_bits + c0, v);
           tmem_ld_wait();
-          if (n < N) {
+          if constexpr (Cf::kTStore) {
+            // this lane holds 16 consecutive rows m of column n: they are
+            // 16 consecutive elements of row n of the stored transpose
+            if (n < N) {
+              float* dst = out + (long long)n * ldo + bm + c0;
+              if (bm + c0 + 16 <= M &&
+                  ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4)
+                  *reinterpret_cast<float4*>(dst + i) = make_float4(
+                      __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                      __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (bm + c0 + i < M) dst[i] = __uint_as_float(v[i]);
+              }
+            }
+          } else if (n < N) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int m = bm + c0 + i;
@@ -446,6 +498,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 namespace {
 
+// 3-D tensor map (x innermost, y rows, z batch) of fp32 with a box of
+// bx × by × 1.  A batch stride of 0 (one matrix shared by every product)
+// gives a batch extent of 1.
+bool encode_3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
+               const float* base, long long x, long long y, long long ld,
+               long long stride, int batch, int bx, int by,
+               CUtensorMapSwizzle swz) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const bool batched = batch > 1 && stride != 0;
+  const cuuint64_t dims[3] = {(cuuint64_t)x, (cuuint64_t)y,
+                              (cuuint64_t)(batched ? batch : 1)};
+  const long long zs = batched ? stride : (y * ld + 3) / 4 * 4;
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)zs * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)bx, (cuuint32_t)by, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                const_cast<float*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <class Cf>
 cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
                        const WaitCfg& wc, cudaStream_t stream) {
@@ -453,29 +526,15 @@ cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
-  const cuuint32_t estr[2] = {1, 1};
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.lda * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)Cf::kBK, (cuuint32_t)Cf::kTileM};
-    if (encode(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-               const_cast<float*>(p.A), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.K};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.ldb * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)Cf::kTileN, (cuuint32_t)Cf::kBK};
-    if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-               const_cast<float*>(p.B), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!encode_3d(encode, &ta, p.A, p.K, p.M, p.lda, p.sA, p.batch, Cf::kBK,
+                 Cf::kTileM, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  const bool ok_b =
+      Cf::kTB ? encode_3d(encode, &tb, p.B, p.K, p.N, p.ldb, p.sB, p.batch,
+                          Cf::kBK, Cf::kTileN, CU_TENSOR_MAP_SWIZZLE_64B)
+              : encode_3d(encode, &tb, p.B, p.N, p.K, p.ldb, p.sB, p.batch,
+                          Cf::kTileN, Cf::kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!ok_b) return cudaErrorInvalidValue;
   auto fn = tf32x3_gemm_kernel<Cf>;
   constexpr int kSmem = smem_bytes<Cf>();
   cudaError_t e =
@@ -484,14 +543,17 @@ cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
   const int tiles_m = (p.M + Cf::kTileM - 1) / Cf::kTileM;
   const int tiles_n = (p.N + Cf::kTileN - 1) / Cf::kTileN;
   const int nk = (p.K + Cf::kBK - 1) / Cf::kBK;
-  if (splits < 1 || !partials) splits = 1;
+  if (splits < 1 || !partials || p.batch > 1) splits = 1;
   const int kb_per_split = (nk + splits - 1) / splits;
   splits = (nk + kb_per_split - 1) / kb_per_split;  // no empty split
   const long long grid = (long long)tiles_m * tiles_n * splits;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fn<<<(unsigned)grid, Cf::kThreads, kSmem, stream>>>(
-      ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, splits,
-      kb_per_split, partials, wc);
+  if (grid > 0x7fffffffLL || p.batch < 1 || p.batch > 65535)
+    return cudaErrorInvalidConfiguration;
+  const int batched_ab =
+      (p.batch > 1 && p.sA != 0 ? 1 : 0) | (p.batch > 1 && p.sB != 0 ? 2 : 0);
+  fn<<<dim3((unsigned)grid, 1, (unsigned)p.batch), Cf::kThreads, kSmem,
+       stream>>>(ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, splits,
+                 kb_per_split, partials, p.sC, batched_ab, wc);
   e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
@@ -527,6 +589,12 @@ cudaError_t launch_tf32x3(const Problem& p, int cfg, int splits,
     case kTc128:
       return launch_cfg<Cfg<128, 4, false>>(p, splits, partials, wc, stream);
     case kTc128Raw:
+      if (p.transB)  // A·Bᵀ with B stored N×K
+        return launch_cfg<Cfg<128, 4, true, true>>(p, splits, partials, wc,
+                                                   stream);
+      if (p.transA)  // caller passed (B, A) swapped: store the transpose
+        return launch_cfg<Cfg<128, 4, true, false, true>>(p, splits, partials,
+                                                          wc, stream);
       return launch_cfg<Cfg<128, 4, true>>(p, splits, partials, wc, stream);
     case kTc256Raw:
       return launch_cfg<Cfg<256, 5, true>>(p, splits, partials, wc, stream);

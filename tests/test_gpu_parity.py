@@ -633,3 +633,23 @@ def test_batched_binding_and_empty_batch():
         G.gemm_f32_batched_ptr(2, 0, 4, 4, 4, 8, 4, 16, 8, 4, 16, 8, 4, 16, 1)
     with pytest.raises(G.GemmError):                   # lda < M for op T
         G.gemm_f32_batched_ptr(1, 0, 8, 4, 4, 8, 4, 32, 8, 4, 16, 8, 4, 32, 1)
+
+
+@pytest.mark.parametrize("form", ["NN", "NT", "TN", "TT"])
+def test_batched_forms_forced_simt(form):
+    """The FFMA path for every form (the tensor path takes NN/NT/TT when
+    the layouts allow; here every form runs on the FFMA kernel)."""
+    with _env("GEMM_F32_AUTO_SIMT", 1):
+        As, Bs, Cs, _, _, _ = _batched_case(form, 300, 260, 77, 3, seed=11,
+                                            gap=0)
+    for i in range(3):
+        check_full(As[i], Bs[i], Cs[i][:, :260], what=f"simt {form} b{i}")
+
+
+@pytest.mark.parametrize("form", ["NT", "TT"])
+def test_transposed_forms_large_sampled(form):
+    """op forms at 2048 x 1536 x 1024, sampled against the oracle."""
+    M, N, K = 2048, 1536, 1024
+    As, Bs, Cs, _, _, _ = _batched_case(form, M, N, K, 1, seed=5)
+    check_sampled_and_rowsums(As[0], Bs[0], np.ascontiguousarray(Cs[0][:, :N]),
+                              what=f"{form} large")
