@@ -49,6 +49,10 @@ def parse_args():
                    help="operand forms (gemm_f32_batched); nn = plain")
     p.add_argument("--batch", type=int, default=1,
                    help="independent products per step (gemm_f32_batched)")
+    p.add_argument("--epilogue", default="none",
+                   choices=["none", "bias", "bias_gelu"],
+                   help="fused epilogue C = act(A·B + bias) "
+                        "(gemm_f32_bias_act)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -247,6 +251,7 @@ def run_ours(args, w, config):
     import torch.distributed as dist
 
     from dense_fp32_matrix_02_gb300 import gemm as G
+    from dense_fp32_matrix_02_gb300 import synth
 
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -294,7 +299,21 @@ def run_ours(args, w, config):
     if batched:  # the tensor kernel takes NN/NT/TT, the FFMA kernel TN
         ran = 1 if args.op == "tn" else 3
 
+    fused = args.epilogue != "none"
+    if fused:
+        ebias = torch.from_numpy(
+            synth.make_operands(1, w.N, 1, seed=7)[1][0]).to(dev)
+        eact = 1 if args.epilogue == "bias_gelu" else 0
+
     def step(i):
+        if fused:
+            ta, tb, tc = sets[i % nsets]
+            G.gemm_f32_bias_act_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K,
+                                    tb.data_ptr(), w.N, ebias.data_ptr(),
+                                    eact, tc.data_ptr(), w.N,
+                                    ws.data_ptr() if ws is not None else 0,
+                                    ws_bytes, handle)
+            return
         if batched:
             xa, xb, xc = bsets[i % nsets]
             G.gemm_f32_batched(xa, xb, xc, trans_a=ta_, trans_b=tb_,
@@ -461,6 +480,7 @@ def main():
                 "int": "integers {-2..2}"}
     config = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
               "op": args.op, "batch": args.batch,
+              "epilogue": args.epilogue,
               "layout": "row-major, ld = row width",
               "inputs": f"A {dist_txt[w.dist_a]} (sigma {w.sigma_a}), "
                         f"B {dist_txt[w.dist_b]} (sigma {w.sigma_b}), "

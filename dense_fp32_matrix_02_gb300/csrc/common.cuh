@@ -36,7 +36,20 @@ struct Problem {
   long long sA = 0, sB = 0, sC = 0;  // batch strides (elements)
   int batch = 1;
   int transA = 0, transB = 0;
+  // fused epilogue: C = act(A·B + bias), bias indexed by column (or NULL)
+  const float* bias = nullptr;
+  int act = 0;  // 0 identity, 1 GELU
 };
+
+enum : int { kActNone = 0, kActGelu = 1 };
+
+// act(v + bias[col]): GELU(x) = x·Φ(x) = x/2·(1 + erf(x/√2)).
+__device__ __forceinline__ float apply_epilogue(float v, const float* bias,
+                                                int act, int col) {
+  if (bias) v += bias[col];
+  if (act == kActGelu) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+  return v;
+}
 
 // Bounded-wait configuration shared by all pipelined kernels.
 struct WaitCfg {

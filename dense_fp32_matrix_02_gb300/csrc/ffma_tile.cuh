@@ -107,15 +107,20 @@ struct FfmaTile {
                                         bool c_vec,
                                         const float (&acc)[8][8]) const {
     const bool interior = (bm + BM <= p.M) && (bn + BN <= p.N);
+    const bool epi = p.bias != nullptr || p.act != kActNone;
+    auto val = [&](int i, int j, int col) {
+      return epi ? apply_epilogue(acc[i][j], p.bias, p.act, col) : acc[i][j];
+    };
     if (interior && c_vec) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float* crow = p.C + (long long)(bm + row0 + 8 * i) * p.ldc + bn + col0;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
+          const int c = bn + col0 + 16 * g;
           *reinterpret_cast<float4*>(crow + 16 * g) =
-              make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2],
-                          acc[i][4 * g + 3]);
+              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
         }
       }
       return;
@@ -130,12 +135,12 @@ struct FfmaTile {
         const int c = bn + col0 + 16 * g;
         if (c_vec && c + 3 < p.N) {
           *reinterpret_cast<float4*>(crow + c) =
-              make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2],
-                          acc[i][4 * g + 3]);
+              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (c + j < p.N) crow[c + j] = acc[i][4 * g + j];
+            if (c + j < p.N) crow[c + j] = val(i, 4 * g + j, c + j);
         }
       }
     }
@@ -243,15 +248,21 @@ struct FfmaTileT {
                                         bool c_vec,
                                         const float (&acc)[8][8]) const {
     const bool interior = (bm + BM <= p.M) && (bn + BN <= p.N);
+    const bool epi = p.bias != nullptr || p.act != kActNone;
+    auto val = [&](int i, int j, int col) {
+      return epi ? apply_epilogue(acc[i][j], p.bias, p.act, col) : acc[i][j];
+    };
     if (interior && c_vec) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float* crow = p.C + (long long)(bm + row_of(i)) * p.ldc + bn + col0;
 #pragma unroll
-        for (int g = 0; g < 2; ++g)
+        for (int g = 0; g < 2; ++g) {
+          const int c = bn + col0 + 16 * g;
           *reinterpret_cast<float4*>(crow + 16 * g) =
-              make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2],
-                          acc[i][4 * g + 3]);
+              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
+        }
       }
       return;
     }
@@ -265,12 +276,12 @@ struct FfmaTileT {
         const int c = bn + col0 + 16 * g;
         if (c_vec && c + 3 < p.N) {
           *reinterpret_cast<float4*>(crow + c) =
-              make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2],
-                          acc[i][4 * g + 3]);
+              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (c + j < p.N) crow[c + j] = acc[i][4 * g + j];
+            if (c + j < p.N) crow[c + j] = val(i, 4 * g + j, c + j);
         }
       }
     }

@@ -206,7 +206,9 @@ namespace {
 // plan that wants more than given runs without split-K.
 int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
              const float* B, int64_t ldb, float* C, int64_t ldc,
-             gemm_f32_stream_t stream, int algo, void* ws, int64_t ws_bytes) {
+             gemm_f32_stream_t stream, int algo, void* ws, int64_t ws_bytes,
+             const float* bias = nullptr, int act = 0) {
+  if (act != kActNone && act != kActGelu) return GEMM_F32_ERR_INVALID_ARG;
   if (algo < GEMM_F32_ALGO_AUTO || algo > GEMM_F32_ALGO_TF32X3)
     return GEMM_F32_ERR_INVALID_ARG;
   if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return GEMM_F32_ERR_INVALID_ARG;
@@ -235,6 +237,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   p.ldb = ldb;
   p.C = C;
   p.ldc = ldc;
+  p.bias = bias;
+  p.act = act;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (plan.algo) {
     case GEMM_F32_ALGO_SIMT:
@@ -380,6 +384,15 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
 }  // namespace
 
 extern "C" {
+
+int gemm_f32_bias_act(int64_t M, int64_t N, int64_t K, const float* A,
+                      int64_t lda, const float* B, int64_t ldb,
+                      const float* bias, int act, float* C, int64_t ldc,
+                      void* workspace, int64_t workspace_bytes,
+                      gemm_f32_stream_t stream) {
+  return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, stream, GEMM_F32_ALGO_AUTO,
+                  workspace, workspace_bytes, bias, act);
+}
 
 int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
                      const float* A, int64_t lda, int64_t strideA,

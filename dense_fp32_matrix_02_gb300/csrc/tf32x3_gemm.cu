@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                        long long ldc, int M, int N, int K, int tiles_m,
                        int tiles_n, int splits, int kb_per_split,
                        float* partials, long long sC, int batched_ab,
-                       WaitCfg wc) {
+                       const float* bias, int act, WaitCfg wc) {
   // batch: matrix blockIdx.z; tensor-map batch coordinates are z for a
   // batched operand and 0 for one shared by every product (batched_ab bits
   // 0 = A, 1 = B); C advances by sC per product.
@@ -424,10 +424,14 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
               }
             }
           } else if (n < N) {
+            // fused epilogue (not on split-K partials: the reduction has it)
+            const bool epi = splits == 1 && (bias != nullptr || act != 0);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int m = bm + c0 + i;
-              if (m < M) out[(long long)m * ldo + n] = __uint_as_float(v[i]);
+              float x = __uint_as_float(v[i]);
+              if (epi) x = apply_epilogue(x, bias, act, n);
+              if (m < M) out[(long long)m * ldo + n] = x;
             }
           }
         }
@@ -448,7 +452,8 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ partials, int splits,
                          int M, int N, float* __restrict__ C, long long ldc,
-                         int vec) {
+                         int vec, const float* __restrict__ bias, int act) {
+  const bool epi = bias != nullptr || act != 0;
   const long long groups_per_row = (N + 3) / 4;
   const long long total = (long long)M * groups_per_row;
   const long long slice = (long long)M * N;
@@ -467,12 +472,18 @@ __global__ void __launch_bounds__(256)
         acc.z += v.z;
         acc.w += v.w;
       }
+      if (epi) {
+        acc.x = apply_epilogue(acc.x, bias, act, j);
+        acc.y = apply_epilogue(acc.y, bias, act, j + 1);
+        acc.z = apply_epilogue(acc.z, bias, act, j + 2);
+        acc.w = apply_epilogue(acc.w, bias, act, j + 3);
+      }
       *reinterpret_cast<float4*>(dst) = acc;
     } else {
       for (int e = 0; e < 4 && j + e < N; ++e) {
         float acc = src[e];
         for (int s = 1; s < splits; ++s) acc += src[e + s * slice];
-        dst[e] = acc;
+        dst[e] = epi ? apply_epilogue(acc, bias, act, j + e) : acc;
       }
     }
   }
@@ -553,7 +564,7 @@ cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
       (p.batch > 1 && p.sA != 0 ? 1 : 0) | (p.batch > 1 && p.sB != 0 ? 2 : 0);
   fn<<<dim3((unsigned)grid, 1, (unsigned)p.batch), Cf::kThreads, kSmem,
        stream>>>(ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, splits,
-                 kb_per_split, partials, p.sC, batched_ab, wc);
+                 kb_per_split, partials, p.sC, batched_ab, p.bias, p.act, wc);
   e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
@@ -563,8 +574,8 @@ cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
   const long long groups = (long long)p.M * ((p.N + 3) / 4);
   const int blocks = (int)((groups + 255) / 256 < 4096 ? (groups + 255) / 256
                                                       : 4096);
-  splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(partials, splits, p.M,
-                                                  p.N, p.C, p.ldc, vec);
+  splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(
+      partials, splits, p.M, p.N, p.C, p.ldc, vec, p.bias, p.act);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,9 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_ex.argtypes = args + [ci]
         L.gemm_f32_ws.restype = ci
         L.gemm_f32_ws.argtypes = args[:-1] + [vp, i64, vp]
+        L.gemm_f32_bias_act.restype = ci
+        L.gemm_f32_bias_act.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp,
+                                        ci, vp, i64, vp, i64, vp]
         L.gemm_f32_batched.restype = ci
         L.gemm_f32_batched.argtypes = [ci, ci, i64, i64, i64, vp, i64, i64,
                                        vp, i64, i64, vp, i64, i64, i64, vp]
@@ -125,6 +128,54 @@ def gemm_f32_noalloc_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,
 
 
 OP_N, OP_T = 0, 1
+ACT_NONE, ACT_GELU = 0, 1
+
+
+def gemm_f32_bias_act_ptr(M, N, K, a_ptr, lda, b_ptr, ldb, bias_ptr, act,
+                          c_ptr, ldc, ws_ptr=0, ws_bytes=0, stream=0):
+    """Raw-pointer gemm_f32_bias_act call."""
+    st = lib().gemm_f32_bias_act(int(M), int(N), int(K), a_ptr or None,
+                                 int(lda), b_ptr or None, int(ldb),
+                                 bias_ptr or None, int(act), c_ptr or None,
+                                 int(ldc), ws_ptr or None, int(ws_bytes),
+                                 stream or None)
+    _check(st, "gemm_f32_bias_act")
+
+
+def gemm_f32_bias_act(a, b, bias=None, act=ACT_NONE, c=None, workspace=None,
+                      stream=None):
+    """C = act(A·B + bias) on CUDA tensors (bias: length-N or None)."""
+    import torch
+    M, K, ap, lda = _matrix_args(a, "a")
+    K2, N, bp, ldb = _matrix_args(b, "b")
+    if K != K2:
+        raise ValueError("inner sizes differ")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    Mc, Nc, cp, ldc = _matrix_args(c, "c")
+    if (Mc, Nc) != (M, N):
+        raise ValueError("c has the wrong shape")
+    bias_ptr = 0
+    if bias is not None:
+        if not bias.is_cuda or bias.dtype != torch.float32 or \
+                bias.numel() != N or (N > 1 and bias.stride(-1) != 1):
+            raise ValueError("bias must be a contiguous float32 CUDA vector "
+                             "of N elements")
+        bias_ptr = bias.data_ptr()
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+        ws_ptr = workspace.data_ptr() if ws_bytes else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    with torch.cuda.device(a.device):
+        st = lib().gemm_f32_bias_act(M, N, K, ap or None, lda, bp or None,
+                                     ldb, bias_ptr or None, int(act),
+                                     cp or None, ldc, ws_ptr or None, ws_bytes,
+                                     handle or None)
+    _check(st, "gemm_f32_bias_act")
+    return c
 
 
 def gemm_f32_batched_ptr(opA, opB, M, N, K, a_ptr, lda, sA, b_ptr, ldb, sB,

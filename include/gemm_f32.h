@@ -100,6 +100,31 @@ GEMM_F32_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, in
                 const float *B, int64_t ldb, float *C, int64_t ldc,
                 gemm_f32_stream_t stream, int algo);
 
+/* Activations for gemm_f32_bias_act. */
+typedef enum {
+    GEMM_F32_ACT_NONE = 0,
+    /* GELU(x) = x·Φ(x) = x/2·(1 + erf(x/√2)), Φ the standard normal
+     * distribution function */
+    GEMM_F32_ACT_GELU = 1
+} gemm_f32_act;
+
+/*
+ * Fused epilogue: C = act(A·B + bias), where bias (length N, device memory,
+ * may be NULL) is added to every row.  "Rendre le GPU rapide" names the
+ * bias add fused into the matrix multiply and a separate GELU kernel among
+ * the things a tuned library does that an unfused pipeline pays for in
+ * memory passes; here both run in the multiply's epilogue (or, when K is
+ * split, in the reduction), so C is written once.  Scratch and kernel
+ * choice as for gemm_f32_ws (workspace may be NULL with 0 bytes).
+ */
+GEMM_F32_API int gemm_f32_bias_act(int64_t M, int64_t N, int64_t K,
+                                   const float *A, int64_t lda,
+                                   const float *B, int64_t ldb,
+                                   const float *bias, int act, float *C,
+                                   int64_t ldc, void *workspace,
+                                   int64_t workspace_bytes,
+                                   gemm_f32_stream_t stream);
+
 /* Operand forms for gemm_f32_batched. */
 typedef enum {
     GEMM_F32_OP_N = 0, /* the operand as stored */

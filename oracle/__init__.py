@@ -16,7 +16,9 @@ operations) and "å…±äº«å†…å­˜ä¸ŽåŒæ­¥", section "SharedArray â€”â€” é™æ€å…±äº
 Every function here is pinned by ``tests/test_oracle.py`` against things the
 pages and the mathematics fix (identities, exact integer products, exact
 rational brute force, a naive float32 loop, the 2MNK operation count and
-metamorphic relations); no function here is "parity unpinned".
+metamorphic relations; for the epilogue, tabulated values of the normal
+distribution function and the identity GELU(x) - GELU(-x) = x); no function
+here is "parity unpinned".
 """
 
 from __future__ import annotations
@@ -73,6 +75,9 @@ class Oracle:
         lib.oracle_gemm_f64_entries.restype = i64
         lib.oracle_gemm_f64_entries.argtypes = [i64, i64, i64, fp, i64, fp,
                                                 i64, i64, dp, dp, dp, dp]
+        lib.oracle_epilogue_f64.restype = ctypes.c_int
+        lib.oracle_epilogue_f64.argtypes = [i64, i64, dp, i64, fp, ctypes.c_int,
+                                            dp, i64]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self._lib = lib
@@ -129,6 +134,24 @@ class Oracle:
             raise ValueError("oracle rejected its arguments")
         return out, bound, fmas
 
+    def epilogue(self, c, bias=None, act=0):
+        """act(c + bias) in float64 for an oracle product c (MÃ—N)."""
+        c = np.ascontiguousarray(c, dtype=np.float64)
+        M, N = c.shape
+        out = np.empty_like(c)
+        b = None
+        if bias is not None:
+            b = np.ascontiguousarray(bias, dtype=np.float32)
+            if b.shape != (N,):
+                raise ValueError("bias must have N elements")
+        st = self._lib.oracle_epilogue_f64(
+            M, N, c.ctypes.data, max(N, 1),
+            b.ctypes.data if b is not None else None, int(act),
+            out.ctypes.data, max(N, 1))
+        if st != 0:
+            raise ValueError("oracle rejected its arguments")
+        return out
+
     def max_threads(self) -> int:
         return int(self._lib.oracle_max_threads())
 
@@ -148,6 +171,10 @@ def gemm(a, b, threads: int = 0, with_bound: bool = True):
 
 def entries(a, b, rows, cols):
     return load().entries(a, b, rows, cols)
+
+
+def epilogue(c, bias=None, act=0):
+    return load().epilogue(c, bias, act)
 
 
 def tolerance(bound, K: int):

@@ -175,3 +175,25 @@ int oracle_max_threads(void) {
     return 1;
 #endif
 }
+
+/*
+ * Epilogue of the fused product C = act(A·B + bias), applied to an oracle
+ * product: out[i][j] = act(C[i][j] + bias[j]) in float64 (bias may be NULL).
+ * act 0 is the identity; act 1 is GELU, x·Φ(x) = x/2·(1 + erf(x/√2)) with Φ
+ * the standard normal distribution function.  The pages name GELU (its own
+ * kernel in "Rendre le GPU rapide", "Les kernels fusionnés") and the fused
+ * bias add (same article, "Et par rapport à PyTorch ?") without a formula;
+ * this is GELU's definition.  C and out may be the same array.
+ */
+int oracle_epilogue_f64(int64_t M, int64_t N, const double *C, int64_t ldc,
+                        const float *bias, int act, double *out,
+                        int64_t ldo) {
+    if (M < 0 || N < 0 || ldc < N || ldo < N || act < 0 || act > 1) return -1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double z = C[i * ldc + j] + (bias ? (double)bias[j] : 0.0);
+            if (act == 1) z = 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+            out[i * ldo + j] = z;
+        }
+    return 0;
+}

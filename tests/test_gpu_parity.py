@@ -653,3 +653,64 @@ def test_transposed_forms_large_sampled(form):
     As, Bs, Cs, _, _, _ = _batched_case(form, M, N, K, 1, seed=5)
     check_sampled_and_rowsums(As[0], Bs[0], np.ascontiguousarray(Cs[0][:, :N]),
                               what=f"{form} large")
+
+
+# ------------------------------------------------------------- epilogue
+def _check_epilogue(a, b, bias, act, c, what):
+    """|C - act(C_ref + bias)| within GELU's slope (< 1.2) times the
+    product's tolerance plus a few float32 ulps of the epilogue itself."""
+    ref, bound, _ = oracle.gemm(a, b)
+    want = oracle.epilogue(ref, bias, act)
+    z = oracle.epilogue(ref, bias, 0)
+    K = a.shape[1]
+    tol = 1.2 * (1e-5 * np.sqrt(K) * bound + 1e-30) + \
+        4 * 2.0**-24 * (np.abs(z) + np.abs(want)) + 1e-30
+    err = np.abs(c.astype(np.float64) - want)
+    assert (err <= tol).all(), \
+        f"{what}: {int((err > tol).sum())} outside, worst {err.max():.3e}"
+
+
+@pytest.mark.parametrize("shape,pad,use_ws", [
+    ((1024, 1024, 1024), False, True),     # tensor path, split-K reduction
+    ((2048, 768, 512), False, False),      # tensor path, epilogue in kernel
+    ((300, 260, 77), True, False),         # unaligned: FFMA kernel
+    ((129, 65, 33), False, True)])
+@pytest.mark.parametrize("with_bias,act", [(True, 1), (False, 1), (True, 0)])
+def test_bias_act(shape, pad, use_ws, with_bias, act):
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=M + N, dist_a="normal",
+                               dist_b="normal")
+    bias = synth.make_operands(1, N, 1, seed=3)[1][0] if with_bias else None
+    if pad:  # odd leading dimensions force the FFMA kernel
+        ta = torch.zeros(M, K + 1, device=DEV)[:, :K]
+        ta.copy_(torch.from_numpy(a))
+        tb = torch.zeros(K, N + 1, device=DEV)[:, :N]
+        tb.copy_(torch.from_numpy(b))
+    else:
+        ta, tb = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    tbias = torch.from_numpy(bias).to(DEV) if with_bias else None
+    need = G.workspace_size(M, N, K) if use_ws else 0
+    ws = torch.empty(max(need // 4, 1), device=DEV) if use_ws else None
+    c = G.gemm_f32_bias_act(ta, tb, tbias, act, workspace=ws)
+    torch.cuda.synchronize()
+    _check_epilogue(a, b, bias, act, c.cpu().numpy(),
+                    f"{shape} bias={with_bias} act={act}")
+    assert G.device_status() == 0
+
+
+def test_bias_exact_on_integers():
+    a, b = synth.make_operands(300, 200, 120, seed=4, dist_a="int",
+                               dist_b="int")
+    bias = np.arange(200, dtype=np.float32) - 100
+    c = G.gemm_f32_bias_act(torch.from_numpy(a).to(DEV),
+                            torch.from_numpy(b).to(DEV),
+                            torch.from_numpy(bias).to(DEV), G.ACT_NONE)
+    torch.cuda.synchronize()
+    ref, _, _ = oracle.gemm(a, b)
+    assert_bitexact(c.cpu().numpy(), oracle.epilogue(ref, bias, 0), "bias int")
+
+
+def test_bias_act_rejects_bad_activation():
+    t = torch.zeros(8, 8, device=DEV)
+    with pytest.raises(G.GemmError):
+        G.gemm_f32_bias_act(t, t, None, 7)

@@ -230,3 +230,34 @@ def test_strided_operands(oracle_lib):
     c, _, _ = oracle_lib.gemm(a, b)
     cs, _, _ = oracle_lib.gemm(big_a[:, :7], big_b[:, :5])
     assert np.array_equal(c, cs)
+
+
+# ------------------------------------------------------------- epilogue
+def test_epilogue_gelu_tabulated_values(oracle_lib):
+    """GELU(x) = x·Φ(x) at points where Φ is tabulated: Φ(0) = 1/2,
+    Φ(1) = 0.8413447460685429, Φ(-1) = 0.15865525393145707,
+    Φ(2) = 0.9772498680518208; far tails give x and 0."""
+    x = np.array([[0.0, 1.0, -1.0, 2.0, 10.0, -10.0]])
+    got = oracle_lib.epilogue(x, act=1)[0]
+    want = [0.0, 0.8413447460685429, -0.15865525393145707,
+            2 * 0.9772498680518208, 10.0, 0.0]
+    assert np.allclose(got, want, rtol=1e-15, atol=1e-20)
+
+
+def test_epilogue_gelu_odd_part_identity(oracle_lib):
+    """Φ(x) + Φ(-x) = 1, so GELU(x) - GELU(-x) = x for every x."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((7, 9)) * 3
+    g = oracle_lib.epilogue(x, act=1)
+    gm = oracle_lib.epilogue(-x, act=1)
+    assert np.allclose(g - gm, x, rtol=1e-14, atol=1e-15)
+
+
+def test_epilogue_bias_broadcast_and_identity(oracle_lib):
+    c = np.arange(12, dtype=np.float64).reshape(3, 4)
+    bias = np.array([0.5, -1.0, 2.0, 0.0], np.float32)
+    out = oracle_lib.epilogue(c, bias, act=0)
+    assert np.array_equal(out, c + bias.astype(np.float64))
+    assert np.array_equal(oracle_lib.epilogue(c), c)
+    with pytest.raises(ValueError):
+        oracle_lib.epilogue(c, bias, act=2)
