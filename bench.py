@@ -57,7 +57,12 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    return p.parse_args()
+    args = p.parse_args()
+    if args.epilogue != "none" and (args.algo != "auto" or args.op != "nn"
+                                    or args.batch != 1):
+        p.error("--epilogue runs gemm_f32_bias_act, which picks its kernel "
+                "itself: use it with --algo auto --op nn --batch 1")
+    return args
 
 
 # ------------------------------------------------------------------ helpers

@@ -44,11 +44,15 @@ struct Problem {
 enum : int { kActNone = 0, kActGelu = 1 };
 
 // act(v + bias[col]): GELU(x) = x·Φ(x) = x/2·(1 + erf(x/√2)).
+__device__ __forceinline__ float epilogue_act(float v, int act) {
+  if (act == kActGelu) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+  return v;
+}
+
 __device__ __forceinline__ float apply_epilogue(float v, const float* bias,
                                                 int act, int col) {
   if (bias) v += bias[col];
-  if (act == kActGelu) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
-  return v;
+  return epilogue_act(v, act);
 }
 
 // Bounded-wait configuration shared by all pipelined kernels.

@@ -108,8 +108,17 @@ struct FfmaTile {
                                         const float (&acc)[8][8]) const {
     const bool interior = (bm + BM <= p.M) && (bn + BN <= p.N);
     const bool epi = p.bias != nullptr || p.act != kActNone;
-    auto val = [&](int i, int j, int col) {
-      return epi ? apply_epilogue(acc[i][j], p.bias, p.act, col) : acc[i][j];
+    // the bias of the thread's 8 columns, loaded once (C stores may alias it)
+    float bcol[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = bn + col0 + 16 * (j >> 2) + (j & 3);
+      bcol[j] = (p.bias != nullptr && c < p.N) ? p.bias[c] : 0.f;
+    }
+    auto val = [&](int i, int j, int) {
+      if (!epi) return acc[i][j];
+      return epilogue_act(p.bias != nullptr ? acc[i][j] + bcol[j] : acc[i][j],
+                          p.act);
     };
     if (interior && c_vec) {
 #pragma unroll
@@ -249,8 +258,17 @@ struct FfmaTileT {
                                         const float (&acc)[8][8]) const {
     const bool interior = (bm + BM <= p.M) && (bn + BN <= p.N);
     const bool epi = p.bias != nullptr || p.act != kActNone;
-    auto val = [&](int i, int j, int col) {
-      return epi ? apply_epilogue(acc[i][j], p.bias, p.act, col) : acc[i][j];
+    // the bias of the thread's 8 columns, loaded once (C stores may alias it)
+    float bcol[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = bn + col0 + 16 * (j >> 2) + (j & 3);
+      bcol[j] = (p.bias != nullptr && c < p.N) ? p.bias[c] : 0.f;
+    }
+    auto val = [&](int i, int j, int) {
+      if (!epi) return acc[i][j];
+      return epilogue_act(p.bias != nullptr ? acc[i][j] + bcol[j] : acc[i][j],
+                          p.act);
     };
     if (interior && c_vec) {
 #pragma unroll

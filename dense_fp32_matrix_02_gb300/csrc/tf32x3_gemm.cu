@@ -400,6 +400,10 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         tc_fence_after_sync();
         const int n = bn + n_loc;
         const int c_begin = h * (kAccCols / 2);
+        // this lane's column n has one bias value; load it once
+        const bool epi = splits == 1 && (bias != nullptr || act != 0);
+        const float bias_n =
+            (epi && bias != nullptr && n < N) ? bias[n] : 0.f;
 #pragma unroll 1
         for (int c0 = c_begin; c0 < c_begin + kAccCols / 2; c0 += 16) {
           uint32_t v[16];
@@ -425,13 +429,18 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
             }
           } else if (n < N) {
             // fused epilogue (not on split-K partials: the reduction has it)
-            const bool epi = splits == 1 && (bias != nullptr || act != 0);
+            if (epi) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float x = __uint_as_float(v[i]);
+                if (bias != nullptr) x += bias_n;
+                v[i] = __float_as_uint(epilogue_act(x, act));
+              }
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int m = bm + c0 + i;
-              float x = __uint_as_float(v[i]);
-              if (epi) x = apply_epilogue(x, bias, act, n);
-              if (m < M) out[(long long)m * ldo + n] = x;
+              if (m < M) out[(long long)m * ldo + n] = __uint_as_float(v[i]);
             }
           }
         }
