@@ -17,8 +17,13 @@ Every function here is pinned by ``tests/test_oracle.py`` against things the
 pages and the mathematics fix (identities, exact integer products, exact
 rational brute force, a naive float32 loop, the 2MNK operation count and
 metamorphic relations; for the epilogue, tabulated values of the normal
-distribution function and the identity GELU(x) - GELU(-x) = x); no function
-here is "parity unpinned".
+distribution function and the identity GELU(x) - GELU(-x) = x; for the
+16-bit operand rounding, hand-worked ties and boundaries of both formats and
+the conversions of torch and numpy); no function here is "parity unpinned".
+
+The mixed-precision product ("Rendre le GPU rapide", "Les Tensor Cores")
+rounds only the operands to 16 bits: ``gemm_mixed`` is ``gemm`` on the
+rounded-and-widened operands.
 """
 
 from __future__ import annotations
@@ -78,6 +83,11 @@ class Oracle:
         lib.oracle_epilogue_f64.restype = ctypes.c_int
         lib.oracle_epilogue_f64.argtypes = [i64, i64, dp, i64, fp, ctypes.c_int,
                                             dp, i64]
+        lib.oracle_round_half.restype = ctypes.c_int
+        lib.oracle_round_half.argtypes = [ctypes.c_int, i64, i64, fp, i64, dp,
+                                          i64]
+        lib.oracle_widen_half.restype = ctypes.c_int
+        lib.oracle_widen_half.argtypes = [ctypes.c_int, i64, fp, dp]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self._lib = lib
@@ -152,6 +162,37 @@ class Oracle:
             raise ValueError("oracle rejected its arguments")
         return out
 
+    def round_half(self, x, half_type: int):
+        """The 16-bit patterns (uint16) of float32 x rounded to bfloat16
+        (half_type 0) or IEEE binary16 (1), nearest with ties to even."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        flat = x.reshape(1, -1) if x.ndim != 2 else x
+        out = np.empty(flat.shape, dtype=np.uint16)
+        rows, cols = flat.shape
+        st = self._lib.oracle_round_half(int(half_type), rows, cols,
+                                         flat.ctypes.data, max(cols, 1),
+                                         out.ctypes.data, max(cols, 1))
+        if st != 0:
+            raise ValueError("oracle rejected its arguments")
+        return out.reshape(x.shape)
+
+    def widen_half(self, h, half_type: int):
+        """float32 values of 16-bit patterns h (exact)."""
+        h = np.ascontiguousarray(h, dtype=np.uint16)
+        out = np.empty(h.shape, dtype=np.float32)
+        st = self._lib.oracle_widen_half(int(half_type), h.size, h.ctypes.data,
+                                         out.ctypes.data)
+        if st != 0:
+            raise ValueError("oracle rejected its arguments")
+        return out
+
+    def gemm_mixed(self, a, b, half_type: int, threads: int = 0):
+        """(C_ref, bound, fmas) of the mixed-precision product: a and b
+        rounded to 16 bits, then the float64 product of the rounded values."""
+        ar = self.widen_half(self.round_half(a, half_type), half_type)
+        br = self.widen_half(self.round_half(b, half_type), half_type)
+        return self.gemm(ar, br, threads)
+
     def max_threads(self) -> int:
         return int(self._lib.oracle_max_threads())
 
@@ -175,6 +216,18 @@ def entries(a, b, rows, cols):
 
 def epilogue(c, bias=None, act=0):
     return load().epilogue(c, bias, act)
+
+
+def round_half(x, half_type: int):
+    return load().round_half(x, half_type)
+
+
+def widen_half(h, half_type: int):
+    return load().widen_half(h, half_type)
+
+
+def gemm_mixed(a, b, half_type: int, threads: int = 0):
+    return load().gemm_mixed(a, b, half_type, threads)
 
 
 def tolerance(bound, K: int):

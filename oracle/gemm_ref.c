@@ -29,7 +29,8 @@
  *   1 drops the last k term, 2 reads B transposed (B[j][k], the flat index
  *   wrapped into B's extent so the mistake stays in bounds),
  *   3 subtracts odd-k terms, 4 reads A one row too high (wraps at M-1),
- *   5 accumulates in float32 instead of float64.
+ *   5 accumulates in float32 instead of float64; 6-8 break the 16-bit
+ *   rounding (see oracle_round_half).
  */
 #include <math.h>
 #include <stdint.h>
@@ -195,5 +196,109 @@ int oracle_epilogue_f64(int64_t M, int64_t N, const double *C, int64_t ldc,
             if (act == 1) z = 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
             out[i * ldo + j] = z;
         }
+    return 0;
+}
+
+/*
+ * Operand rounding of the mixed-precision product ("Rendre le GPU rapide",
+ * "Les Tensor Cores"): only the two operands of the multiply are rounded to
+ * a 16-bit float; every sum and every tensor stays float32.  The oracle of
+ * that product is therefore oracle_gemm_f64 applied to the operands after
+ * oracle_round_half and oracle_widen_half (widening is exact).
+ *
+ * type 0, bfloat16: the upper 16 bits of the float32 pattern, rounded to
+ *   nearest with ties to even the way the pages do it: add 0x7FFF plus the
+ *   lowest kept bit to the 32-bit pattern, then drop the low 16 bits.
+ *   Overflow carries into the exponent and yields ±Inf, as IEEE rounding
+ *   does.  The pages do not treat NaN (the carry could turn a NaN pattern
+ *   into Inf or a wrapped sign); here a NaN stays a quiet NaN.
+ * type 1, IEEE binary16 (1 sign, 5 exponent bits with bias 15, 10 stored
+ *   significand bits), from the format's definition: |x| >= 65520 (halfway
+ *   between 65504 and 2^16, which ties to the even 2^16) gives ±Inf;
+ *   otherwise |x| is rounded to the nearest multiple of its quantum
+ *   2^(e-10), e = max(floor(log2|x|), -14), ties to an even multiple.
+ *   Below 2^-14 the quantum stays 2^-24 (gradual underflow).
+ *
+ * ORACLE_MUTANT 6 rounds bfloat16 by truncation; 7 breaks binary16 ties
+ * away from zero; 8 flushes values below 2^-14 to zero (no gradual
+ * underflow).
+ */
+static uint16_t round_bf16(float x) {
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);          /* NaN, quiet */
+#if ORACLE_MUTANT == 6
+    return (uint16_t)(u >> 16);
+#else
+    return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+#endif
+}
+
+static uint16_t round_f16(float x) {
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+    const double a = fabs((double)x);
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u);  /* also ±Inf */
+    if (a == 0.0) return sign;
+    int ex;
+    (void)frexp(a, &ex);               /* a = m·2^ex, m in [0.5, 1) */
+    int e = ex - 1;                    /* floor(log2 a) */
+#if ORACLE_MUTANT == 8
+    if (e < -14) return sign;
+#endif
+    if (e < -14) e = -14;
+    const double r = ldexp(a, 10 - e); /* a / quantum, exact */
+    double n = floor(r);
+    const double d = r - n;            /* exact: r has at most 24 bits */
+#if ORACLE_MUTANT == 7
+    if (d >= 0.5) n += 1.0;
+#else
+    if (d > 0.5 || (d == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;
+#endif
+    if (e == -14 && n <= 1024.0)       /* subnormal, or 2^-14 exactly */
+        return (uint16_t)(sign | (uint16_t)n);
+    if (n == 2048.0) {                 /* rounded up to the next binade */
+        n = 1024.0;
+        e += 1;
+    }
+    if (e > 15) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) |
+                      (uint16_t)(n - 1024.0));
+}
+
+/* dst[i][j] = round(src[i][j]) for a rows×cols block; row strides in
+ * elements.  Returns 0, or -1 for bad arguments. */
+int oracle_round_half(int type, int64_t rows, int64_t cols, const float *src,
+                      int64_t lds, uint16_t *dst, int64_t ldd) {
+    if ((type != 0 && type != 1) || rows < 0 || cols < 0 || lds < cols ||
+        ldd < cols)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < cols; ++j)
+            dst[i * ldd + j] = type == 0 ? round_bf16(src[i * lds + j])
+                                         : round_f16(src[i * lds + j]);
+    return 0;
+}
+
+/* dst[t] = the float32 value of the 16-bit pattern src[t] (exact). */
+int oracle_widen_half(int type, int64_t n, const uint16_t *src, float *dst) {
+    if ((type != 0 && type != 1) || n < 0) return -1;
+    for (int64_t t = 0; t < n; ++t) {
+        const uint16_t h = src[t];
+        float v;
+        if (type == 0) {
+            const uint32_t u = (uint32_t)h << 16;
+            memcpy(&v, &u, 4);
+        } else {
+            const int E = (h >> 10) & 31, F = h & 1023;
+            double m;
+            if (E == 0) m = ldexp((double)F, -24);
+            else if (E == 31) m = F ? NAN : INFINITY;
+            else m = ldexp((double)(1024 + F), E - 25);
+            v = (float)((h & 0x8000u) ? -m : m);
+        }
+        dst[t] = v;
+    }
     return 0;
 }

@@ -7,7 +7,9 @@ brute force, a naive float32 loop inside its rounding-error bound, the
 pages' operation count 2MNK ("3 · La mémoire partagée", §3.1) and
 metamorphic relations.  ``test_mutant_is_caught`` builds oracle copies with
 one planted mistake each (dropped term, transposed operand, wrong sign,
-wrong row, float32 accumulation) and checks that some pin fails on each.
+wrong row, float32 accumulation; truncating bfloat16 rounding, binary16
+ties away from zero, binary16 without subnormals) and checks that some pin
+fails on each.
 """
 
 from __future__ import annotations
@@ -195,17 +197,143 @@ PINS = [pin_golden, pin_identity, pin_all_ones, pin_index_product,
         pin_empty]
 
 
-@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+# ------------------------------------------------ 16-bit operand rounding
+# Hand-worked values of both formats ("Rendre le GPU rapide", "Les Tensor
+# Cores": operands rounded to nearest, ties to even).  bfloat16 keeps 7
+# stored bits (quantum 2^-7 in [1, 2)); binary16 keeps 10 (quantum 2^-10 in
+# [1, 2), 2^-24 below 2^-14) and overflows past 65504.
+HALF_WORKED = [
+    # (value, bfloat16 bits, binary16 bits)
+    (1.0, 0x3F80, 0x3C00),
+    (1 + 2**-8, 0x3F80, 0x3C04),           # bf16: halfway, even is 1.0
+    (1 + 3 * 2**-8, 0x3F82, 0x3C0C),       # bf16: halfway, even is 1+2^-6
+    (1 + 2**-8 + 2**-20, 0x3F81, 0x3C04),  # bf16: just above halfway
+    (-(1 + 2**-7 + 2**-9), 0xBF81, 0xBC0A),
+    (1 + 2**-11, 0x3F80, 0x3C00),          # f16: halfway, even is 1.0
+    (1 + 3 * 2**-11, 0x3F80, 0x3C02),      # f16: halfway, even is 1+2^-9
+    (65504.0, 0x4780, 0x7BFF),             # largest binary16
+    (65519.0, 0x4780, 0x7BFF),
+    (65520.0, 0x4780, 0x7C00),             # halfway to 2^16: ties to Inf
+    (2.0**-14, 0x3880, 0x0400),            # smallest normal binary16
+    (2.0**-24, 0x3380, 0x0001),            # smallest subnormal binary16
+    (2.0**-25, 0x3300, 0x0000),            # halfway 0 .. 2^-24: even is 0
+    (3 * 2.0**-25, 0x33C0, 0x0002),        # halfway 1 .. 2 quanta: even 2
+    (2.0**-14 - 2.0**-25, 0x3880, 0x0400), # rounds up into the normals
+    (3.0e38, 0x7F62, 0x7C00),
+    (3.4028234663852886e38, 0x7F80, 0x7C00),  # FLT_MAX: bf16 overflows
+    (-0.0, 0x8000, 0x8000),
+    (float("inf"), 0x7F80, 0x7C00),
+    (float("-inf"), 0xFF80, 0xFC00),
+]
+
+
+def pin_half_worked_values(orc):
+    x = np.array([v for v, _, _ in HALF_WORKED], np.float32)
+    assert orc.round_half(x, 0).tolist() == [b for _, b, _ in HALF_WORKED]
+    assert orc.round_half(x, 1).tolist() == [h for _, _, h in HALF_WORKED]
+
+
+def _float32_sample(n, seed):
+    """Finite float32 values over every exponent, plus exact ties of both
+    formats (low 16 bits 0x8000 for bfloat16; for binary16 values whose
+    bits below the kept ones are exactly one half)."""
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32)
+    bits = bits[(bits & 0x7F800000) != 0x7F800000]
+    ties_bf = (bits & 0xFFFF0000) | 0x8000
+    ties_f16 = (bits & 0xFFFFE000) | 0x1000
+    # binary16 range: exponents -30 .. 16 with ties at the 13th bit
+    e = rng.integers(-30, 17, n // 4)
+    m = rng.integers(0, 2**23, n // 4)
+    small = np.ldexp(1 + m / 2.0**23, e).astype(np.float32)
+    return np.concatenate([bits.view(np.float32), ties_bf.view(np.float32),
+                           ties_f16.view(np.float32), small,
+                           -small]).astype(np.float32)
+
+
+def pin_bf16_matches_torch(orc):
+    """bfloat16 rounding equals torch's float32 -> bfloat16 conversion
+    (round to nearest even) on every exponent, on ties, and keeps NaN."""
+    torch = pytest.importorskip("torch")
+    x = _float32_sample(40000, 11)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(orc.round_half(x, 0), want.view(np.uint16))
+    nan = orc.round_half(np.array([np.nan], np.float32), 0)
+    assert (nan[0] & 0x7F80) == 0x7F80 and (nan[0] & 0x7F) != 0
+
+
+def pin_f16_matches_numpy(orc):
+    """binary16 rounding equals numpy's float32 -> float16 conversion
+    (IEEE round to nearest even, gradual underflow, overflow to Inf)."""
+    x = _float32_sample(40000, 12)
+    with np.errstate(over="ignore"):  # overflow to Inf is the point
+        want = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(orc.round_half(x, 1), want)
+    nan = orc.round_half(np.array([np.nan], np.float32), 1)
+    assert (nan[0] & 0x7C00) == 0x7C00 and (nan[0] & 0x3FF) != 0
+
+
+def pin_widen_exact(orc):
+    """Widening gives every 16-bit pattern's value: binary16 as numpy
+    decodes it, bfloat16 as torch does; rounding a widened value gives the
+    pattern back (every representable value rounds to itself)."""
+    torch = pytest.importorskip("torch")
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f16 = orc.widen_half(h, 1)
+    ref16 = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref16)
+    assert np.array_equal(np.isnan(f16), nan)
+    assert np.array_equal(f16[~nan].view(np.uint32), ref16[~nan].view(np.uint32))
+    bf = orc.widen_half(h, 0)
+    refbf = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).float().numpy()
+    nanb = np.isnan(refbf)
+    assert np.array_equal(np.isnan(bf), nanb)
+    assert np.array_equal(bf[~nanb].view(np.uint32), refbf[~nanb].view(np.uint32))
+    assert np.array_equal(orc.round_half(f16[~nan], 1), h[~nan])
+    assert np.array_equal(orc.round_half(bf[~nanb], 0), h[~nanb])
+
+
+def pin_mixed_small_integers(orc):
+    """The pages' test of the mixed-precision product: integers in [-8, 8]
+    are exact in 16 bits and their sums exact in float32, so the result is
+    the exact integer product."""
+    rng = np.random.default_rng(5)
+    a = rng.integers(-8, 9, (7, 300)).astype(np.float32)
+    b = rng.integers(-8, 9, (300, 5)).astype(np.float32)
+    exact = a.astype(np.int64) @ b.astype(np.int64)
+    for t in (0, 1):
+        c, _, _ = orc.gemm_mixed(a, b, t)
+        assert np.array_equal(c, exact.astype(np.float64))
+
+
+def pin_mixed_rounds_operands_only(orc):
+    """The mixed product is the exact product of the rounded operands: with
+    B = I it returns A rounded (worked values above), not A."""
+    x = np.array([[v for v, _, _ in HALF_WORKED[:8]]], np.float32)
+    for t in (0, 1):
+        c, _, _ = orc.gemm_mixed(x, np.eye(8, dtype=np.float32), t)
+        want = [w[1 + t] for w in HALF_WORKED[:8]]
+        got = orc.round_half(c.astype(np.float32), t)[0].tolist()
+        assert got == want
+
+
+HALF_PINS = [pin_half_worked_values, pin_bf16_matches_torch,
+             pin_f16_matches_numpy, pin_widen_exact, pin_mixed_small_integers,
+             pin_mixed_rounds_operands_only]
+
+
+@pytest.mark.parametrize("pin", PINS + HALF_PINS,
+                         ids=[p.__name__ for p in PINS + HALF_PINS])
 def test_pin(pin, oracle_lib):
     pin(oracle_lib)
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_mutant_is_caught(mutant, tmp_path):
     """Each planted mistake makes at least one pin fail."""
     orc = oracle.Oracle(oracle.build(mutant, outdir=str(tmp_path)))
     failed = []
-    for pin in PINS:
+    for pin in PINS + HALF_PINS:
         try:
             pin(orc)
         except AssertionError:
