@@ -511,6 +511,107 @@ unsigned int gemm_f32_set_debug_flags(unsigned int flags) {
   return g_debug_flags.exchange(flags);
 }
 
+// ------------------------------------------------ mixed precision (16-bit)
+
+int64_t gemm_f32_mixed_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return -GEMM_F32_ERR_INVALID_ARG;
+  const int64_t a = M * ((K + 7) / 8 * 8) * 2;
+  const int64_t b = K * ((N + 7) / 8 * 8) * 2;
+  return (a + 255) / 256 * 256 + b;
+}
+
+int gemm_f32_round16(int type, int64_t rows, int64_t cols, const float* src,
+                     int64_t lds, void* dst, int64_t ldd,
+                     gemm_f32_stream_t stream) {
+  if (type != GEMM_F32_MIXED_BF16 && type != GEMM_F32_MIXED_F16)
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || lds < cols || ldd < cols)
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return GEMM_F32_OK;
+  if (!src || !dst || (reinterpret_cast<uintptr_t>(dst) & 1u))
+    return GEMM_F32_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = gemm_f32_impl::launch_round16(type, rows, cols, src, lds,
+                                    static_cast<uint16_t*>(dst), ldd,
+                                    d->sm_count,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GEMM_F32_OK : fail_cuda(e);
+}
+
+int gemm_f32_mixed16(int type, int64_t M, int64_t N, int64_t K,
+                     const void* A, int64_t lda, const void* B, int64_t ldb,
+                     float* C, int64_t ldc, gemm_f32_stream_t stream) {
+  if (type != GEMM_F32_MIXED_BF16 && type != GEMM_F32_MIXED_F16)
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || ldc < N)
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
+    return GEMM_F32_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return GEMM_F32_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_F32_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    e = gemm_f32_impl::launch_fill_zero(C, ldc, M, N, d->sm_count, s);
+    return e == cudaSuccess ? GEMM_F32_OK : fail_cuda(e);
+  }
+  if (d->cc_major != 10 || !aligned16(A) || !aligned16(B) || lda % 8 != 0 ||
+      ldb % 8 != 0)
+    return GEMM_F32_ERR_UNSUPPORTED;
+  gemm_f32_impl::Problem16 p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.type = type;
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  gemm_f32_impl::WaitCfg wc;
+  wc.limit = g_wait_ns.load();
+  wc.debug = g_debug_flags.load();
+  wc.status = d->status;
+  e = gemm_f32_impl::launch_mixed16(p, d->sm_count,
+                                    aligned16(C) && ldc % 4 == 0, wc, s);
+  return e == cudaSuccess ? GEMM_F32_OK : fail_cuda(e);
+}
+
+int gemm_f32_mixed(int type, int64_t M, int64_t N, int64_t K, const float* A,
+                   int64_t lda, const float* B, int64_t ldb, float* C,
+                   int64_t ldc, void* workspace, int64_t workspace_bytes,
+                   gemm_f32_stream_t stream) {
+  if (type != GEMM_F32_MIXED_BF16 && type != GEMM_F32_MIXED_F16)
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || ldc < N)
+    return GEMM_F32_ERR_INVALID_ARG;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
+    return GEMM_F32_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return GEMM_F32_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_F32_ERR_INVALID_ARG;
+  if (K == 0)
+    return gemm_f32_mixed16(type, M, N, 0, nullptr, 0, nullptr, N, C, ldc,
+                            stream);
+  const int64_t need = gemm_f32_mixed_workspace_size(M, N, K);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return GEMM_F32_ERR_INVALID_ARG;
+  const int64_t lda16 = (K + 7) / 8 * 8, ldb16 = (N + 7) / 8 * 8;
+  char* ws = static_cast<char*>(workspace);
+  void* a16 = ws;
+  void* b16 = ws + (M * lda16 * 2 + 255) / 256 * 256;
+  int st = gemm_f32_round16(type, M, K, A, lda, a16, lda16, stream);
+  if (st != GEMM_F32_OK) return st;
+  st = gemm_f32_round16(type, K, N, B, ldb, b16, ldb16, stream);
+  if (st != GEMM_F32_OK) return st;
+  return gemm_f32_mixed16(type, M, N, K, a16, lda16, b16, ldb16, C, ldc,
+                          stream);
+}
+
 int gemm_f32_version(void) { return 100; }
 
 }  // extern "C"

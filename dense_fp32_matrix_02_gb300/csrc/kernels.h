@@ -84,4 +84,30 @@ int run_auto_with_scratch(int64_t M, int64_t N, int64_t K, const float* A,
                           int64_t ldc, void* scratch, int64_t scratch_bytes,
                           gemm_f32_stream_t stream);
 
+// One mixed-precision product: 16-bit A (M×K) and B (K×N), row-major.
+struct Problem16 {
+  int M, N, K;
+  int type;  // gemm_f32_mixed_type
+  const void* A;
+  long long lda;
+  const void* B;
+  long long ldb;
+  float* C;
+  long long ldc;
+};
+
+// tcgen05 kind::f16 kernel, persistent over min(tiles, sm_count) CTAs.
+// Needs A, B 16-byte aligned, lda and ldb multiples of 8, K >= 1.
+cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
+                           const WaitCfg& wc, cudaStream_t stream);
+
+// dst = round16(src) (type gemm_f32_mixed_type) for a rows×cols block.
+cudaError_t launch_round16(int type, long long rows, long long cols,
+                           const float* src, long long lds, uint16_t* dst,
+                           long long ldd, int sm_count, cudaStream_t stream);
+
+// C[0:M, 0:N] = 0.
+cudaError_t launch_fill_zero(float* C, long long ldc, long long M, long long N,
+                             int sm_count, cudaStream_t stream);
+
 }  // namespace gemm_f32_impl

@@ -1,0 +1,416 @@
+// Mixed-precision matrix product on the 5th-generation tensor cores:
+// C (fp32) = A·B with A and B 16-bit floats (bfloat16 or IEEE binary16)
+// and fp32 accumulation: the arithmetic of "Rendre le GPU rapide", "Les
+// Tensor Cores" (only the operands are 16-bit; sums and tensors stay fp32).
+//
+// One persistent CTA per SM walks the 128×256 output tiles (a grid-stride
+// walk over a grouped tile order, so CTAs running at the same time share A
+// row-panels and B column-panels in L2):
+//   warp 0      TMA producer.  Per k-block of 64: the A tile (128 rows of
+//               64 k, K-major, 128-byte swizzle) and the B tile (64 k rows
+//               of 256 n, N-major, as four 64×64 boxes, 128-byte swizzle)
+//               into a 4-stage ring.
+//   warp 1      MMA issuer.  Four tcgen05.mma kind::f16 (M 128, N 256,
+//               K 16) per stage into one of two TMEM accumulators of 256
+//               columns; tcgen05.commit releases the stage and, after the
+//               last k-block, publishes the accumulator.
+//   warps 2-9   Epilogue.  tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32·(w mod 4) + 0..31, i.e. those rows of the tile, and
+//               one half of its columns), fp32 stores to C guarded by M and
+//               N, then release of the accumulator, which the tile after
+//               next accumulates into; storing one tile overlaps the MMAs of
+//               the next.
+// Every mbarrier wait is bounded by %globaltimer.  A CTA that gives up sets
+// the status word, lets its copies and MMAs in flight land, frees TMEM and
+// returns without storing further tiles.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace gemm_f32_impl {
+namespace mixed16 {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // kBK: 128-byte rows
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
+constexpr int kStageBytesA = kBM * kBK * 2;    // 16 KB
+constexpr int kBoxBytesB = 64 * kBK * 2;       // 8 KB: 64 n × 64 k
+constexpr int kStageBytesB = kBN * kBK * 2;    // 32 KB
+constexpr int kOffB = kStages * kStageBytesA;
+constexpr int kOffCtl = kOffB + kStages * kStageBytesB;
+constexpr int kAccCols = kBN;                  // fp32 columns per accumulator
+constexpr int kTmemCols = 2 * kAccCols;        // 512: the whole TMEM
+constexpr long long kDrainNs = 2000000000LL;
+constexpr uint32_t kSleepNs = 100000;
+
+struct __align__(8) Control {
+  uint64_t full[kStages];   // TMA -> MMA (transaction bytes)
+  uint64_t empty[kStages];  // MMA completion -> producer
+  uint64_t acc_full[2];     // last MMA of a tile -> epilogue
+  uint64_t acc_empty[2];    // epilogue warps -> MMA (one arrival per warp)
+  uint64_t mma_done;        // every MMA issued has completed
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr int kSmemBytes = kOffCtl + (int)sizeof(Control) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           long long limit_ns,
+                                           volatile int* abort, bool sleep) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (sleep ? mbar_try_wait_sleep(bar, parity, kSleepNs)
+              : mbar_try_wait(bar, parity))
+      return true;
+    if (sleep || (i & 15u) == 0) {
+      if (abort && *abort) return false;
+      if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
+    }
+  }
+}
+
+// ab_type: 0 binary16, 1 bfloat16 (the kind::f16 operand format code).
+template <int AB_TYPE>
+__global__ void __launch_bounds__(kThreads, 1)
+    mixed16_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, float* C,
+                   long long ldc, int M, int N, int K, int tiles_m,
+                   int tiles_n, int c_vec, WaitCfg wc) {
+  constexpr uint32_t kIdesc = idesc_f16(kBM, kBN, AB_TYPE, true);
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Control* ctl = reinterpret_cast<Control*>(smem + kOffCtl);
+  volatile int* abort = &ctl->abort;
+  auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
+  auto empty = [&](int s) { return smem_u32(&ctl->empty[s]); };
+  auto acc_full = [&](int b) { return smem_u32(&ctl->acc_full[b]); };
+  auto acc_empty = [&](int b) { return smem_u32(&ctl->acc_empty[b]); };
+  const uint32_t mma_done = smem_u32(&ctl->mma_done);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = (K + kBK - 1) / kBK;  // >= 1 (host)
+  const int total = tiles_m * tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), kEpiWarps);
+    }
+    mbar_init(mma_done, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;  // k-blocks issued, over all tiles of this CTA
+      if (!(wc.debug & kDebugStallProducer)) {
+        for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+          int tm, tn;
+          tile_coords<8>(t, tiles_m, tiles_n, tm, tn);
+          for (int kb = 0; kb < nk; ++kb) {
+            const int s = it % kStages;
+            if (it >= kStages &&
+                !wait_phase(empty(s), ((it / kStages) - 1) & 1, wc.limit,
+                            abort, false)) {
+              *abort = 1;
+              record_status(wc.status, kStatusTimeoutEmpty);
+              break;
+            }
+            mbar_arrive_expect_tx(full(s), kStageBytesA + kStageBytesB);
+            tma_load_2d(sbase + s * kStageBytesA, &tmap_a, full(s), kb * kBK,
+                        tm * kBM);
+            const uint32_t bdst = sbase + kOffB + s * kStageBytesB;
+#pragma unroll
+            for (int c = 0; c < kBN / 64; ++c)
+              tma_load_2d(bdst + c * kBoxBytesB, &tmap_b, full(s),
+                          tn * kBN + 64 * c, kb * kBK);
+            ++it;
+          }
+        }
+      }
+      if (*abort) {  // let the copies still in flight land before leaving
+        for (int k = it > kStages ? it - kStages : 0; k < it; ++k)
+          if (!wait_phase(full(k % kStages), (k / kStages) & 1, kDrainNs,
+                          nullptr, false))
+            record_status(wc.status, kStatusTimeoutDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x, i = 0; ok && t < total; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (i >= 2 && !wait_phase(acc_empty(b), ((i >> 1) - 1) & 1, wc.limit,
+                                  abort, false)) {
+          *abort = 1;
+          record_status(wc.status, kStatusTimeoutMma);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + b * kAccCols;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!wait_phase(full(s), (it / kStages) & 1, wc.limit, abort,
+                          false)) {
+            *abort = 1;
+            record_status(wc.status, kStatusTimeoutFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = sbase + s * kStageBytesA;
+          const uint32_t b0 = sbase + kOffB + s * kStageBytesB;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // A: 16 k = 32 bytes along the swizzled row; B: 16 k rows
+            const uint64_t ad = smem_desc_sw128(a0 + 32 * kk, 16, 1024);
+            const uint64_t bd =
+                smem_desc_sw128(b0 + 2048 * kk, kBoxBytesB, 1024);
+            mma_f16_ss(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+          }
+          tc_commit(empty(s));
+        }
+        if (ok) tc_commit(acc_full(b));
+      }
+      // no MMA may still run when TMEM is freed at the end
+      tc_commit(mma_done);
+      if (!wait_phase(mma_done, 0, kDrainNs, nullptr, false))
+        record_status(wc.status, kStatusTimeoutDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;         // TMEM lane quarter = rows 32q..32q+31
+    const int h = (warp - 2) >> 2;  // column half
+    const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
+    for (int t = blockIdx.x, i = 0; t < total; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      const bool ok =
+          wait_phase(acc_full(b), (i >> 1) & 1, wc.limit, abort, true);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort = 1;
+        if (lane == 0) record_status(wc.status, kStatusTimeoutMma);
+        break;
+      }
+      tc_fence_after_sync();
+      int tm, tn;
+      tile_coords<8>(t, tiles_m, tiles_n, tm, tn);
+      const int m = tm * kBM + q * 32 + lane;
+      const int n0 = tn * kBN + h * (kAccCols / 2);
+      float* crow = C + (long long)m * ldc;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kAccCols / 2; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_bits + b * kAccCols + h * (kAccCols / 2) + c0,
+                  v);
+        tmem_ld_wait();
+        const int n = n0 + c0;
+        if (m < M) {
+          if (c_vec && n + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(crow + n + j) = make_float4(
+                  __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                  __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n + j < N) crow[n + j] = __uint_as_float(v[j]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(b));
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// dst = src rounded to 16 bits (nearest, ties to even) for a rows×cols
+// block.  vec: cols, lds and ldd multiples of 4, src 16-byte and dst 8-byte
+// aligned, so each thread converts four consecutive elements.
+template <int AB_TYPE>
+__global__ void __launch_bounds__(256)
+    round16_kernel(long long rows, long long cols,
+                   const float* __restrict__ src, long long lds,
+                   uint16_t* __restrict__ dst, long long ldd, int vec) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long first = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (vec) {
+    const long long groups = cols / 4;
+    const long long total = rows * groups;
+    for (long long g = first; g < total; g += stride) {
+      const long long i = g / groups, j = (g % groups) * 4;
+      const float4 x = *reinterpret_cast<const float4*>(src + i * lds + j);
+      uint2 o;
+      if constexpr (AB_TYPE == 1) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+      } else {
+        const __half2 lo = __floats2half2_rn(x.x, x.y);
+        const __half2 hi = __floats2half2_rn(x.z, x.w);
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+      }
+      *reinterpret_cast<uint2*>(dst + i * ldd + j) = o;
+    }
+  } else {
+    const long long total = rows * cols;
+    for (long long g = first; g < total; g += stride) {
+      const long long i = g / cols, j = g % cols;
+      const float x = src[i * lds + j];
+      uint16_t o;
+      if constexpr (AB_TYPE == 1) {
+        const __nv_bfloat16 r = __float2bfloat16_rn(x);
+        o = *reinterpret_cast<const uint16_t*>(&r);
+      } else {
+        const __half r = __float2half_rn(x);
+        o = *reinterpret_cast<const uint16_t*>(&r);
+      }
+      dst[i * ldd + j] = o;
+    }
+  }
+}
+
+// C[0:M, 0:N] = 0 (the empty sum of a K = 0 product).
+__global__ void __launch_bounds__(256)
+    fill_zero_kernel(float* C, long long ldc, long long M, long long N) {
+  const long long total = M * N;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+       g < total; g += (long long)gridDim.x * blockDim.x)
+    C[(g / N) * ldc + g % N] = 0.f;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map of a row-major 16-bit matrix (x contiguous) with a 64 × by box in
+// the 128-byte swizzle; out-of-range elements read as zeros.
+bool encode_16(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
+               int type, const void* base, long long x, long long y,
+               long long ld, int by) {
+  const cuuint64_t dims[2] = {(cuuint64_t)x, (cuuint64_t)y};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)by};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(m,
+                type == GEMM_F32_MIXED_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                2, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace mixed16
+
+cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
+                           const WaitCfg& wc, cudaStream_t stream) {
+  using namespace mixed16;
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  if (!encode_16(encode, &ta, p.type, p.A, p.K, p.M, p.lda, kBM) ||
+      !encode_16(encode, &tb, p.type, p.B, p.N, p.K, p.ldb, kBK))
+    return cudaErrorInvalidValue;
+  auto fn = p.type == GEMM_F32_MIXED_BF16 ? mixed16_kernel<1>
+                                          : mixed16_kernel<0>;
+  cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(fn), kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long tiles_m = (p.M + kBM - 1) / kBM;
+  const long long tiles_n = (p.N + kBN - 1) / kBN;
+  const long long total = tiles_m * tiles_n;
+  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int grid = (int)(total < sm_count ? total : sm_count);
+  fn<<<grid, kThreads, kSmemBytes, stream>>>(
+      ta, tb, p.C, p.ldc, p.M, p.N, p.K, (int)tiles_m, (int)tiles_n,
+      c_vec ? 1 : 0, wc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_round16(int type, long long rows, long long cols,
+                           const float* src, long long lds, uint16_t* dst,
+                           long long ldd, int sm_count, cudaStream_t stream) {
+  using namespace mixed16;
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const bool vec = cols % 4 == 0 && lds % 4 == 0 && ldd % 4 == 0 &&
+                   (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(dst) & 7u) == 0;
+  const long long work = vec ? rows * (cols / 4) : rows * cols;
+  long long blocks = (work + 255) / 256;
+  const long long cap = 8LL * sm_count;
+  if (blocks > cap) blocks = cap;
+  if (type == GEMM_F32_MIXED_BF16)
+    round16_kernel<1><<<(int)blocks, 256, 0, stream>>>(rows, cols, src, lds,
+                                                       dst, ldd, vec ? 1 : 0);
+  else
+    round16_kernel<0><<<(int)blocks, 256, 0, stream>>>(rows, cols, src, lds,
+                                                       dst, ldd, vec ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_zero(float* C, long long ldc, long long M, long long N,
+                             int sm_count, cudaStream_t stream) {
+  using namespace mixed16;
+  if (M == 0 || N == 0) return cudaSuccess;
+  long long blocks = (M * N + 255) / 256;
+  const long long cap = 8LL * sm_count;
+  if (blocks > cap) blocks = cap;
+  fill_zero_kernel<<<(int)blocks, 256, 0, stream>>>(C, ldc, M, N);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm_f32_impl

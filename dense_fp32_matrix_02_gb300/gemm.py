@@ -81,6 +81,16 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_set_debug_flags.argtypes = [ctypes.c_uint]
         L.gemm_f32_version.restype = ci
         L.gemm_f32_version.argtypes = []
+        L.gemm_f32_mixed16.restype = ci
+        L.gemm_f32_mixed16.argtypes = [ci, i64, i64, i64, vp, i64, vp, i64,
+                                       vp, i64, vp]
+        L.gemm_f32_mixed.restype = ci
+        L.gemm_f32_mixed.argtypes = [ci, i64, i64, i64, vp, i64, vp, i64, vp,
+                                     i64, vp, i64, vp]
+        L.gemm_f32_round16.restype = ci
+        L.gemm_f32_round16.argtypes = [ci, i64, i64, vp, i64, vp, i64, vp]
+        L.gemm_f32_mixed_workspace_size.restype = i64
+        L.gemm_f32_mixed_workspace_size.argtypes = [i64, i64, i64]
         _lib = L
         return L
 
@@ -296,10 +306,12 @@ def workspace_size(M, N, K) -> int:
     return n
 
 
-def _matrix_args(t, name):
+def _matrix_args(t, name, dtypes=None):
     import torch
-    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32:
-        raise TypeError(f"{name} must be a float32 torch tensor")
+    dtypes = dtypes or (torch.float32,)
+    if not isinstance(t, torch.Tensor) or t.dtype not in dtypes:
+        names = " or ".join(str(d).replace("torch.", "") for d in dtypes)
+        raise TypeError(f"{name} must be a {names} torch tensor")
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D")
     if not t.is_cuda:
@@ -398,3 +410,131 @@ DEBUG_STALL_PRODUCER = 1
 
 def version() -> int:
     return int(lib().gemm_f32_version())
+
+
+# ------------------------------------------------ mixed precision (16-bit)
+MIXED_BF16, MIXED_F16 = 0, 1
+
+
+def _mixed_type(dtype_or_type):
+    import torch
+    if dtype_or_type in (MIXED_BF16, torch.bfloat16):
+        return MIXED_BF16
+    if dtype_or_type in (MIXED_F16, torch.float16):
+        return MIXED_F16
+    raise ValueError("16-bit type must be bfloat16 or float16")
+
+
+def _mixed_dtype(t):
+    import torch
+    return torch.bfloat16 if t == MIXED_BF16 else torch.float16
+
+
+def _handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def gemm_f32_mixed16_ptr(type_, M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,
+                         stream=0):
+    """Raw-pointer gemm_f32_mixed16 call (16-bit operands, fp32 C)."""
+    st = lib().gemm_f32_mixed16(int(type_), int(M), int(N), int(K),
+                                a_ptr or None, int(lda), b_ptr or None,
+                                int(ldb), c_ptr or None, int(ldc),
+                                stream or None)
+    _check(st, "gemm_f32_mixed16")
+
+
+def gemm_f32_mixed16(a, b, c=None, stream=None):
+    """C (fp32) = A·B for bfloat16 or float16 CUDA tensors of one dtype,
+    fp32 accumulation on the tensor cores."""
+    import torch
+    if a.dtype != b.dtype:
+        raise TypeError("a and b must have the same 16-bit dtype")
+    dt = (torch.bfloat16, torch.float16)
+    M, K, ap, lda = _matrix_args(a, "a", dt)
+    K2, N, bp, ldb = _matrix_args(b, "b", dt)
+    if K != K2:
+        raise ValueError("inner sizes differ")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    Mc, Nc, cp, ldc = _matrix_args(c, "c")
+    if (Mc, Nc) != (M, N):
+        raise ValueError("c has the wrong shape")
+    with torch.cuda.device(a.device):
+        gemm_f32_mixed16_ptr(_mixed_type(a.dtype), M, N, K, ap, lda, bp, ldb,
+                             cp, ldc, _handle(stream, a.device))
+    return c
+
+
+def round16_ptr(type_, rows, cols, src_ptr, lds, dst_ptr, ldd, stream=0):
+    """Raw-pointer gemm_f32_round16 call."""
+    st = lib().gemm_f32_round16(int(type_), int(rows), int(cols),
+                                src_ptr or None, int(lds), dst_ptr or None,
+                                int(ldd), stream or None)
+    _check(st, "gemm_f32_round16")
+
+
+def round16(x, half=MIXED_BF16, out=None, stream=None):
+    """x (2-D float32 CUDA tensor) rounded to bfloat16 or float16 (nearest,
+    ties to even) by the library's kernel; returns the 16-bit tensor."""
+    import torch
+    t = _mixed_type(half)
+    rows, cols, xp, lds = _matrix_args(x, "x")
+    if out is None:
+        out = torch.empty((rows, cols), dtype=_mixed_dtype(t), device=x.device)
+    r2, c2, op, ldd = _matrix_args(out, "out", (_mixed_dtype(t),))
+    if (r2, c2) != (rows, cols):
+        raise ValueError("out has the wrong shape")
+    with torch.cuda.device(x.device):
+        round16_ptr(t, rows, cols, xp, lds, op, ldd, _handle(stream, x.device))
+    return out
+
+
+def mixed_workspace_size(M, N, K) -> int:
+    """Workspace bytes gemm_f32_mixed needs."""
+    n = int(lib().gemm_f32_mixed_workspace_size(int(M), int(N), int(K)))
+    if n < 0:
+        _check(-n, "gemm_f32_mixed_workspace_size")
+    return n
+
+
+def gemm_f32_mixed_ptr(type_, M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,
+                       ws_ptr, ws_bytes, stream=0):
+    """Raw-pointer gemm_f32_mixed call (fp32 operands rounded first)."""
+    st = lib().gemm_f32_mixed(int(type_), int(M), int(N), int(K),
+                              a_ptr or None, int(lda), b_ptr or None,
+                              int(ldb), c_ptr or None, int(ldc),
+                              ws_ptr or None, int(ws_bytes), stream or None)
+    _check(st, "gemm_f32_mixed")
+
+
+def gemm_f32_mixed(a, b, half=MIXED_BF16, c=None, workspace=None,
+                   stream=None):
+    """Mixed-precision C = A·B of float32 CUDA tensors: operands rounded to
+    bfloat16 (default) or float16, fp32 products and sums, fp32 C.  The
+    rounding scratch is `workspace` (a CUDA tensor of at least
+    mixed_workspace_size bytes), allocated here when not given."""
+    import torch
+    t = _mixed_type(half)
+    M, K, ap, lda = _matrix_args(a, "a")
+    K2, N, bp, ldb = _matrix_args(b, "b")
+    if K != K2:
+        raise ValueError("inner sizes differ")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    Mc, Nc, cp, ldc = _matrix_args(c, "c")
+    if (Mc, Nc) != (M, N):
+        raise ValueError("c has the wrong shape")
+    need = mixed_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8,
+                                device=a.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(a.device):
+        gemm_f32_mixed_ptr(t, M, N, K, ap, lda, bp, ldb, cp, ldc,
+                           workspace.data_ptr() if ws_bytes else 0, ws_bytes,
+                           _handle(stream, a.device))
+    return c

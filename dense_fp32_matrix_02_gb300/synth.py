@@ -26,6 +26,10 @@ Distributions (each maps draws to float32 exactly as written):
 * ``int``      small integers in {-2, ..., 2}: ``((x >> 32) * 5) >> 32`` minus
   2, computed in unsigned 64-bit integers.  Float32 holds these exactly, and
   any sum of at most 2**22 products of them stays an exact float32 integer.
+* ``int8``     integers in {-8, ..., 8}: ``((x >> 32) * 17) >> 32`` minus 8,
+  the inputs of the mixed-precision exactness test ("Rendre le GPU rapide",
+  "Les Tensor Cores"): exact in bfloat16 and binary16, and sums of at most
+  2**18 products of them stay exact float32 integers.
 
 The workloads (sizes, distributions and seeds) are the five dense FP32 GEMM
 cases of this library's test and benchmark plan; ``WORKLOADS`` lists them.
@@ -63,7 +67,7 @@ def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
 def _draws_per_element(dist: str) -> int:
     if dist == "normal":
         return 2
-    if dist in ("uniform", "int"):
+    if dist in ("uniform", "int", "int8"):
         return 1
     raise ValueError(f"unknown distribution {dist!r}")
 
@@ -78,6 +82,11 @@ def _fill(seed: int, start: int, n: int, dist: str, sigma: float) -> np.ndarray:
         with np.errstate(over="ignore"):
             v = ((x >> np.uint64(32)) * np.uint64(5)) >> np.uint64(32)
         return (v.astype(np.int64) - 2).astype(np.float32)
+    if dist == "int8":
+        x = splitmix64(seed, start, n)
+        with np.errstate(over="ignore"):
+            v = ((x >> np.uint64(32)) * np.uint64(17)) >> np.uint64(32)
+        return (v.astype(np.int64) - 8).astype(np.float32)
     if dist == "normal":
         x = splitmix64(seed, start, 2 * n)
         x1 = x[0::2]

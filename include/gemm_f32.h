@@ -152,6 +152,65 @@ GEMM_F32_API int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N,
                                   int64_t strideC, int64_t batch,
                                   gemm_f32_stream_t stream);
 
+/* 16-bit operand formats of the mixed-precision products. */
+typedef enum {
+    GEMM_F32_MIXED_BF16 = 0, /* bfloat16: the upper half of a float32 */
+    GEMM_F32_MIXED_F16 = 1   /* IEEE binary16: 5 exponent, 10 stored bits */
+} gemm_f32_mixed_type;
+
+/*
+ * Mixed-precision product, "Rendre le GPU rapide", "Les Tensor Cores": only
+ * the multiply's operands are 16-bit floats; products and sums are fp32
+ * and C is fp32.  NOT within gemm_f32's tolerance for fp32 operands (the
+ * operands carry 8 or 11 significant bits); exact when the operands and
+ * every partial sum are representable, e.g. integers in [-8, 8] with
+ * K <= 2^18.  It is a separate entry, never chosen by gemm_f32.
+ *
+ * gemm_f32_mixed16: A (M×K, lda) and B (K×N, ldb) already hold 16-bit
+ * values of `type` (gemm_f32_mixed_type), row-major in device memory, 16-byte
+ * aligned, with lda and ldb multiples of 8 (else GEMM_F32_ERR_UNSUPPORTED);
+ * C is fp32 M×N (ldc >= N, any alignment).  Tensor cores (tcgen05,
+ * kind::f16) with fp32 accumulation in tensor memory; needs an sm_10x GPU.
+ * M == 0 or N == 0 launches nothing; K == 0 sets C to 0.
+ */
+GEMM_F32_API int gemm_f32_mixed16(int type, int64_t M, int64_t N, int64_t K,
+                                  const void *A, int64_t lda, const void *B,
+                                  int64_t ldb, float *C, int64_t ldc,
+                                  gemm_f32_stream_t stream);
+
+/*
+ * dst = src rounded to the 16-bit `type` for a rows×cols block of fp32
+ * (row stride lds) into 16-bit storage (row stride ldd), both in device
+ * memory: round to nearest, ties to even, overflow to ±Inf, binary16
+ * subnormals kept; NaN stays NaN.  The pages round bfloat16 the same way
+ * (add half a step plus the lowest kept bit, then cut).
+ */
+GEMM_F32_API int gemm_f32_round16(int type, int64_t rows, int64_t cols,
+                                  const float *src, int64_t lds, void *dst,
+                                  int64_t ldd, gemm_f32_stream_t stream);
+
+/*
+ * The mixed-precision product of fp32 operands: A and B are rounded to
+ * `type` (as gemm_f32_round16) into `workspace`, then multiplied as by
+ * gemm_f32_mixed16.  Any alignment and any leading dimensions >= the row
+ * widths.  `workspace` is 16-byte aligned device memory of at least
+ * gemm_f32_mixed_workspace_size(M, N, K) bytes (else
+ * GEMM_F32_ERR_INVALID_ARG); it holds the rounded A (M rows of K rounded
+ * up to a multiple of 8) and then, from the next 256-byte boundary, the
+ * rounded B (K rows of N rounded up likewise), and is in use until the
+ * stream passes this call.
+ */
+GEMM_F32_API int gemm_f32_mixed(int type, int64_t M, int64_t N, int64_t K,
+                                const float *A, int64_t lda, const float *B,
+                                int64_t ldb, float *C, int64_t ldc,
+                                void *workspace, int64_t workspace_bytes,
+                                gemm_f32_stream_t stream);
+
+/* Workspace bytes gemm_f32_mixed needs for an M×N×K product (negative
+ * status for negative sizes). */
+GEMM_F32_API int64_t gemm_f32_mixed_workspace_size(int64_t M, int64_t N,
+                                                   int64_t K);
+
 /*
  * As gemm_f32 (automatic kernel choice), with caller-owned device scratch
  * that the library may use to split K over several CTAs per tile when the

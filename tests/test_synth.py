@@ -45,6 +45,9 @@ def test_distributions_and_layout():
         b.ravel(), v[1500:])
     ai, bi = synth.make_operands(64, 64, 64, 0, "int", "int")
     assert set(np.unique(ai)) <= {-2.0, -1.0, 0.0, 1.0, 2.0}
+    a8, _ = synth.make_operands(64, 64, 64, 0, "int8", "int8")
+    assert set(np.unique(a8)) == {float(v) for v in range(-8, 9)}
+    assert abs(a8.mean()) < 0.2
     an, bn = synth.WORKLOADS["mlp"].operands()
     assert abs(an.std() - 1.0) < 0.01 and abs(bn.std() - 0.02) < 0.0002
     assert abs(an.mean()) < 0.01
