@@ -53,6 +53,14 @@ def parse_args():
                    choices=["none", "bias", "bias_gelu"],
                    help="fused epilogue C = act(A·B + bias) "
                         "(gemm_f32_bias_act)")
+    p.add_argument("--precision", default="fp32",
+                   choices=["fp32", "bf16", "f16"],
+                   help="fp32: the FP32 product (default); bf16/f16: the "
+                        "mixed-precision product gemm_f32_mixed16 on 16-bit "
+                        "operands resident in HBM")
+    p.add_argument("--from-f32", action="store_true",
+                   help="with --precision bf16/f16: time gemm_f32_mixed "
+                        "(fp32 operands rounded inside the step)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -62,6 +70,12 @@ def parse_args():
                                     or args.batch != 1):
         p.error("--epilogue runs gemm_f32_bias_act, which picks its kernel "
                 "itself: use it with --algo auto --op nn --batch 1")
+    if args.precision != "fp32" and (args.algo != "auto" or args.op != "nn"
+                                     or args.batch != 1
+                                     or args.epilogue != "none"):
+        p.error("--precision bf16/f16 runs the mixed-precision product alone")
+    if args.from_f32 and args.precision == "fp32":
+        p.error("--from-f32 goes with --precision bf16/f16")
     return args
 
 
@@ -80,6 +94,7 @@ KERNEL_SOURCES = {
     "tf32x3": ["tf32x3_gemm.cu", "tcgen05.cuh", "common.cuh", "kernels.h"],
     "simt": ["simt_gemm.cu", "ffma_tile.cuh", "common.cuh", "kernels.h"],
     "tma": ["tma_ffma_gemm.cu", "ffma_tile.cuh", "common.cuh", "kernels.h"],
+    "mixed16": ["mixed_gemm.cu", "tcgen05.cuh", "common.cuh", "kernels.h"],
 }
 TF32_FLOP_PER_CLK_PER_SM = 4096  # tcgen05 kind::tf32 dense (ncu peak rate)
 
@@ -250,6 +265,47 @@ def run_reference(args, w, config):
     print(json.dumps(line), flush=True)
 
 
+def timed_region(step, args, stream, dev, world):
+    """W warm-up steps, then K steps between CUDA events on `stream`, with
+    a barrier and a synchronize on both sides and nvidia-smi clocks sampled
+    meanwhile.  Returns (ms, max ms over ranks, clocks, wall seconds)."""
+    import torch
+    import torch.distributed as dist
+
+    from dense_fp32_matrix_02_gb300 import gemm as G
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if G.device_status() != 0:
+        raise SystemExit("kernel status word set during warm-up")
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001 - older torch
+        gpu_uuid = None
+    sampler = ClockSampler(gpu_uuid)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = start.elapsed_time(end)
+    ms_max = reduce_max_over_ranks(ms, dev)
+    if G.device_status() != 0:
+        raise SystemExit("kernel status word set during the timed region")
+    return ms, ms_max, clocks, wall
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args, w, config):
     import torch
@@ -334,38 +390,7 @@ def run_ours(args, w, config):
             G.gemm_f32_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K, tb.data_ptr(),
                            w.N, tc.data_ptr(), w.N, handle, algo)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if G.device_status() != 0:
-        raise SystemExit("kernel status word set during warm-up")
-
-    gpu_uuid = None
-    try:
-        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:  # noqa: BLE001 - older torch
-        gpu_uuid = None
-    sampler = ClockSampler(gpu_uuid)
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    wall0 = time.perf_counter()
-    start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    end.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    ms = start.elapsed_time(end)
-    ms_max = reduce_max_over_ranks(ms, dev)
-    if G.device_status() != 0:
-        raise SystemExit("kernel status word set during the timed region")
+    ms, ms_max, clocks, wall = timed_region(step, args, stream, dev, world)
 
     flops = float(w.flops) * args.batch
     value = weak_scaling_value(flops, args.steps, world, ms_max)
@@ -477,6 +502,127 @@ def run_ours(args, w, config):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------ ours, mixed precision
+def run_mixed(args, w, config):
+    """The mixed-precision product ("Rendre le GPU rapide", "Les Tensor
+    Cores"): 16-bit operands, fp32 accumulation, on the tensor cores."""
+    import torch
+    import torch.distributed as dist
+
+    from dense_fp32_matrix_02_gb300 import gemm as G
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    if w.K % 8 or w.N % 8:
+        raise SystemExit("16-bit operands need K and N multiples of 8")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    t = G.MIXED_BF16 if args.precision == "bf16" else G.MIXED_F16
+    a, b = w.operands()
+    nsets = 3
+    f32 = [(torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev))]
+    for _ in range(nsets - 1):
+        f32.append((f32[0][0].clone(), f32[0][1].clone()))
+    sets = [(G.round16(fa, t), G.round16(fb, t),
+             torch.empty(w.M, w.N, device=dev)) for fa, fb in f32]
+    if not args.from_f32:
+        del f32
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    ws_bytes = G.mixed_workspace_size(w.M, w.N, w.K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def step(i):
+        xa, xb, xc = sets[i % nsets]
+        if args.from_f32:
+            fa, fb = f32[i % nsets]
+            G.gemm_f32_mixed_ptr(t, w.M, w.N, w.K, fa.data_ptr(), w.K,
+                                 fb.data_ptr(), w.N, xc.data_ptr(), w.N,
+                                 ws.data_ptr(), ws_bytes, handle)
+        else:
+            G.gemm_f32_mixed16_ptr(t, w.M, w.N, w.K, xa.data_ptr(), w.K,
+                                   xb.data_ptr(), w.N, xc.data_ptr(), w.N,
+                                   handle)
+
+    ms, ms_max, clocks, wall = timed_region(step, args, stream, dev, world)
+    flops = float(w.flops)
+    value = weak_scaling_value(flops, args.steps, world, ms_max)
+    kernel_ms = ms / args.steps
+
+    # ---- end to end: fp32 operands from pinned host memory, the public
+    # gemm_f32_mixed call (rounding + product), C back to the host
+    ha = torch.from_numpy(a).pin_memory()
+    hb = torch.from_numpy(b).pin_memory()
+    hc = torch.empty(w.M, w.N, dtype=torch.float32).pin_memory()
+    ea = torch.empty(w.M, w.K, device=dev)
+    eb = torch.empty(w.K, w.N, device=dev)
+    ec = sets[0][2]
+
+    def e2e_step():
+        ea.copy_(ha, non_blocking=True)
+        eb.copy_(hb, non_blocking=True)
+        G.gemm_f32_mixed(ea, eb, t, ec, workspace=ws, stream=stream)
+        hc.copy_(ec, non_blocking=True)
+
+    e_steps = max(1, args.e2e_steps)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    s2 = torch.cuda.Event(enable_timing=True)
+    e2 = torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_value = weak_scaling_value(
+        flops, e_steps, world, reduce_max_over_ranks(s2.elapsed_time(e2), dev))
+
+    peaks, peaks_src = load_peaks()
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]  # binary16 has the same nominal dense rate
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"{peaks_src} bf16 burst (cuBLAS bf16 GEMM)",
+            "traffic": None if args.from_f32
+            else recorded_traffic("mixed16", w.name),
+            "algorithmic_bytes": 2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N,
+            "kernel_ms": kernel_ms}
+    if args.from_f32:
+        roof["note"] = ("step = two rounding kernels + the product; "
+                        "achieved is over the whole step")
+    line = {
+        "metric": f"mixed-precision GEMM TFLOPS ({args.precision} operands, "
+                  "fp32 accumulation)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.precision,
+        "data": "synthetic", "config": config, "kernel": "mixed16",
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
+                "d2h_bytes_per_step": 4 * w.M * w.N},
+        "gpu_launches": args.steps * (3 if args.from_f32 else 1),
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        ar = oracle.widen_half(oracle.round_half(a, t), t)
+        br = oracle.widen_half(oracle.round_half(b, t), t)
+        line["cpu_baseline"] = cpu_baseline(w, ar, br, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     from dense_fp32_matrix_02_gb300 import synth
@@ -493,8 +639,17 @@ def main():
               "l2": "3 rotating input/output sets (3 x "
                     f"{w.bytes / 2**20:.0f} MiB) between timed steps",
               "parallelism": f"independent problem per GPU x {args.gpus}"}
+    if args.precision != "fp32":
+        config["precision"] = (f"{args.precision} operands, fp32 products, "
+                               "sums and C")
+        config["operands"] = ("fp32 in HBM, rounded inside each step"
+                              if args.from_f32 else
+                              f"{args.precision} in HBM (rounded once before "
+                              "timing)")
     if args.impl == "reference":
         run_reference(args, w, config)
+    elif args.precision != "fp32":
+        run_mixed(args, w, config)
     else:
         run_ours(args, w, config)
 
