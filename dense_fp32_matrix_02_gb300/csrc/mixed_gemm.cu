@@ -16,10 +16,16 @@
 //               last k-block, publishes the accumulator.
 //   warps 2-9   Epilogue.  tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32·(w mod 4) + 0..31, i.e. those rows of the tile, and
-//               one half of its columns), fp32 stores to C guarded by M and
-//               N, then release of the accumulator, which the tile after
-//               next accumulates into; storing one tile overlaps the MMAs of
-//               the next.
+//               one half of its columns, 32 columns at a time).  Each 32×32
+//               block goes through a 4 KB shared-memory staging buffer of the
+//               warp (128-byte swizzle) and out by a TMA bulk tensor store,
+//               which writes whole 128-byte row segments and skips what lies
+//               past M or N.  The accumulator is released once read, so the
+//               tile after next accumulates into it while this one is still
+//               being written; storing one tile overlaps the MMAs of the
+//               next.  Where C cannot be described by a tensor map (not
+//               16-byte aligned, or ldc not a multiple of 4) each lane
+//               stores its row directly instead.
 // Every mbarrier wait is bounded by %globaltimer.  A CTA that gives up sets
 // the status word, lets its copies and MMAs in flight land, frees TMEM and
 // returns without storing further tiles.
@@ -28,6 +34,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -44,7 +51,9 @@ constexpr int kStageBytesA = kBM * kBK * 2;    // 16 KB
 constexpr int kBoxBytesB = 64 * kBK * 2;       // 8 KB: 64 n × 64 k
 constexpr int kStageBytesB = kBN * kBK * 2;    // 32 KB
 constexpr int kOffB = kStages * kStageBytesA;
-constexpr int kOffCtl = kOffB + kStages * kStageBytesB;
+constexpr int kStagingBytes = 32 * 32 * 4;     // one warp's 32×32 fp32 block
+constexpr int kOffStaging = kOffB + kStages * kStageBytesB;
+constexpr int kOffCtl = kOffStaging + kEpiWarps * kStagingBytes;
 constexpr int kAccCols = kBN;                  // fp32 columns per accumulator
 constexpr int kTmemCols = 2 * kAccCols;        // 512: the whole TMEM
 constexpr long long kDrainNs = 2000000000LL;
@@ -83,9 +92,12 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
 template <int AB_TYPE>
 __global__ void __launch_bounds__(kThreads, 1)
     mixed16_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_b, float* C,
+                   const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_c, float* C,
                    long long ldc, int M, int N, int K, int tiles_m,
-                   int tiles_n, int c_vec, WaitCfg wc) {
+                   int tiles_n, int c_mode, WaitCfg wc) {
+  // c_mode: 2 = TMA stores through staging, 1 = direct 16-byte stores,
+  // 0 = direct scalar stores
   constexpr uint32_t kIdesc = idesc_f16(kBM, kBN, AB_TYPE, true);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -119,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
+    if (c_mode == 2) prefetch_tmap(&tmap_c);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -214,6 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;         // TMEM lane quarter = rows 32q..32q+31
     const int h = (warp - 2) >> 2;  // column half
     const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
+    // staging: row r (this lane) is 128 bytes at r·128, its 16-byte chunk j
+    // at slot j ^ (r mod 8), the layout a 128-byte-swizzle TMA store reads
+    unsigned char* stg = smem + kOffStaging + (warp - 2) * kStagingBytes;
+    const uint32_t stg_s = sbase + kOffStaging + (warp - 2) * kStagingBytes;
     for (int t = blockIdx.x, i = 0; t < total; t += gridDim.x, ++i) {
       const int b = i & 1;
       const bool ok =
@@ -226,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       int tm, tn;
       tile_coords<8>(t, tiles_m, tiles_n, tm, tn);
-      const int m = tm * kBM + q * 32 + lane;
+      const int m0 = tm * kBM + q * 32;
+      const int m = m0 + lane;
       const int n0 = tn * kBN + h * (kAccCols / 2);
       float* crow = C + (long long)m * ldc;
 #pragma unroll 1
@@ -235,9 +253,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_bits + b * kAccCols + h * (kAccCols / 2) + c0,
                   v);
         tmem_ld_wait();
+        if (c0 + 32 == kAccCols / 2) {
+          // all of this warp's part of the accumulator is in registers
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty(b));
+        }
         const int n = n0 + c0;
-        if (m < M) {
-          if (c_vec && n + 32 <= N) {
+        if (c_mode == 2) {
+          if (lane == 0) bulk_wait_group_read<0>();  // staging free again
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(stg + lane * 128 +
+                                       ((j ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(v[4 * j]),
+                            __uint_as_float(v[4 * j + 1]),
+                            __uint_as_float(v[4 * j + 2]),
+                            __uint_as_float(v[4 * j + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && m0 < M && n < N) {  // else nothing to write
+            tma_store_2d(&tmap_c, stg_s, n, m0);
+            bulk_commit_group();
+          }
+        } else if (m < M) {
+          if (c_mode == 1 && n + 32 <= N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
               *reinterpret_cast<float4*>(crow + n + j) = make_float4(
@@ -250,10 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty(b));
     }
+    if (c_mode == 2 && lane == 0) bulk_wait_group<0>();  // C written
   }
 
   tc_fence_before_sync();
@@ -365,6 +404,21 @@ cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
   if (!encode_16(encode, &ta, p.type, p.A, p.K, p.M, p.lda, kBM) ||
       !encode_16(encode, &tb, p.type, p.B, p.N, p.K, p.ldb, kBK))
     return cudaErrorInvalidValue;
+  // C: fp32 M×N, 32×32 boxes in the 128-byte swizzle (rows of 128 bytes)
+  CUtensorMap tc;
+  std::memset(&tc, 0, sizeof(tc));
+  int c_mode = c_vec ? 1 : 0;
+  if (c_vec) {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.ldc * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.C, dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      c_mode = 2;
+  }
   auto fn = p.type == GEMM_F32_MIXED_BF16 ? mixed16_kernel<1>
                                           : mixed16_kernel<0>;
   cudaError_t e =
@@ -375,9 +429,9 @@ cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
   const long long total = tiles_m * tiles_n;
   if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int grid = (int)(total < sm_count ? total : sm_count);
-  fn<<<grid, kThreads, kSmemBytes, stream>>>(
-      ta, tb, p.C, p.ldc, p.M, p.N, p.K, (int)tiles_m, (int)tiles_n,
-      c_vec ? 1 : 0, wc);
+  fn<<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, tc, p.C, p.ldc, p.M,
+                                              p.N, p.K, (int)tiles_m,
+                                              (int)tiles_n, c_mode, wc);
   return cudaGetLastError();
 }
 
