@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -227,11 +228,20 @@ def cpu_baseline(w, a, b, target_s):
     rows = calibrate_rows(a, b, target_s)
     t = oracle_rows_timing(a, b, rows)
     flops = 2.0 * rows * w.N * w.K
+    cores = oracle.load().max_threads()
+    # and one thread alone, on a quarter of the per-core share of rows
+    rows1 = max(1, rows // max(1, 4 * cores))
+    t1 = oracle_rows_timing(a, b, rows1, threads=1)
     return {"value": flops / t / 1e12, "unit": "TFLOP/s",
-            "cores": oracle.load().max_threads(), "kind": "oracle",
+            "cores": cores, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of A times all of B "
                       f"({rows}x{w.N}x{w.K}, float64 accumulation, "
-                      f"{t:.1f} s)"}
+                      f"{t:.1f} s)",
+            "single_thread": {
+                "value": 2.0 * rows1 * w.N * w.K / t1 / 1e12,
+                "unit": "TFLOP/s",
+                "sample": f"rows 0..{rows1 - 1} ({rows1}x{w.N}x{w.K}, "
+                          f"{t1:.1f} s, 1 thread)"}}
 
 
 def run_reference(args, w, config):
@@ -287,23 +297,82 @@ def timed_region(step, args, stream, dev, world):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    # events at the edges of 5 equal chunks of the K steps: the whole
+    # region is timed once, the chunks give the spread between samples
+    nchunks = min(5, args.steps)
+    edges = [round(c * args.steps / nchunks) for c in range(nchunks + 1)]
+    events = [torch.cuda.Event(enable_timing=True) for _ in edges]
     wall0 = time.perf_counter()
-    start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    end.record(stream)
+    events[0].record(stream)
+    for c in range(nchunks):
+        for i in range(edges[c], edges[c + 1]):
+            step(i)
+        events[c + 1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = start.elapsed_time(end)
+    ms = events[0].elapsed_time(events[-1])
     ms_max = reduce_max_over_ranks(ms, dev)
     if G.device_status() != 0:
         raise SystemExit("kernel status word set during the timed region")
+    chunk_ms = [events[c].elapsed_time(events[c + 1]) /
+                max(1, edges[c + 1] - edges[c]) for c in range(nchunks)]
+    clocks["chunk_ms_per_step"] = chunk_ms
     return ms, ms_max, clocks, wall
+
+
+def sample_stats(flops_per_step, chunk_ms):
+    """Median, worst and best TFLOP/s over the timed chunks."""
+    v = sorted(flops_per_step / (m / 1e3) / 1e12 for m in chunk_ms if m > 0)
+    if not v:
+        return None
+    return {"n": len(v), "median": statistics.median(v), "min": v[0],
+            "max": v[-1], "unit": "TFLOP/s"}
+
+
+def rotating_sets(set_bytes, l2_bytes):
+    """Input/output sets to rotate between timed steps so that the ones a
+    step touches were last used more than 2x the L2 size of traffic ago."""
+    return max(3, min(8192, math.ceil(2.1 * l2_bytes / max(set_bytes, 1))))
+
+
+def measure_ffma_peak(dev, stream, target_ms=60.0):
+    """The FP32 pipe's rate from the library's FMA-chain probe (best of 3
+    launches of about target_ms each), with the SM clocks seen meanwhile."""
+    import torch
+
+    from dense_fp32_matrix_02_gb300 import gemm as G
+    sink = torch.zeros(256, device=dev)
+    handle = stream.cuda_stream
+
+    def run(iters):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        G.ffma_peak_launch(iters, sink, handle)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    iters = 256
+    run(iters)
+    t = run(iters)
+    iters = max(256, int(iters * target_ms / max(t, 1e-3)))
+    run(iters)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001 - older torch
+        uuid = None
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    best = min(run(iters) for _ in range(3))
+    clocks = sampler.stop()
+    flops = G.ffma_peak_flops(iters)
+    return {"tflops": flops / (best / 1e3) / 1e12, "ms": best,
+            "iters": iters, "sm_mhz": clocks.get("sm_mhz"),
+            "reasons": clocks.get("reasons")}
 
 
 # ------------------------------------------------------------------ ours
@@ -324,7 +393,8 @@ def run_ours(args, w, config):
 
     algo = ALGOS[args.algo]
     a, b = w.operands()
-    nsets = 3
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = rotating_sets(w.bytes * args.batch, l2_bytes)
     ta0 = torch.from_numpy(a).to(dev)
     tb0 = torch.from_numpy(b).to(dev)
     sets = [(ta0, tb0, torch.empty(w.M, w.N, device=dev))]
@@ -394,6 +464,7 @@ def run_ours(args, w, config):
 
     flops = float(w.flops) * args.batch
     value = weak_scaling_value(flops, args.steps, world, ms_max)
+    samples = sample_stats(flops, clocks.pop("chunk_ms_per_step"))
     # one GEMM launch per step (plus the split-K reduction when it splits);
     # launch gaps are included
     kernel_ms = ms / args.steps
@@ -450,7 +521,11 @@ def run_ours(args, w, config):
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     smax = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-    fp32_peak = 2.0 * sms * FP32_LANES_PER_SM * smax * 1e6 / 1e12
+    # FP32 pipe: measured by the FMA-chain probe (primary) and the nameplate
+    # 2 flop x 128 lanes x SMs x maximum clock beside it
+    probe = measure_ffma_peak(dev, stream)
+    fp32_nameplate = 2.0 * sms * FP32_LANES_PER_SM * smax * 1e6 / 1e12
+    fp32_peak = probe["tflops"]
     achieved = flops / (kernel_ms / 1e3) / 1e12
     algo_name = G.ALGO_NAMES.get(ran, str(ran))
     if algo_name == "tf32x3":
@@ -469,13 +544,19 @@ def run_ours(args, w, config):
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak,
                 "unit": "TFLOP/s", "frac": achieved / fp32_peak,
-                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes "
-                               f"x 2 flop x {smax:.0f} MHz (max SM clock)"}
+                "peak_source": "measured: FMA-chain probe on every SM "
+                               f"({probe['sm_mhz']} MHz median)",
+                "peak_nameplate": fp32_nameplate,
+                "frac_nameplate": achieved / fp32_nameplate,
+                "nameplate_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 "
+                                    f"lanes x 2 flop x {smax:.0f} MHz"}
     roof["traffic"] = recorded_traffic(algo_name, w.name)
     roof["algorithmic_bytes"] = w.bytes * args.batch
     roof["kernel_ms"] = kernel_ms
 
-    fp32_roof = min(fp32_peak, (flops / w.bytes) * peaks["hbm_gbs"] / 1e3)
+    bw_roof = (flops / (w.bytes * args.batch)) * peaks["hbm_gbs"] / 1e3
+    fp32_roof = min(fp32_peak, bw_roof)
+    fp32_roof_nameplate = min(fp32_nameplate, bw_roof)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -485,6 +566,11 @@ def run_ours(args, w, config):
         "kernel": algo_name,
         "pct_fp32_roofline": 100.0 * (value / world) / fp32_roof,
         "fp32_roofline_tflops": fp32_roof,
+        "fp32_roofline_source": "min(measured FFMA probe, I x HBM)",
+        "pct_fp32_roofline_nameplate":
+            100.0 * (value / world) / fp32_roof_nameplate,
+        "ffma_probe": probe,
+        "samples": samples,
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N) * args.batch,
@@ -522,7 +608,8 @@ def run_mixed(args, w, config):
         dist.init_process_group("nccl", device_id=dev)
     t = G.MIXED_BF16 if args.precision == "bf16" else G.MIXED_F16
     a, b = w.operands()
-    nsets = 3
+    nsets = rotating_sets(2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N,
+                          torch.cuda.get_device_properties(dev).L2_cache_size)
     f32 = [(torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev))]
     for _ in range(nsets - 1):
         f32.append((f32[0][0].clone(), f32[0][1].clone()))
@@ -550,6 +637,7 @@ def run_mixed(args, w, config):
     ms, ms_max, clocks, wall = timed_region(step, args, stream, dev, world)
     flops = float(w.flops)
     value = weak_scaling_value(flops, args.steps, world, ms_max)
+    samples = sample_stats(flops, clocks.pop("chunk_ms_per_step"))
     kernel_ms = ms / args.steps
 
     # ---- end to end: fp32 operands from pinned host memory, the public
@@ -604,6 +692,7 @@ def run_mixed(args, w, config):
         "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.precision,
         "data": "synthetic", "config": config, "kernel": "mixed16",
+        "samples": samples,
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
@@ -636,8 +725,9 @@ def main():
               "inputs": f"A {dist_txt[w.dist_a]} (sigma {w.sigma_a}), "
                         f"B {dist_txt[w.dist_b]} (sigma {w.sigma_b}), "
                         f"SplitMix64 seed {w.seed}",
-              "l2": "3 rotating input/output sets (3 x "
-                    f"{w.bytes / 2**20:.0f} MiB) between timed steps",
+              "l2": "rotating input/output sets between timed steps, "
+                    "together more than 2x the L2 size (at least 3 sets "
+                    f"of {w.bytes / 2**20:.1f} MiB)",
               "parallelism": f"independent problem per GPU x {args.gpus}"}
     if args.precision != "fp32":
         config["precision"] = (f"{args.precision} operands, fp32 products, "

@@ -89,6 +89,10 @@ def lib() -> ctypes.CDLL:
                                      i64, vp, i64, vp]
         L.gemm_f32_round16.restype = ci
         L.gemm_f32_round16.argtypes = [ci, i64, i64, vp, i64, vp, i64, vp]
+        L.gemm_f32_ffma_peak_launch.restype = ci
+        L.gemm_f32_ffma_peak_launch.argtypes = [i64, vp, vp]
+        L.gemm_f32_ffma_peak_flops.restype = i64
+        L.gemm_f32_ffma_peak_flops.argtypes = [i64]
         L.gemm_f32_mixed_workspace_size.restype = i64
         L.gemm_f32_mixed_workspace_size.argtypes = [i64, i64, i64]
         _lib = L
@@ -538,3 +542,19 @@ def gemm_f32_mixed(a, b, half=MIXED_BF16, c=None, workspace=None,
                            workspace.data_ptr() if ws_bytes else 0, ws_bytes,
                            _handle(stream, a.device))
     return c
+
+
+# ------------------------------------------------ FP32 FMA throughput probe
+def ffma_peak_launch(iters, sink, stream=0):
+    """Launches the FMA-chain probe (``sink``: a CUDA float32 tensor of at
+    least 256 elements); time it on ``stream``."""
+    st = lib().gemm_f32_ffma_peak_launch(int(iters), sink.data_ptr(),
+                                         stream or None)
+    _check(st, "gemm_f32_ffma_peak_launch")
+
+
+def ffma_peak_flops(iters) -> int:
+    n = int(lib().gemm_f32_ffma_peak_flops(int(iters)))
+    if n < 0:
+        _check(-n, "gemm_f32_ffma_peak_flops")
+    return n

@@ -212,6 +212,21 @@ GEMM_F32_API int64_t gemm_f32_mixed_workspace_size(int64_t M, int64_t N,
                                                    int64_t K);
 
 /*
+ * FP32 FMA throughput probe (measurement, not part of any product): launches
+ * a kernel of independent FMA chains, `iters` loop iterations per thread, on
+ * every SM at full residency; `sink` is device memory of at least 256 floats
+ * (never written in practice).  Time it on `stream` and divide
+ * gemm_f32_ffma_peak_flops(iters) by the time for the FP32 pipe's measured
+ * rate, the ceiling of the FFMA kernels.  Launches only; no sync.
+ */
+GEMM_F32_API int gemm_f32_ffma_peak_launch(int64_t iters, float *sink,
+                                           gemm_f32_stream_t stream);
+
+/* Floating-point operations (2 per FMA) one gemm_f32_ffma_peak_launch with
+ * `iters` performs on the current device; negative status on error. */
+GEMM_F32_API int64_t gemm_f32_ffma_peak_flops(int64_t iters);
+
+/*
  * As gemm_f32 (automatic kernel choice), with caller-owned device scratch
  * that the library may use to split K over several CTAs per tile when the
  * tiles alone would leave most SMs idle (a second kernel then sums the
