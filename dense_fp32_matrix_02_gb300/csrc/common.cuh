@@ -157,6 +157,35 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar,
   return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on one phase of an mbarrier: false once the CTA abort flag
+// (if given) is raised or `limit_ns` of %globaltimer time have passed.
+// sleep_ns > 0 lets each probe suspend the thread until the phase completes
+// (for at most sleep_ns) instead of polling, leaving issue slots to the
+// warps that compute; 0 polls, for single-thread roles (TMA producer, MMA
+// issuer) that must react at once.
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
+                                             long long limit_ns,
+                                             volatile int* abort,
+                                             uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (sleep_ns ? mbar_try_wait_sleep(bar, parity, sleep_ns)
+                 : mbar_try_wait(bar, parity))
+      return true;
+    if (sleep_ns || (i & 15u) == 0) {
+      if (abort && *abort) return false;
+      if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled bulk tensor load into shared memory, completion counted on the
 // mbarrier in transaction bytes.  c0 is the innermost coordinate.

@@ -181,6 +181,21 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
 
 namespace gemm_f32_impl {
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
 cudaError_t ensure_smem_attr(const void* fn, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

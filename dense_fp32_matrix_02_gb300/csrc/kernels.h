@@ -2,6 +2,8 @@
 // kernel translation units.  Not installed; not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,6 +27,10 @@ enum SimtCfg {
   kSimtKm128x128x16Occ1 = 9,
   kSimtCfgCount = 10
 };
+
+// The driver's cuTensorMapEncodeTiled, looked up once (thread-safe); null
+// if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize for `fn` on the current
 // device once (a launch asking for more than 48 KB fails without it).

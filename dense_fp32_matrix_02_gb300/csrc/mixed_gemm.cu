@@ -72,20 +72,12 @@ struct __align__(8) Control {
 constexpr int kSmemBytes = kOffCtl + (int)sizeof(Control) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
+// sleep: the epilogue warps, idle while a tile accumulates; the producer
+// and the MMA issuer poll.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            long long limit_ns,
                                            volatile int* abort, bool sleep) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (sleep ? mbar_try_wait_sleep(bar, parity, kSleepNs)
-              : mbar_try_wait(bar, parity))
-      return true;
-    if (sleep || (i & 15u) == 0) {
-      if (abort && *abort) return false;
-      if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
-    }
-  }
+  return bounded_wait(bar, parity, limit_ns, abort, sleep ? kSleepNs : 0u);
 }
 
 // ab_type: 0 binary16, 1 bfloat16 (the kind::f16 operand format code).
@@ -360,21 +352,6 @@ __global__ void __launch_bounds__(256)
     C[(g / N) * ldc + g % N] = 0.f;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                         cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 2-D map of a row-major 16-bit matrix (x contiguous) with a 64 × by box in
 // the 128-byte swizzle; out-of-range elements read as zeros.
 bool encode_16(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
@@ -398,7 +375,7 @@ bool encode_16(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
 cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
                            const WaitCfg& wc, cudaStream_t stream) {
   using namespace mixed16;
-  auto encode = encode_fn();
+  auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   if (!encode_16(encode, &ta, p.type, p.A, p.K, p.M, p.lda, kBM) ||

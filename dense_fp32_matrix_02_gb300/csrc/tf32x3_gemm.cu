@@ -139,17 +139,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            long long limit_ns,
                                            volatile int* abort,
                                            bool sleep = true) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (sleep ? mbar_try_wait_sleep(bar, parity, kSleepNs)
-              : mbar_try_wait(bar, parity))
-      return true;
-    if (sleep || (i & 15u) == 0) {
-      if (abort && *abort) return false;
-      if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
-    }
-  }
+  return bounded_wait(bar, parity, limit_ns, abort, sleep ? kSleepNs : 0u);
 }
 
 // The same for all 32 lanes of a warp: every lane waits, and the warp goes
@@ -499,21 +489,6 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- host
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                         cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 }  // namespace tf32x3
 
 namespace {
@@ -543,7 +518,7 @@ template <class Cf>
 cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
                        const WaitCfg& wc, cudaStream_t stream) {
   using namespace tf32x3;
-  auto encode = encode_fn();
+  auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   if (!encode_3d(encode, &ta, p.A, p.K, p.M, p.lda, p.sA, p.batch, Cf::kBK,

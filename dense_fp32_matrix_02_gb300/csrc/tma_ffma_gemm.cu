@@ -45,25 +45,12 @@ struct TCfg {
   static constexpr int kSmemBytes = kOffBar + 2 * STAGES * 8 + 16 + 1024;
 };
 
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-  return t;
-}
-
-// Bounded wait; false when `limit_ns` passes or the CTA abort flag is set.
+// Bounded wait (polling); false when `limit_ns` passes or the CTA abort
+// flag is set.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            long long limit_ns,
                                            volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = now_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0) {
-      if (abort && *abort) return false;
-      if ((long long)(now_ns() - t0) > limit_ns) return false;
-    }
-  }
+  return bounded_wait(bar, parity, limit_ns, abort, 0u);
 }
 
 template <class Cf>
@@ -164,22 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ok && !*abort) tile.store(p, bm, bn, c_vec != 0, acc);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                         cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    tried = true;
-  }
-  return fn;
-}
-
 }  // namespace tma_ffma
 
 namespace {
@@ -188,9 +159,7 @@ template <class Cf>
 cudaError_t launch_cfg(const Problem& p, bool c_vec, const WaitCfg& wc,
                        cudaStream_t stream) {
   using namespace tma_ffma;
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  std::call_once(once, [] { encode = encode_fn(); });
+  const auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   const cuuint32_t estr[2] = {1, 1};
