@@ -62,6 +62,9 @@ def parse_args():
     p.add_argument("--from-f32", action="store_true",
                    help="with --precision bf16/f16: time gemm_f32_mixed "
                         "(fp32 operands rounded inside the step)")
+    p.add_argument("--graph", action="store_true",
+                   help="capture the timed steps in CUDA graphs (one per "
+                        "timing chunk) and time their replay")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -302,11 +305,31 @@ def timed_region(step, args, stream, dev, world):
     nchunks = min(5, args.steps)
     edges = [round(c * args.steps / nchunks) for c in range(nchunks + 1)]
     events = [torch.cuda.Event(enable_timing=True) for _ in edges]
+    graphs = None
+    if getattr(args, "graph", False):
+        # each chunk's steps captured once (the warm-up above did the
+        # library's one-time set-up eagerly), replayed once untimed
+        cap = torch.cuda.Stream(dev)
+        graphs = []
+        for c in range(nchunks):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(edges[c], edges[c + 1]):
+                    step(i, cap)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for g in graphs:
+                g.replay()
+        torch.cuda.synchronize()
     wall0 = time.perf_counter()
     events[0].record(stream)
     for c in range(nchunks):
-        for i in range(edges[c], edges[c + 1]):
-            step(i)
+        if graphs is not None:
+            with torch.cuda.stream(stream):
+                graphs[c].replay()
+        else:
+            for i in range(edges[c], edges[c + 1]):
+                step(i)
         events[c + 1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -436,29 +459,32 @@ def run_ours(args, w, config):
             synth.make_operands(1, w.N, 1, seed=7)[1][0]).to(dev)
         eact = 1 if args.epilogue == "bias_gelu" else 0
 
-    def step(i):
+    def step(i, on=None):
+        # on: the stream to launch on (the capture stream in graph mode)
+        s_obj = on if on is not None else stream
+        h = s_obj.cuda_stream
         if fused:
             ta, tb, tc = sets[i % nsets]
             G.gemm_f32_bias_act_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K,
                                     tb.data_ptr(), w.N, ebias.data_ptr(),
                                     eact, tc.data_ptr(), w.N,
                                     ws.data_ptr() if ws is not None else 0,
-                                    ws_bytes, handle)
+                                    ws_bytes, h)
             return
         if batched:
             xa, xb, xc = bsets[i % nsets]
             G.gemm_f32_batched(xa, xb, xc, trans_a=ta_, trans_b=tb_,
-                               stream=stream)
+                               stream=s_obj)
             return
         ta, tb, tc = sets[i % nsets]
         if algo == 0:
             G.gemm_f32_ws_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K,
                               tb.data_ptr(), w.N, tc.data_ptr(), w.N,
                               ws.data_ptr() if ws is not None else 0,
-                              ws_bytes, handle)
+                              ws_bytes, h)
         else:
             G.gemm_f32_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K, tb.data_ptr(),
-                           w.N, tc.data_ptr(), w.N, handle, algo)
+                           w.N, tc.data_ptr(), w.N, h, algo)
 
     ms, ms_max, clocks, wall = timed_region(step, args, stream, dev, world)
 
@@ -622,17 +648,18 @@ def run_mixed(args, w, config):
     ws_bytes = G.mixed_workspace_size(w.M, w.N, w.K)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
-    def step(i):
+    def step(i, on=None):
+        h = (on if on is not None else stream).cuda_stream
         xa, xb, xc = sets[i % nsets]
         if args.from_f32:
             fa, fb = f32[i % nsets]
             G.gemm_f32_mixed_ptr(t, w.M, w.N, w.K, fa.data_ptr(), w.K,
                                  fb.data_ptr(), w.N, xc.data_ptr(), w.N,
-                                 ws.data_ptr(), ws_bytes, handle)
+                                 ws.data_ptr(), ws_bytes, h)
         else:
             G.gemm_f32_mixed16_ptr(t, w.M, w.N, w.K, xa.data_ptr(), w.K,
                                    xb.data_ptr(), w.N, xc.data_ptr(), w.N,
-                                   handle)
+                                   h)
 
     ms, ms_max, clocks, wall = timed_region(step, args, stream, dev, world)
     flops = float(w.flops)
@@ -728,7 +755,8 @@ def main():
               "l2": "rotating input/output sets between timed steps, "
                     "together more than 2x the L2 size (at least 3 sets "
                     f"of {w.bytes / 2**20:.1f} MiB)",
-              "parallelism": f"independent problem per GPU x {args.gpus}"}
+              "parallelism": f"independent problem per GPU x {args.gpus}",
+              "launch": "CUDA graph replay" if args.graph else "stream"}
     if args.precision != "fp32":
         config["precision"] = (f"{args.precision} operands, fp32 products, "
                                "sums and C")
