@@ -115,3 +115,55 @@ def test_product_has_no_oracle_or_cpu_fallback():
         assert "oracle" not in text.replace("float64 oracle", ""), name
         assert "torch.matmul" not in text and "np.matmul" not in text, name
         assert " @ " not in text, name
+
+
+C_PROGRAM = r"""
+/* A plain C99 caller of the library: only the public header, no CUDA
+   headers, no C++.  Every call below is answered by the host-side checks,
+   before any CUDA call, so no GPU is needed. */
+#include <stdio.h>
+#include <string.h>
+#include "gemm_f32.h"
+
+static int fails = 0;
+#define EXPECT(cond) do { if (!(cond)) { printf("FAIL %s\n", #cond); ++fails; } } while (0)
+
+int main(void) {
+    float a[4] = {0}, b[4] = {0}, c[4] = {0};
+    EXPECT(gemm_f32_version() >= 100);
+    EXPECT(strcmp(gemm_f32_status_string(GEMM_F32_OK), "ok") == 0);
+    EXPECT(gemm_f32(-1, 2, 2, a, 2, b, 2, c, 2, NULL) == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32(2, 2, 2, a, 1, b, 2, c, 2, NULL) == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32(2, 2, 2, NULL, 2, b, 2, c, 2, NULL) == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32(0, 2, 2, NULL, 2, NULL, 2, NULL, 2, NULL) == GEMM_F32_OK);
+    EXPECT(gemm_f32_ex(2, 2, 2, a, 2, b, 2, c, 2, NULL, 99) == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32_batched(GEMM_F32_OP_N, 7, 2, 2, 2, a, 2, 0, b, 2, 0, c, 2, 0, 1, NULL)
+           == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32_bias_act(2, 2, 2, a, 2, b, 2, NULL, 5, c, 2, NULL, 0, NULL)
+           == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32_mixed16(7, 2, 2, 2, a, 8, b, 8, c, 2, NULL) == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32_round16(GEMM_F32_MIXED_BF16, 2, 4, a, 2, b, 4, NULL)
+           == GEMM_F32_ERR_INVALID_ARG);
+    EXPECT(gemm_f32_mixed_workspace_size(-1, 1, 1) < 0);
+    EXPECT(gemm_f32_host(2, 2, 2, a, 1, b, 2, c, 2, NULL, NULL, NULL, NULL, 0, NULL)
+           == GEMM_F32_ERR_INVALID_ARG);
+    printf("%s\n", fails ? "C caller: failures" : "C caller: ok");
+    return fails != 0;
+}
+"""
+
+
+def test_plain_c_caller(built_lib, tmp_path):
+    """The header compiles as C99 and a C program linked against the
+    library gets the documented status codes."""
+    src = tmp_path / "caller.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(built_lib)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe), "-L", libdir, "-l:" + os.path.basename(built_lib),
+                    "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "C caller: ok" in out.stdout
