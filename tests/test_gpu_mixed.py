@@ -247,3 +247,31 @@ def test_mixed16_timeout_path_reports_and_recovers():
     want, _, _ = oracle.gemm_mixed(a, b, G.MIXED_BF16)
     assert_bitexact(run_mixed16(a, b, G.MIXED_BF16), want, what="after")
     assert G.device_status() == 0
+
+
+@pytest.mark.parametrize("t", TYPES, ids=TYPE_IDS)
+def test_mixed16_unaligned_c_direct_stores(t):
+    """C that no tensor map can describe (offset by one element, odd
+    leading dimension): the epilogue stores lane by lane, guarded."""
+    M, N, K = 300, 520, 136
+    a, b = synth.make_operands(M, N, K, seed=41, dist_a="int8")
+    ah, bh = oracle.round_half(a, t), oracle.round_half(b, t)
+    store = torch.full((M * (N + 3) + 1,), float("nan"), device=DEV)
+    c = store[1:].view(M, N + 3)[:, :N]  # 4-byte aligned only, ldc = N + 3
+    G.gemm_f32_mixed16(_dev16(ah, t), _dev16(bh, t), c)
+    torch.cuda.synchronize()
+    want, _, _ = oracle.gemm_mixed(a, b, t)
+    assert_bitexact(c.cpu().numpy(), want, what="unaligned C")
+    pad = store[1:].view(M, N + 3)[:, N:]
+    assert torch.isnan(pad).all()  # the padding is left alone
+
+
+def test_f16_rounding_overflows_to_inf():
+    """fp32 values beyond binary16's range round to ±Inf, as the oracle's
+    IEEE rounding says; bfloat16 keeps them finite."""
+    x = np.array([[7.0e4, -7.0e4, 65519.0, 65520.0, 1e38, -1e-8]], np.float32)
+    for t in TYPES:
+        got = G.round16(torch.from_numpy(x).to(DEV), t)
+        torch.cuda.synchronize()
+        bits = got.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(bits, oracle.round_half(x, t))
