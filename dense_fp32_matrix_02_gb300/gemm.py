@@ -558,3 +558,64 @@ def ffma_peak_flops(iters) -> int:
     if n < 0:
         _check(-n, "gemm_f32_ffma_peak_flops")
     return n
+
+
+# ------------------------------------------------ layout-aware front end
+def _operand_form(t, name):
+    """(op, rows, cols, ld, batch, batch_stride) of a 2-D or 3-D float32
+    CUDA tensor whose matrices are row-major (op N) or transposed views of
+    row-major storage (op T, rows/cols of the logical matrix)."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or \
+            not t.is_cuda:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+    if t.dim() == 2:
+        batch, sb = 1, 0
+        r, c = t.shape
+        s0, s1 = t.stride()
+    elif t.dim() == 3:
+        batch, r, c = t.shape
+        sb = t.stride(0) if batch > 1 else 0
+        s0, s1 = t.stride(1), t.stride(2)
+    else:
+        raise ValueError(f"{name} must be 2-D or 3-D")
+    if s1 == 1 or c <= 1:
+        return OP_N, r, c, max(s0 if r > 1 else c, c, 1), batch, sb
+    if s0 == 1 or r <= 1:
+        # element (i, j) at i + j·s1: the transpose of a c×r row-major
+        # matrix with leading dimension s1
+        return OP_T, r, c, max(s1 if c > 1 else r, r, 1), batch, sb
+    raise ValueError(f"{name}: neither rows nor columns are contiguous; "
+                     "pass a row-major tensor or a transposed view of one")
+
+
+def matmul(a, b, out=None, stream=None):
+    """The product a·b for float32 CUDA tensors, 2-D or batched 3-D (a 2-D
+    operand is shared by every product), where each operand may be
+    row-major or a transposed view of row-major storage (e.g. ``w.t()``):
+    the library reads it in place through gemm_f32_batched, without a copy.
+    Returns C (row-major, allocated if ``out`` is None)."""
+    import torch
+    opa, M, K, lda, ba, sa = _operand_form(a, "a")
+    opb, K2, N, ldb, bb, sb = _operand_form(b, "b")
+    if K != K2:
+        raise ValueError(f"inner sizes differ: {tuple(a.shape)} x "
+                         f"{tuple(b.shape)}")
+    batch = max(ba, bb)
+    if ba not in (1, batch) or bb not in (1, batch):
+        raise ValueError("batch sizes differ")
+    shape = (batch, M, N) if (a.dim() == 3 or b.dim() == 3) else (M, N)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=a.device)
+    elif tuple(out.shape) != shape or out.dtype != torch.float32:
+        raise ValueError(f"out must be a float32 tensor of shape {shape}")
+    opc, Mc, Nc, ldc, bc, sc = _operand_form(out, "out")
+    if opc != OP_N:
+        raise ValueError("out must be row-major")
+    if batch > 1 and sc == 0:
+        raise ValueError("out must hold one matrix per product")
+    with torch.cuda.device(a.device):
+        gemm_f32_batched_ptr(opa, opb, M, N, K, a.data_ptr(), lda, sa,
+                             b.data_ptr(), ldb, sb, out.data_ptr(), ldc, sc,
+                             batch, _handle(stream, a.device))
+    return out
