@@ -24,7 +24,8 @@ enum : unsigned int {
 // One problem as the kernels see it.  Leading dimensions in elements.
 // Batched calls add per-matrix element strides; a kernel launched with
 // gridDim.z = batch handles matrix blockIdx.z.  transA / transB: the operand
-// is stored transposed (A as K×M with row stride lda, B as N×K with ldb).
+// is stored transposed (A as K×M with row stride lda, B as N×K with ldb);
+// storeT: the product is written to C transposed.
 struct Problem {
   int M, N, K;
   const float* A;
@@ -36,6 +37,8 @@ struct Problem {
   long long sA = 0, sB = 0, sC = 0;  // batch strides (elements)
   int batch = 1;
   int transA = 0, transB = 0;
+  // store Cᵀ (row n of the stored matrix = column n of the computed tile)
+  int storeT = 0;
   // fused epilogue: C = act(A·B + bias), bias indexed by column (or NULL)
   const float* bias = nullptr;
   int act = 0;  // 0 identity, 1 GELU

@@ -362,14 +362,14 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
                    mult4(sA) && mult4(sB);
   const bool c_vec = aligned16(C) && mult4(ldc) && mult4(sC);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The tensor kernel takes NN, NT and TT (TN has no copy-free mapping onto
-  // its operand layouts) when TMA can describe every operand: aligned, and
-  // batch strides 0 or at least one whole stored matrix.
+  // The tensor kernel takes every form (TN through its converters) when
+  // TMA can describe every operand: aligned, and batch strides 0 or at
+  // least one whole stored matrix.
   const int64_t rows_a = ta ? K : M, rows_b = tb ? N : K;
   const bool strides_ok = (batch == 1) ||
                           ((sA == 0 || sA >= rows_a * lda) &&
                            (sB == 0 || sB >= rows_b * ldb));
-  if (d->cc_major == 10 && vec && K >= 1 && !(ta && !tb) && strides_ok &&
+  if (d->cc_major == 10 && vec && K >= 1 && strides_ok &&
       env_int("GEMM_F32_AUTO_SIMT", 0) == 0) {
     Problem q = p;
     if (ta && tb) {  // C = (B·A)ᵀ: swap the operands, store the transpose
@@ -381,8 +381,9 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
       q.B = A;
       q.ldb = lda;
       q.sB = sA;
-      q.transA = 1;  // marks the swapped form
+      q.transA = 0;
       q.transB = 0;
+      q.storeT = 1;
     }
     WaitCfg wc;
     wc.limit = g_wait_ns.load();

@@ -61,11 +61,17 @@ namespace tf32x3 {
 // 128 rows n of 16 k (64-byte swizzle) and a converter lane reads its own
 // row instead of a column.  TSTORE: the product computed is Cᵀ and is
 // stored transposed (used for op(A)ᵀ·op(B)ᵀ = (B·A)ᵀ with A, B swapped).
+// TA: A is stored transposed (K×M, M-contiguous); its tile lands as 16 rows
+// k of 128 m in a staging buffer, and each converter lane takes one m (a
+// column of the staged tile, contiguous across the warp) and writes the
+// raw value and the small part K-major, in the 64-byte swizzle TMA would
+// have used, into the stage's A buffers.
 template <int TILE_M, int STAGES, bool RAW_BIG, bool TB = false,
-          bool TSTORE = false>
+          bool TSTORE = false, bool TA = false>
 struct Cfg {
   static constexpr bool kTB = TB;
   static constexpr bool kTStore = TSTORE;
+  static constexpr bool kTA = TA;
   // RAW_BIG: the MMAs read the raw fp32 operands as their "big" part and the
   // tensor core keeps their top 19 bits (TF32 truncation); converters then
   // write only small = x - trunc(x).  Otherwise big is rounded to the
@@ -85,12 +91,16 @@ struct Cfg {
   static constexpr uint32_t kIdesc = idesc_tf32(kTileN, kTileM);
   static constexpr int kOffASmall = kStages * kStageBytesA;
   static constexpr int kOffB = 2 * kStages * kStageBytesA;
-  static constexpr int kOffCtl = kOffB + kStages * kStageBytesB;
+  // TA: the staging buffers of the stored (transposed) A tiles
+  static constexpr int kOffAT = kOffB + kStages * kStageBytesB;
+  static constexpr int kOffCtl = kOffAT + (TA ? kStages * kStageBytesA : 0);
   static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
   static_assert(kTmemNeed <= kTmemCols, "TMEM budget");
   static_assert(TILE_M % 16 == 0 && TILE_M >= 64 && TILE_M <= 256,
                 "MMA N in [64, 256], multiple of 16");
   static_assert(!TB || RAW_BIG, "transposed B only with the raw split");
+  static_assert(!TA || (RAW_BIG && TILE_M == 128 && !TB && !TSTORE),
+                "transposed A: raw split, 128-row tiles, plain B and store");
 };
 
 constexpr int kMaxStages = 8;
@@ -240,8 +250,12 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
             break;
           }
           mbar_arrive_expect_tx(full(s), kStageBytesA + kStageBytesB);
-          tma_load_3d(sbase + s * kStageBytesA, &tmap_a, full(s),
-                      (kb0 + kb) * kBK, bm, za);
+          if constexpr (Cf::kTA)  // stored A: x = m, y = k
+            tma_load_3d(sbase + Cf::kOffAT + s * kStageBytesA, &tmap_a,
+                        full(s), bm, (kb0 + kb) * kBK, za);
+          else
+            tma_load_3d(sbase + s * kStageBytesA, &tmap_a, full(s),
+                        (kb0 + kb) * kBK, bm, za);
           if constexpr (Cf::kTB)
             tma_load_3d(sbase + kOffB + s * kStageBytesB, &tmap_b, full(s),
                         (kb0 + kb) * kBK, bn, zb);
@@ -343,15 +357,44 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         }
         tmem_st8(tcol, big);
         tmem_st8(tcol + kBK, small);
-        // A: the raw tile stays the big part; only small is written
+        if constexpr (Cf::kTA) {
+          // A row m = n_loc, k in [8h, 8h + 8): read down column m of the
+          // staged [k][m] tile, write two 16-byte chunks of row m, raw and
+          // small, at chunk c ^ ((m >> 1) & 3) of the 64-byte rows
+          const float* acol = reinterpret_cast<const float*>(
+                                  smem + Cf::kOffAT + s * kStageBytesA) +
+                              n_loc + 8 * h * kTileM;
+          float ax[8];
 #pragma unroll
-        for (int j = 0; j < kChunksPerThread; ++j) {
-          const int c = t + 32 * kConvWarps * j;
-          const float4 v = araw[c];
-          asml[c] = make_float4(__uint_as_float(tf32_small_of_truncated(v.x)),
-                                __uint_as_float(tf32_small_of_truncated(v.y)),
-                                __uint_as_float(tf32_small_of_truncated(v.z)),
-                                __uint_as_float(tf32_small_of_truncated(v.w)));
+          for (int k = 0; k < 8; ++k) ax[k] = acol[k * kTileM];
+          unsigned char* rraw = smem + s * kStageBytesA + n_loc * 64;
+          unsigned char* rsml =
+              smem + kOffASmall + s * kStageBytesA + n_loc * 64;
+          const int sw = (n_loc >> 1) & 3;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int pos = ((2 * h + c) ^ sw) << 4;
+            *reinterpret_cast<float4*>(rraw + pos) =
+                make_float4(ax[4 * c], ax[4 * c + 1], ax[4 * c + 2],
+                            ax[4 * c + 3]);
+            *reinterpret_cast<float4*>(rsml + pos) = make_float4(
+                __uint_as_float(tf32_small_of_truncated(ax[4 * c])),
+                __uint_as_float(tf32_small_of_truncated(ax[4 * c + 1])),
+                __uint_as_float(tf32_small_of_truncated(ax[4 * c + 2])),
+                __uint_as_float(tf32_small_of_truncated(ax[4 * c + 3])));
+          }
+        } else {
+          // A: the raw tile stays the big part; only small is written
+#pragma unroll
+          for (int j = 0; j < kChunksPerThread; ++j) {
+            const int c = t + 32 * kConvWarps * j;
+            const float4 v = araw[c];
+            asml[c] = make_float4(
+                __uint_as_float(tf32_small_of_truncated(v.x)),
+                __uint_as_float(tf32_small_of_truncated(v.y)),
+                __uint_as_float(tf32_small_of_truncated(v.z)),
+                __uint_as_float(tf32_small_of_truncated(v.w)));
+          }
         }
       } else {
 #pragma unroll
@@ -521,9 +564,12 @@ cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
-  if (!encode_3d(encode, &ta, p.A, p.K, p.M, p.lda, p.sA, p.batch, Cf::kBK,
-                 Cf::kTileM, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
+  const bool ok_a =
+      Cf::kTA ? encode_3d(encode, &ta, p.A, p.M, p.K, p.lda, p.sA, p.batch,
+                          Cf::kTileM, Cf::kBK, CU_TENSOR_MAP_SWIZZLE_NONE)
+              : encode_3d(encode, &ta, p.A, p.K, p.M, p.lda, p.sA, p.batch,
+                          Cf::kBK, Cf::kTileM, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok_a) return cudaErrorInvalidValue;
   const bool ok_b =
       Cf::kTB ? encode_3d(encode, &tb, p.B, p.K, p.N, p.ldb, p.sB, p.batch,
                           Cf::kBK, Cf::kTileN, CU_TENSOR_MAP_SWIZZLE_64B)
@@ -587,9 +633,12 @@ cudaError_t launch_tf32x3(const Problem& p, int cfg, int splits,
       if (p.transB)  // A·Bᵀ with B stored N×K
         return launch_cfg<Cfg<128, 4, true, true>>(p, splits, partials, wc,
                                                    stream);
-      if (p.transA)  // caller passed (B, A) swapped: store the transpose
+      if (p.storeT)  // caller passed (B, A) swapped: store the transpose
         return launch_cfg<Cfg<128, 4, true, false, true>>(p, splits, partials,
                                                           wc, stream);
+      if (p.transA)  // Aᵀ·B with A stored K×M: A transposed by the converters
+        return launch_cfg<Cfg<128, 3, true, false, false, true>>(
+            p, splits, partials, wc, stream);
       return launch_cfg<Cfg<128, 4, true>>(p, splits, partials, wc, stream);
     case kTc256Raw:
       return launch_cfg<Cfg<256, 5, true>>(p, splits, partials, wc, stream);

@@ -142,8 +142,8 @@ typedef enum {
  * batch = 0, M = 0 or N = 0 launches nothing; batch <= 65535.  Kernel
  * choice as for gemm_f32: the 3xTF32 tensor kernel where its layouts allow
  * (16-byte aligned operands, leading dimensions and strides multiples of 4,
- * forms NN, NT and TT), the FFMA kernel otherwise.  Within the tolerance of
- * gemm_f32 for every form.
+ * every form), the FFMA kernel otherwise.  Within the tolerance of gemm_f32
+ * for every form.
  */
 GEMM_F32_API int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N,
                                   int64_t K, const float *A, int64_t lda,

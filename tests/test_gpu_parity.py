@@ -637,7 +637,7 @@ def test_batched_binding_and_empty_batch():
 
 @pytest.mark.parametrize("form", ["NN", "NT", "TN", "TT"])
 def test_batched_forms_forced_simt(form):
-    """The FFMA path for every form (the tensor path takes NN/NT/TT when
+    """The FFMA path for every form (the tensor path takes every form when
     the layouts allow; here every form runs on the FFMA kernel)."""
     with _env("GEMM_F32_AUTO_SIMT", 1):
         As, Bs, Cs, _, _, _ = _batched_case(form, 300, 260, 77, 3, seed=11,
@@ -646,7 +646,7 @@ def test_batched_forms_forced_simt(form):
         check_full(As[i], Bs[i], Cs[i][:, :260], what=f"simt {form} b{i}")
 
 
-@pytest.mark.parametrize("form", ["NT", "TT"])
+@pytest.mark.parametrize("form", ["NT", "TT", "TN"])
 def test_transposed_forms_large_sampled(form):
     """op forms at 2048 x 1536 x 1024, sampled against the oracle."""
     M, N, K = 2048, 1536, 1024
