@@ -14,10 +14,12 @@
 // and fill the rest with zeros, and the epilogue stores only elements inside
 // M×N.
 //
-// A is copied one float at a time so it can land transposed (As[BK][BM],
-// as in §3.4 of the same page); B is copied in 16-byte chunks when VEC is
-// true (B 16-byte aligned, ldb a multiple of 4) and one float at a time
-// otherwise, so any alignment and any leading dimension work.
+// With aligned operands (VEC: 16-byte aligned, leading dimensions multiples
+// of 4) A is copied in 16-byte chunks and kept K-major (FfmaTile, read along
+// K); otherwise it is copied one float at a time and lands transposed
+// (As[BK][BM], as in §3.4 of the same page; FfmaTileT).  B is copied in
+// 16-byte chunks when VEC holds and one float at a time otherwise, so any
+// alignment and any leading dimension work.
 #include <type_traits>
 
 #include "ffma_tile.cuh"

@@ -22,24 +22,33 @@
 //   * the MMA's A operand is Bᵀ (128 columns of C × k), written into TMEM by
 //     converter threads: TMEM lane n takes column n of the B tile, which the
 //     32 threads of a warp read as contiguous rows of B in shared memory;
-//   * the MMA's B operand is the A tile (256 rows of C × k), K-major as TMA
-//     copies it from row-major A, 64-byte swizzled.
+//   * the MMA's B operand is the A tile (TILE_M rows of C × k), K-major as
+//     TMA copies it from row-major A, 64-byte swizzled.
 // The fp32 accumulator D (TMEM lane = column n of C, TMEM column = row m of
 // C) is read back by the same converter warps, whose 32 lanes then store 32
 // consecutive columns of one row of C.
 //
-// Warp roles (320 threads, one CTA per SM):
-//   warp 0     TMA producer (one thread): A tile 256×16, B tile 16×128 per
-//              stage into a 5-stage ring, completion counted on full[s];
+// Tiles: TILE_M rows × 128 columns of C.  The default is 128 × 128 with a
+// 4-stage ring of 16-deep k stages (24 KB each) and 256 TMEM columns, so
+// two CTAs share each SM and one CTA's epilogue overlaps the other's main
+// loop; TILE_M = 256 (5 stages, one CTA per SM) is the alternative.
+// Warp roles (320 threads):
+//   warp 0     TMA producer (one thread): the A tile TILE_M×16 and the B
+//              tile 16×128 of each stage, completion counted on full[s];
 //   warp 1     TMEM allocator and MMA issuer (one thread): waits conv[s],
-//              issues 2 k-steps × 3 TF32 MMAs (M=128, N=256, K=8), commits
-//              the stage's release to empty[s];
+//              issues 2 k-steps × 3 TF32 MMAs (M = 128, N = TILE_M, K = 8),
+//              commits the stage's release to empty[s];
 //   warps 2-9  converters, two per TMEM lane quarter (a warp may only touch
 //              the 32 lanes of quarter warp % 4): each splits half of the
-//              stage's k range of Bᵀ into TMEM and a quarter of the A tile
-//              in shared memory (big written back in place, small into its
-//              own buffer), then stores half of its quarter's columns of D
-//              in the epilogue.
+//              stage's k range of Bᵀ into TMEM and its share of the A tile
+//              in shared memory (the small part into its own buffer; with
+//              the rounded split also big, written back in place), then
+//              stores half of its quarter's columns of D in the epilogue.
+// Operand forms (128 × 128 tiles): B stored N×K (TB), A stored K×M (TA,
+// transposed by the converters from a staging buffer), and C stored
+// transposed (TSTORE) for the swapped form of op(A)ᵀ·op(B)ᵀ; strided
+// batches run as gridDim.z; split-K writes partial tiles that a second
+// kernel adds in split order.
 // Every mbarrier wait is bounded by a %globaltimer deadline; a wait that
 // runs out sets the status word and a CTA-wide abort flag, the roles drain
 // their copies and MMAs in flight, TMEM is freed, and the CTA ends without
