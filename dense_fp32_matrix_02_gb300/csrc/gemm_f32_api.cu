@@ -83,6 +83,7 @@ struct Plan {
   int simt_cfg;  // for ALGO_SIMT
   int tc_cfg;    // for ALGO_TF32X3
   int splits;    // split-K factor for ALGO_TF32X3 (1 = none)
+  int full_tiles;  // tiles computed whole before the split ones
   long long ws_bytes;  // scratch the plan needs (0 = none)
   bool vec;      // 16-byte operand copies
   bool c_vec;    // 16-byte C stores
@@ -123,18 +124,41 @@ int choose_tc_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   return kTc128Raw;
 }
 
-// Split-K factor for the tensor path: enough CTAs to fill every slot when
-// the tiles alone leave most SMs idle, at least 8 k stages per split.
-int choose_splits(int64_t M, int64_t N, int64_t K, int tile_m,
-                  const DeviceInfo& d) {
+// Split-K for the tensor path, so that the CTAs fill the GPU:
+//  * tiles fill fewer than half of the CTA slots: every tile is split,
+//    slots / tiles ways;
+//  * otherwise the tiles of the last, partly filled round (tiles mod slots
+//    of them) are split floor(slots / tail) ways, so they spread over the
+//    whole GPU instead of running one per SM while the rest idle (a lone
+//    tile costs about as long as a full round);
+// at least 8 k stages per split, at most 16 splits.  GEMM_F32_SPLITS forces
+// every tile to split that many ways; GEMM_F32_TAIL_SPLIT=0 keeps the last
+// round whole.
+void choose_splits(int64_t M, int64_t N, int64_t K, int tile_m,
+                   const DeviceInfo& d, Plan* plan) {
   const int forced = env_int("GEMM_F32_SPLITS", 0);
   const int64_t nk = (K + 15) / 16;
   const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + 127) / 128);
   const int64_t slots = (tile_m == 128 ? 2 : 1) * (int64_t)d.sm_count;
-  int64_t s = forced > 0 ? forced : (2 * tiles >= slots ? 1 : slots / tiles);
-  if (forced <= 0) s = std::min<int64_t>(s, nk / 8);
-  s = std::min<int64_t>(std::min<int64_t>(s, nk), 16);
-  return (int)std::max<int64_t>(s, 1);
+  int64_t s = 1, full = tiles;
+  if (forced > 0) {
+    s = std::min<int64_t>(std::min<int64_t>(forced, nk), 16);
+    full = 0;
+  } else if (2 * tiles < slots) {
+    s = std::min<int64_t>(std::min<int64_t>(slots / tiles, nk / 8), 16);
+    full = 0;
+  } else if (tiles % slots != 0 && env_int("GEMM_F32_TAIL_SPLIT", 1) != 0) {
+    const int64_t tail = tiles % slots;
+    s = std::min<int64_t>(std::min<int64_t>(slots / tail, nk / 8), 16);
+    full = tiles - tail;
+  }
+  if (s < 2) {
+    s = 1;
+    full = tiles;
+  }
+  plan->splits = (int)s;
+  plan->full_tiles = (int)full;
+  plan->ws_bytes = tf32x3_partials_bytes(tile_m, tiles - full, (int)s);
 }
 
 // Decides which kernel runs.  Returns a status; fills *plan on success.
@@ -148,6 +172,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   plan->simt_cfg = choose_simt_cfg(M, N, d);
   plan->tc_cfg = choose_tc_cfg(M, N, d);
   plan->splits = 1;
+  plan->full_tiles = 0;
   plan->ws_bytes = 0;
   const bool tcgen05_ok = d.cc_major == 10 && vec && K >= 1;
   switch (algo) {
@@ -170,10 +195,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     default:
       return GEMM_F32_ERR_INVALID_ARG;
   }
-  if (plan->algo == GEMM_F32_ALGO_TF32X3) {
-    plan->splits = choose_splits(M, N, K, tf32x3_tile_m(plan->tc_cfg), d);
-    if (plan->splits > 1) plan->ws_bytes = (long long)plan->splits * M * N * 4;
-  }
+  if (plan->algo == GEMM_F32_ALGO_TF32X3)
+    choose_splits(M, N, K, tf32x3_tile_m(plan->tc_cfg), d, plan);
   return GEMM_F32_OK;
 }
 
@@ -272,7 +295,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       wc.limit = g_wait_ns.load();
       wc.debug = g_debug_flags.load();
       wc.status = d->status;
-      e = launch_tf32x3(p, plan.tc_cfg, plan.splits,
+      e = launch_tf32x3(p, plan.tc_cfg, plan.full_tiles, plan.splits,
                         plan.splits > 1 ? static_cast<float*>(ws) : nullptr,
                         wc, s);
       break;
@@ -389,7 +412,7 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
     wc.limit = g_wait_ns.load();
     wc.debug = g_debug_flags.load();
     wc.status = d->status;
-    e = launch_tf32x3(q, kTc128Raw, 1, nullptr, wc, s);
+    e = launch_tf32x3(q, kTc128Raw, 0, 1, nullptr, wc, s);
   } else {
     e = launch_simt(p, choose_simt_cfg(M, N, *d), vec, c_vec, s);
   }

@@ -52,9 +52,10 @@ enum TcCfg {
 
 int tf32x3_tile_m(int cfg);
 
-// Bytes of partial tiles a split-K launch with `splits` > 1 writes (and the
-// reduction reads): splits × M × N floats.
-long long tf32x3_partials_bytes(const Problem& p, int splits);
+// Bytes of the partial tiles a launch that splits `split_tiles` tiles of
+// tile_m × 128 over `splits` > 1 CTAs each writes (and the reduction reads).
+long long tf32x3_partials_bytes(int tile_m, long long split_tiles,
+                                int splits);
 
 // 3xTF32 tcgen05 kernel.  Needs A, B 16-byte aligned, lda and ldb multiples
 // of 4, K >= 1 and an sm_100-family device.  Batched problems (p.batch > 1,
@@ -62,11 +63,13 @@ long long tf32x3_partials_bytes(const Problem& p, int splits);
 // with configuration kTc128Raw, one of p.transB (B stored N×K), p.transA
 // (A stored K×M) or p.storeT (C stored transposed: the caller swapped the
 // operands, op(A)ᵀ·op(B)ᵀ computed as B·A).  With splits > 1 and a
-// `partials` buffer of tf32x3_partials_bytes, the K range is split over
-// `splits` CTAs per tile and a second kernel sums the partial tiles into C
-// in split order (deterministic).  splits is reduced so no split is empty.
-cudaError_t launch_tf32x3(const Problem& p, int cfg, int splits,
-                          float* partials, const WaitCfg& wc,
+// `partials` buffer of tf32x3_partials_bytes for the tiles past the first
+// full_tiles (grouped order), each of those tiles' K range is split over
+// `splits` CTAs and a second kernel sums the partial tiles into C in split
+// order (deterministic); full_tiles = 0 splits every tile.  splits is
+// reduced so no split is empty.  Single products only.
+cudaError_t launch_tf32x3(const Problem& p, int cfg, int full_tiles,
+                          int splits, float* partials, const WaitCfg& wc,
                           cudaStream_t stream);
 
 // Scratch bytes the automatic plan wants for these arguments on the current

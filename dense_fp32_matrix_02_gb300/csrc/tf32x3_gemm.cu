@@ -175,8 +175,9 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, float* C,
                        long long ldc, int M, int N, int K, int tiles_m,
-                       int tiles_n, int splits, int kb_per_split,
-                       float* partials, long long sC, int batched_ab,
+                       int tiles_n, int full_tiles, int tail_splits,
+                       int kb_per_split, float* partials, long long sC,
+                       int batched_ab,
                        const float* bias, int act, WaitCfg wc) {
   // batch: matrix blockIdx.z; tensor-map batch coordinates are z for a
   // batched operand and 0 for one shared by every product (batched_ab bits
@@ -196,24 +197,35 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   volatile int* abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // split-K: the `splits` CTAs of one tile are adjacent in the grid; split
-  // s covers k stages [s·kb_per_split, min(nk, (s+1)·kb_per_split)) and, when
-  // splits > 1, writes its partial tile to partials[s] (an M×N row-major
-  // slice) for the reduction kernel.
-  const int split = blockIdx.x % splits;
+  // Work of this CTA.  The first full_tiles CTAs each take one whole tile
+  // (in the grouped tile order) and store it to C.  Each tile after those
+  // (a tail tile: the last, partly filled round of CTAs) is split over
+  // tail_splits adjacent CTAs: CTA full_tiles + j·tail_splits + s sums k
+  // stages [s·kb_per_split, min(nk, (s+1)·kb_per_split)) of tail tile j and
+  // stores that partial tile, TILE_M × 128 row-major, to workspace slot
+  // j·tail_splits + s; a second kernel adds the slots in split order.
+  const bool whole = (int)blockIdx.x < full_tiles;
+  const int jt = whole ? 0 : ((int)blockIdx.x - full_tiles) / tail_splits;
+  const int split = whole ? 0 : ((int)blockIdx.x - full_tiles) % tail_splits;
   int tm, tn;
-  tile_coords<8>(blockIdx.x / splits, tiles_m, tiles_n, tm, tn);
+  tile_coords<8>(whole ? (int)blockIdx.x : full_tiles + jt, tiles_m, tiles_n,
+                 tm, tn);
   const int bm = tm * kTileM, bn = tn * kTileN;
   const int nk_total = (K + kBK - 1) / kBK;
   const int kb0 = split * kb_per_split;
-  const int nk = min(nk_total, kb0 + kb_per_split) - kb0;  // >= 1 (host)
+  const int nk = whole ? nk_total
+                       : min(nk_total, kb0 + kb_per_split) - kb0;  // >= 1
   const int z = blockIdx.z;
   const int za = (batched_ab & 1) ? z : 0, zb = (batched_ab & 2) ? z : 0;
+  // element (m, n) goes to out[(m − mo)·ldo + (n − no)]
   float* out = C + z * sC;
   long long ldo = ldc;
-  if (splits > 1) {
-    out = partials + (long long)split * M * N;
-    ldo = N;
+  int mo = 0, no = 0;
+  if (!whole) {
+    out = partials + (long long)(jt * tail_splits + split) * kTileM * kTileN;
+    ldo = kTileN;
+    mo = bm;
+    no = bn;
   }
 
   auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
@@ -443,7 +455,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         const int n = bn + n_loc;
         const int c_begin = h * (kAccCols / 2);
         // this lane's column n has one bias value; load it once
-        const bool epi = splits == 1 && (bias != nullptr || act != 0);
+        const bool epi = whole && (bias != nullptr || act != 0);
         const float bias_n =
             (epi && bias != nullptr && n < N) ? bias[n] : 0.f;
 #pragma unroll 1
@@ -470,7 +482,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
               }
             }
           } else if (n < N) {
-            // fused epilogue (not on split-K partials: the reduction has it)
+            // fused epilogue (not on partial tiles: the reduction has it)
             if (epi) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -482,7 +494,9 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int m = bm + c0 + i;
-              if (m < M) out[(long long)m * ldo + n] = __uint_as_float(v[i]);
+              if (m < M)
+                out[(long long)(m - mo) * ldo + (n - no)] =
+                    __uint_as_float(v[i]);
             }
           }
         }
@@ -498,44 +512,48 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   }
 }
 
-// C[i][j] = sum over s = 0..splits-1, in that order, of partials[s][i][j].
-// Each thread sums four consecutive elements of one row.
+// Tail tile j (tile full_tiles + j in the grouped order): C = the sum over
+// s = 0..tail_splits−1, in that order, of partial slot j·tail_splits + s,
+// then the fused epilogue.  Each thread adds four consecutive columns of one
+// row of one tile.
 __global__ void __launch_bounds__(256)
-    splitk_reduce_kernel(const float* __restrict__ partials, int splits,
-                         int M, int N, float* __restrict__ C, long long ldc,
-                         int vec, const float* __restrict__ bias, int act) {
+    tail_reduce_kernel(const float* __restrict__ partials, int tail_splits,
+                       int full_tiles, int tail_tiles, int tile_m,
+                       int tiles_m, int tiles_n, int M, int N,
+                       float* __restrict__ C, long long ldc, int vec,
+                       const float* __restrict__ bias, int act) {
+  constexpr int kCols = 128, kGroups = kCols / 4;
   const bool epi = bias != nullptr || act != 0;
-  const long long groups_per_row = (N + 3) / 4;
-  const long long total = (long long)M * groups_per_row;
-  const long long slice = (long long)M * N;
+  const long long slot = (long long)tile_m * kCols;
+  const long long per_tile = (long long)tile_m * kGroups;
+  const long long total = (long long)tail_tiles * per_tile;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x;
        g < total; g += (long long)gridDim.x * blockDim.x) {
-    const int i = (int)(g / groups_per_row);
-    const int j = (int)(g % groups_per_row) * 4;
-    const float* src = partials + (long long)i * N + j;
-    float* dst = C + (long long)i * ldc + j;
-    if (vec && j + 3 < N) {
-      float4 acc = *reinterpret_cast<const float4*>(src);
-      for (int s = 1; s < splits; ++s) {
-        const float4 v = *reinterpret_cast<const float4*>(src + s * slice);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-      }
-      if (epi) {
-        acc.x = apply_epilogue(acc.x, bias, act, j);
-        acc.y = apply_epilogue(acc.y, bias, act, j + 1);
-        acc.z = apply_epilogue(acc.z, bias, act, j + 2);
-        acc.w = apply_epilogue(acc.w, bias, act, j + 3);
-      }
-      *reinterpret_cast<float4*>(dst) = acc;
+    const int j = (int)(g / per_tile);
+    const int rem = (int)(g % per_tile);
+    const int r = rem / kGroups, c4 = (rem % kGroups) * 4;
+    int tm, tn;
+    tile_coords<8>(full_tiles + j, tiles_m, tiles_n, tm, tn);
+    const int m = tm * tile_m + r, n = tn * kCols + c4;
+    if (m >= M || n >= N) continue;
+    const float* src = partials + (long long)j * tail_splits * slot +
+                       (long long)r * kCols + c4;
+    float4 acc = *reinterpret_cast<const float4*>(src);
+    for (int s = 1; s < tail_splits; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(src + s * slot);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    float a[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (epi)
+      for (int e = 0; e < 4; ++e) a[e] = apply_epilogue(a[e], bias, act, n + e);
+    float* dst = C + (long long)m * ldc + n;
+    if (vec && n + 3 < N) {
+      *reinterpret_cast<float4*>(dst) = make_float4(a[0], a[1], a[2], a[3]);
     } else {
-      for (int e = 0; e < 4 && j + e < N; ++e) {
-        float acc = src[e];
-        for (int s = 1; s < splits; ++s) acc += src[e + s * slice];
-        dst[e] = epi ? apply_epilogue(acc, bias, act, j + e) : acc;
-      }
+      for (int e = 0; e < 4 && n + e < N; ++e) dst[e] = a[e];
     }
   }
 }
@@ -567,8 +585,9 @@ bool encode_3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
 }
 
 template <class Cf>
-cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
-                       const WaitCfg& wc, cudaStream_t stream) {
+cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
+                       float* partials, const WaitCfg& wc,
+                       cudaStream_t stream) {
   using namespace tf32x3;
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
@@ -593,28 +612,38 @@ cudaError_t launch_cfg(const Problem& p, int splits, float* partials,
   const int tiles_m = (p.M + Cf::kTileM - 1) / Cf::kTileM;
   const int tiles_n = (p.N + Cf::kTileN - 1) / Cf::kTileN;
   const int nk = (p.K + Cf::kBK - 1) / Cf::kBK;
-  if (splits < 1 || !partials || p.batch > 1) splits = 1;
-  const int kb_per_split = (nk + splits - 1) / splits;
-  splits = (nk + kb_per_split - 1) / kb_per_split;  // no empty split
-  const long long grid = (long long)tiles_m * tiles_n * splits;
+  const long long tiles = (long long)tiles_m * tiles_n;
+  int ts = tail_splits;
+  long long full = full_tiles;
+  if (ts < 2 || !partials || p.batch > 1 || full < 0 || full >= tiles) {
+    ts = 1;
+    full = tiles;
+  }
+  const int kb_per_split = (nk + ts - 1) / ts;
+  ts = (nk + kb_per_split - 1) / kb_per_split;  // no empty split
+  if (ts < 2) full = tiles;
+  const long long tail = tiles - full;
+  const long long grid = full + tail * ts;
   if (grid > 0x7fffffffLL || p.batch < 1 || p.batch > 65535)
     return cudaErrorInvalidConfiguration;
   const int batched_ab =
       (p.batch > 1 && p.sA != 0 ? 1 : 0) | (p.batch > 1 && p.sB != 0 ? 2 : 0);
   fn<<<dim3((unsigned)grid, 1, (unsigned)p.batch), Cf::kThreads, kSmem,
-       stream>>>(ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, splits,
-                 kb_per_split, partials, p.sC, batched_ab, p.bias, p.act, wc);
+       stream>>>(ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n,
+                 (int)full, ts, kb_per_split, partials, p.sC, batched_ab,
+                 p.bias, p.act, wc);
   e = cudaGetLastError();
-  if (e != cudaSuccess || splits == 1) return e;
+  if (e != cudaSuccess || tail == 0) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
-                   p.ldc % 4 == 0 && p.N % 4 == 0)
+                   p.ldc % 4 == 0)
                       ? 1
                       : 0;
-  const long long groups = (long long)p.M * ((p.N + 3) / 4);
+  const long long groups = tail * Cf::kTileM * (128 / 4);
   const int blocks = (int)((groups + 255) / 256 < 4096 ? (groups + 255) / 256
                                                       : 4096);
-  splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(
-      partials, splits, p.M, p.N, p.C, p.ldc, vec, p.bias, p.act);
+  tail_reduce_kernel<<<blocks, 256, 0, stream>>>(
+      partials, ts, (int)full, (int)tail, Cf::kTileM, tiles_m, tiles_n, p.M,
+      p.N, p.C, p.ldc, vec, p.bias, p.act);
   return cudaGetLastError();
 }
 
@@ -625,32 +654,37 @@ int tf32x3_tile_m(int cfg) {
   return (cfg == kTc256 || cfg == kTc256Raw) ? 256 : 128;
 }
 
-long long tf32x3_partials_bytes(const Problem& p, int splits) {
-  return splits > 1 ? (long long)splits * p.M * p.N * 4 : 0;
+long long tf32x3_partials_bytes(int tile_m, long long split_tiles,
+                                int splits) {
+  return splits > 1 ? split_tiles * splits * tile_m * 128LL * 4 : 0;
 }
 
-cudaError_t launch_tf32x3(const Problem& p, int cfg, int splits,
-                          float* partials, const WaitCfg& wc,
+cudaError_t launch_tf32x3(const Problem& p, int cfg, int full_tiles,
+                          int splits, float* partials, const WaitCfg& wc,
                           cudaStream_t stream) {
   using namespace tf32x3;
   switch (cfg) {
     case kTc256:
-      return launch_cfg<Cfg<256, 5, false>>(p, splits, partials, wc, stream);
+      return launch_cfg<Cfg<256, 5, false>>(p, full_tiles, splits, partials,
+                                            wc, stream);
     case kTc128:
-      return launch_cfg<Cfg<128, 4, false>>(p, splits, partials, wc, stream);
+      return launch_cfg<Cfg<128, 4, false>>(p, full_tiles, splits, partials,
+                                            wc, stream);
     case kTc128Raw:
       if (p.transB)  // A·Bᵀ with B stored N×K
-        return launch_cfg<Cfg<128, 4, true, true>>(p, splits, partials, wc,
-                                                   stream);
+        return launch_cfg<Cfg<128, 4, true, true>>(p, full_tiles, splits,
+                                                   partials, wc, stream);
       if (p.storeT)  // caller passed (B, A) swapped: store the transpose
-        return launch_cfg<Cfg<128, 4, true, false, true>>(p, splits, partials,
-                                                          wc, stream);
+        return launch_cfg<Cfg<128, 4, true, false, true>>(p, full_tiles, splits,
+                                                          partials, wc, stream);
       if (p.transA)  // Aᵀ·B with A stored K×M: A transposed by the converters
         return launch_cfg<Cfg<128, 3, true, false, false, true>>(
-            p, splits, partials, wc, stream);
-      return launch_cfg<Cfg<128, 4, true>>(p, splits, partials, wc, stream);
+            p, full_tiles, splits, partials, wc, stream);
+      return launch_cfg<Cfg<128, 4, true>>(p, full_tiles, splits, partials,
+                                           wc, stream);
     case kTc256Raw:
-      return launch_cfg<Cfg<256, 5, true>>(p, splits, partials, wc, stream);
+      return launch_cfg<Cfg<256, 5, true>>(p, full_tiles, splits, partials,
+                                           wc, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -414,9 +414,23 @@ def run_gpu_ws(a, b, ws_bytes=None):
     return tc.cpu().numpy(), need
 
 
+def _slots():
+    return 2 * torch.cuda.get_device_properties(DEV).multi_processor_count
+
+
 def test_workspace_size_policy():
-    assert G.workspace_size(1024, 1024, 1024) > 0          # 64 tiles
-    assert G.workspace_size(4096, 4096, 4096) == 0         # 1024 tiles
+    """Scratch = split tiles × splits × one 128 × 128 fp32 partial tile."""
+    slots = _slots()
+    tile = 128 * 128 * 4
+    # few tiles: all split, slots // tiles ways (at least 8 k stages each)
+    assert G.workspace_size(1024, 1024, 1024) == 64 * min(slots // 64, 8) * tile
+    # a partly filled last round: its tiles split slots // tail ways
+    tail = 1024 % slots
+    s = min(slots // tail, 4096 // 16 // 8, 16)
+    assert G.workspace_size(4096, 4096, 4096) == (tail * s * tile
+                                                  if s > 1 else 0)
+    # whole rounds: nothing to split
+    assert G.workspace_size(128 * (slots // 19), 128 * 19, 4096) == 0
     assert G.workspace_size(64, 64, 64) == 0               # K too short
     assert G.workspace_size(0, 5, 5) == 0
 
@@ -443,7 +457,9 @@ def test_splitk_forced(splits, shape):
     a, b = synth.make_operands(M, N, K, seed=splits + M)
     with _env("GEMM_F32_SPLITS", splits):
         need = G.workspace_size(M, N, K)
-        assert need == min(splits, (K + 15) // 16) * M * N * 4 or need == 0
+        s = min(splits, (K + 15) // 16, 16)
+        tiles = ((M + 127) // 128) * ((N + 127) // 128)
+        assert need == (tiles * s * 128 * 128 * 4 if s > 1 else 0)
         c, _ = run_gpu_ws(a, b)
         check_full(a, b, c, what=f"split {splits} {shape}")
         ai, bi = synth.make_operands(M, N, K, seed=splits, dist_a="int",
@@ -457,6 +473,54 @@ def test_splitk_small_workspace_falls_back():
     need = G.workspace_size(1024, 1024, 1024)
     c, _ = run_gpu_ws(a, b, ws_bytes=need - 4)
     check_full(a, b, c, what="too-small workspace")
+
+
+# a last round of tiles split over the GPU: 17 x 19 = 323 tiles on 304
+# CTA slots leave a 19-tile tail (the bottom tile-row, ragged in M and N
+# for the second shape; K ragged too)
+TAIL_SHAPES = [(17 * 128, 19 * 128, 512), (2100, 2420, 1000)]
+
+
+@pytest.mark.parametrize("shape", TAIL_SHAPES,
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tail_split_shapes(shape):
+    M, N, K = shape
+    if ((M + 127) // 128) * ((N + 127) // 128) <= _slots():
+        pytest.skip("this GPU fills the tiles in one round")
+    a, b = synth.make_operands(M, N, K, seed=M + K)
+    c, need = run_gpu_ws(a, b)
+    assert need > 0
+    check_full(a, b, c, what=f"tail split {shape}")
+    ai, bi = synth.make_operands(M, N, K, seed=N, dist_a="int", dist_b="int")
+    ci, _ = run_gpu_ws(ai, bi)
+    check_full(ai, bi, ci, exact=True, what=f"tail split {shape} int")
+    c2, _ = run_gpu_ws(a, b)
+    assert np.array_equal(c.view(np.uint32), c2.view(np.uint32))
+    assert G.device_status() == 0
+
+
+def test_tail_split_mlp_sampled():
+    """8192 x 3072 x 768: 1536 tiles, the last 16 split over the GPU."""
+    w = synth.WORKLOADS["mlp"]
+    a, b = w.operands()
+    c, need = run_gpu_ws(a, b)
+    assert need > 0
+    check_sampled_and_rowsums(a, b, c, what="mlp tail split")
+
+
+def test_tail_split_fused_epilogue():
+    M, N, K = 2100, 2420, 1000
+    a, b = synth.make_operands(M, N, K, seed=77, dist_a="normal",
+                               dist_b="normal")
+    bias = synth.make_operands(1, N, 1, seed=78)[1][0]
+    need = G.workspace_size(M, N, K)
+    ws = torch.empty(max(need // 4, 1), device=DEV)
+    c = G.gemm_f32_bias_act(torch.from_numpy(a).to(DEV),
+                            torch.from_numpy(b).to(DEV),
+                            torch.from_numpy(bias).to(DEV), G.ACT_GELU,
+                            workspace=ws)
+    torch.cuda.synchronize()
+    _check_epilogue(a, b, bias, G.ACT_GELU, c.cpu().numpy(), "tail gelu")
 
 
 def test_splitk_deterministic():
