@@ -616,9 +616,25 @@ int gemm_f32_mixed16(int type, int64_t M, int64_t N, int64_t K,
   wc.limit = g_wait_ns.load();
   wc.debug = g_debug_flags.load();
   wc.status = d->status;
-  e = gemm_f32_impl::launch_mixed16(p, d->sm_count,
-                                    aligned16(C) && ldc % 4 == 0, wc, s);
+  const gemm_f32_impl::Plan16 plan = gemm_f32_impl::plan_mixed16(
+      M, N, d->sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0);
+  e = gemm_f32_impl::launch_mixed16(p, plan, aligned16(C) && ldc % 4 == 0,
+                                    wc, s);
   return e == cudaSuccess ? GEMM_F32_OK : fail_cuda(e);
+}
+
+int gemm_f32_mixed_plan(int64_t M, int64_t N, int64_t out[4]) {
+  if (M < 1 || N < 1 || !out) return GEMM_F32_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const gemm_f32_impl::Plan16 plan = gemm_f32_impl::plan_mixed16(
+      M, N, d->sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0);
+  out[0] = plan.wn;
+  out[1] = plan.full;
+  out[2] = plan.parts;
+  out[3] = plan.grid;
+  return GEMM_F32_OK;
 }
 
 int gemm_f32_mixed(int type, int64_t M, int64_t N, int64_t K, const float* A,

@@ -105,9 +105,29 @@ struct Problem16 {
   long long ldc;
 };
 
-// tcgen05 kind::f16 kernel, persistent over min(tiles, sm_count) CTAs.
+// How the 16-bit kernel cuts C into work units, one per CTA at a time:
+// tiles of 128 rows by `wn` columns (256, or 128 / 64 when N is that
+// narrow, so no MMA computes columns that all lie past N), walked in the
+// grouped order; the first `full` tiles whole, in whole rounds of the
+// grid, and each tile of the last, partly filled round (every tile, when
+// there are fewer tiles than SMs) cut into `parts` strips of wn / parts
+// columns, so that the last round spreads over the GPU instead of leaving
+// most SMs idle while one tile per busy SM runs its whole length.
+struct Plan16 {
+  int wn;
+  long long tiles_m, tiles_n;
+  long long full;  // whole tiles; the rest are split
+  int parts;       // strips per split tile: 1, 2 or 4
+  long long units;
+  int grid;        // persistent CTAs: min(units, sm_count)
+};
+
+// narrow = false keeps every tile whole and 256 wide.
+Plan16 plan_mixed16(long long M, long long N, int sm_count, bool narrow);
+
+// tcgen05 kind::f16 kernel, persistent over plan.grid CTAs.
 // Needs A, B 16-byte aligned, lda and ldb multiples of 8, K >= 1.
-cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
+cudaError_t launch_mixed16(const Problem16& p, const Plan16& plan, bool c_vec,
                            const WaitCfg& wc, cudaStream_t stream);
 
 // dst = round16(src) (type gemm_f32_mixed_type) for a rows×cols block.

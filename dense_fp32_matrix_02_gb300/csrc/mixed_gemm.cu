@@ -3,20 +3,23 @@
 // and fp32 accumulation: the arithmetic of "Rendre le GPU rapide", "Les
 // Tensor Cores" (only the operands are 16-bit; sums and tensors stay fp32).
 //
-// One persistent CTA per SM walks the 128×256 output tiles (a grid-stride
-// walk over a grouped tile order, so CTAs running at the same time share A
-// row-panels and B column-panels in L2):
+// One persistent CTA per SM walks the work units: 128-row output tiles
+// 256 columns wide (128 or 64 when N is that narrow), and, in the last,
+// partly filled round, strips of 128 or 64 columns cut from its tiles
+// (Plan16).  The walk is grid-stride over a grouped tile order, so CTAs
+// running at the same time share A row-panels and B column-panels in L2:
 //   warp 0      TMA producer.  Per k-block of 64: the A tile (128 rows of
-//               64 k, K-major, 128-byte swizzle) and the B tile (64 k rows
-//               of 256 n, N-major, as four 64×64 boxes, 128-byte swizzle)
-//               into a 4-stage ring.
-//   warp 1      MMA issuer.  Four tcgen05.mma kind::f16 (M 128, N 256,
-//               K 16) per stage into one of two TMEM accumulators of 256
-//               columns; tcgen05.commit releases the stage and, after the
-//               last k-block, publishes the accumulator.
+//               64 k, K-major, 128-byte swizzle) and the unit's B columns
+//               (64 k rows of up to 256 n, N-major, as 64×64 boxes,
+//               128-byte swizzle) into a 4-stage ring.
+//   warp 1      MMA issuer.  Four tcgen05.mma kind::f16 (M 128, N = the
+//               unit's width, K 16) per stage into one of two TMEM
+//               accumulators of 256 columns; tcgen05.commit releases the
+//               stage and, after the last k-block, publishes the
+//               accumulator.
 //   warps 2-9   Epilogue.  tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32·(w mod 4) + 0..31, i.e. those rows of the tile, and
-//               one half of its columns, 32 columns at a time).  Each 32×32
+//               one half of the unit's columns, 32 columns at a time).  Each 32×32
 //               block goes through a 4 KB shared-memory staging buffer of the
 //               warp (128-byte swizzle) and out by a TMA bulk tensor store,
 //               which writes whole 128-byte row segments and skips what lies
@@ -80,6 +83,25 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
   return bounded_wait(bar, parity, limit_ns, abort, sleep ? kSleepNs : 0u);
 }
 
+// Work unit u of a Plan16: tile row tm, first column n0, width columns.
+struct Unit {
+  int tm, n0, width;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, int tiles_m, int tiles_n,
+                                        int wn, int full, int parts) {
+  int t = u, part = 0, width = wn;
+  if (u >= full) {
+    const int v = u - full;
+    t = full + v / parts;
+    part = v - (v / parts) * parts;
+    width = wn / parts;
+  }
+  int tm, tn;
+  tile_coords<8>(t, tiles_m, tiles_n, tm, tn);
+  return Unit{tm, tn * wn + part * width, width};
+}
+
 // ab_type: 0 binary16, 1 bfloat16 (the kind::f16 operand format code).
 template <int AB_TYPE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -87,10 +109,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, float* C,
                    long long ldc, int M, int N, int K, int tiles_m,
-                   int tiles_n, int c_mode, WaitCfg wc) {
+                   int tiles_n, int wn, int whole, int parts, int units,
+                   int c_mode, WaitCfg wc) {
   // c_mode: 2 = TMA stores through staging, 1 = direct 16-byte stores,
   // 0 = direct scalar stores
-  constexpr uint32_t kIdesc = idesc_f16(kBM, kBN, AB_TYPE, true);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -105,7 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (K + kBK - 1) / kBK;  // >= 1 (host)
-  const int total = tiles_m * tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -139,9 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;  // k-blocks issued, over all tiles of this CTA
       if (!(wc.debug & kDebugStallProducer)) {
-        for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
-          int tm, tn;
-          tile_coords<8>(t, tiles_m, tiles_n, tm, tn);
+        for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+          const Unit w = unit_of(u, tiles_m, tiles_n, wn, whole, parts);
+          const int boxes = w.width / 64;
           for (int kb = 0; kb < nk; ++kb) {
             const int s = it % kStages;
             if (it >= kStages &&
@@ -151,14 +172,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               record_status(wc.status, kStatusTimeoutEmpty);
               break;
             }
-            mbar_arrive_expect_tx(full(s), kStageBytesA + kStageBytesB);
+            mbar_arrive_expect_tx(full(s),
+                                  kStageBytesA + boxes * kBoxBytesB);
             tma_load_2d(sbase + s * kStageBytesA, &tmap_a, full(s), kb * kBK,
-                        tm * kBM);
+                        w.tm * kBM);
             const uint32_t bdst = sbase + kOffB + s * kStageBytesB;
-#pragma unroll
-            for (int c = 0; c < kBN / 64; ++c)
+            for (int c = 0; c < boxes; ++c)
               tma_load_2d(bdst + c * kBoxBytesB, &tmap_b, full(s),
-                          tn * kBN + 64 * c, kb * kBK);
+                          w.n0 + 64 * c, kb * kBK);
             ++it;
           }
         }
@@ -175,8 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x, i = 0; ok && t < total; t += gridDim.x, ++i) {
+      for (int u = blockIdx.x, i = 0; ok && u < units; u += gridDim.x, ++i) {
         const int b = i & 1;
+        const uint32_t idesc = idesc_f16(
+            kBM, unit_of(u, tiles_m, tiles_n, wn, whole, parts).width,
+            AB_TYPE, true);
         if (i >= 2 && !wait_phase(acc_empty(b), ((i >> 1) - 1) & 1, wc.limit,
                                   abort, false)) {
           *abort = 1;
@@ -203,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ad = smem_desc_sw128(a0 + 32 * kk, 16, 1024);
             const uint64_t bd =
                 smem_desc_sw128(b0 + 2048 * kk, kBoxBytesB, 1024);
-            mma_f16_ss(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+            mma_f16_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0);
           }
           tc_commit(empty(s));
         }
@@ -223,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // at slot j ^ (r mod 8), the layout a 128-byte-swizzle TMA store reads
     unsigned char* stg = smem + kOffStaging + (warp - 2) * kStagingBytes;
     const uint32_t stg_s = sbase + kOffStaging + (warp - 2) * kStagingBytes;
-    for (int t = blockIdx.x, i = 0; t < total; t += gridDim.x, ++i) {
+    for (int u = blockIdx.x, i = 0; u < units; u += gridDim.x, ++i) {
       const int b = i & 1;
       const bool ok =
           wait_phase(acc_full(b), (i >> 1) & 1, wc.limit, abort, true);
@@ -233,19 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      int tm, tn;
-      tile_coords<8>(t, tiles_m, tiles_n, tm, tn);
-      const int m0 = tm * kBM + q * 32;
+      const Unit w = unit_of(u, tiles_m, tiles_n, wn, whole, parts);
+      const int half = w.width / 2;  // 32, 64 or 128 columns per warp
+      const int m0 = w.tm * kBM + q * 32;
       const int m = m0 + lane;
-      const int n0 = tn * kBN + h * (kAccCols / 2);
+      const int n0 = w.n0 + h * half;
       float* crow = C + (long long)m * ldc;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kAccCols / 2; c0 += 32) {
+      for (int c0 = 0; c0 < half; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_bits + b * kAccCols + h * (kAccCols / 2) + c0,
-                  v);
+        tmem_ld32(tmem + lane_bits + b * kAccCols + h * half + c0, v);
         tmem_ld_wait();
-        if (c0 + 32 == kAccCols / 2) {
+        if (c0 + 32 == half) {
           // all of this warp's part of the accumulator is in registers
           tc_fence_before_sync();
           __syncwarp();
@@ -372,7 +395,33 @@ bool encode_16(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
 
 }  // namespace mixed16
 
-cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
+Plan16 plan_mixed16(long long M, long long N, int sm_count, bool narrow) {
+  Plan16 p;
+  p.wn = (!narrow || N > 128) ? 256 : (N > 64 ? 128 : 64);
+  p.tiles_m = (M + 127) / 128;
+  p.tiles_n = (N + p.wn - 1) / p.wn;
+  const long long total = p.tiles_m * p.tiles_n;
+  const long long g = sm_count > 0 ? sm_count : 1;
+  p.full = total;
+  p.parts = 1;
+  if (narrow) {
+    // the tiles of the last, partly filled round: all of them when there
+    // are fewer tiles than SMs
+    const long long tail = total % g;
+    int parts = 1;
+    while (tail > 0 && parts * 2 <= p.wn / 64 && tail * parts * 2 <= g)
+      parts *= 2;
+    if (parts > 1) {
+      p.full = total - tail;
+      p.parts = parts;
+    }
+  }
+  p.units = p.full + (total - p.full) * p.parts;
+  p.grid = (int)(p.units < g ? p.units : g);
+  return p;
+}
+
+cudaError_t launch_mixed16(const Problem16& p, const Plan16& plan, bool c_vec,
                            const WaitCfg& wc, cudaStream_t stream) {
   using namespace mixed16;
   auto encode = tensor_map_encoder();
@@ -401,14 +450,17 @@ cudaError_t launch_mixed16(const Problem16& p, int sm_count, bool c_vec,
   cudaError_t e =
       ensure_smem_attr(reinterpret_cast<const void*>(fn), kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long tiles_m = (p.M + kBM - 1) / kBM;
-  const long long tiles_n = (p.N + kBN - 1) / kBN;
-  const long long total = tiles_m * tiles_n;
-  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int grid = (int)(total < sm_count ? total : sm_count);
-  fn<<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, tc, p.C, p.ldc, p.M,
-                                              p.N, p.K, (int)tiles_m,
-                                              (int)tiles_n, c_mode, wc);
+  if (plan.units > 0x7fffffffLL || plan.units < 1 || plan.grid < 1 ||
+      (plan.wn != 64 && plan.wn != 128 && plan.wn != 256) ||
+      (plan.parts != 1 && plan.parts != 2 && plan.parts != 4) ||
+      plan.wn / plan.parts < 64 ||
+      plan.tiles_m != (p.M + kBM - 1) / kBM ||
+      plan.tiles_n != (p.N + plan.wn - 1) / plan.wn)
+    return cudaErrorInvalidConfiguration;
+  fn<<<plan.grid, kThreads, kSmemBytes, stream>>>(
+      ta, tb, tc, p.C, p.ldc, p.M, p.N, p.K, (int)plan.tiles_m,
+      (int)plan.tiles_n, plan.wn, (int)plan.full, plan.parts,
+      (int)plan.units, c_mode, wc);
   return cudaGetLastError();
 }
 

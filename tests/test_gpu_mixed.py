@@ -188,6 +188,69 @@ def test_mixed16_large_sampled(t):
     assert_within_tolerance(c[rows, cols], want, bound, K, what="sampled")
 
 
+# ------------------------------------------------------------- work units
+def _sms():
+    return torch.cuda.get_device_properties(DEV).multi_processor_count
+
+
+def _split_cases():
+    """Shapes that reach each way the 16-bit kernel cuts C, for this GPU's
+    SM count g: (M, N, K, expected plan)."""
+    g = _sms()
+    half_tail = g // 2 - 3        # 2 strips fit, 4 do not
+    return [
+        # one round and a tail of g/2 - 3 tiles: 128-column strips
+        ((g + half_tail) * 128 - 5, 256, 72,
+         dict(width=256, whole=g, parts=2)),
+        # one round and a tail of 8 tiles: 64-column strips
+        ((g + 8) * 128 - 77, 256, 40, dict(width=256, whole=g, parts=4)),
+        # fewer tiles than SMs: every tile cut in four
+        (300, 520, 136, dict(width=256, whole=0, parts=4)),
+        # N <= 128: 128-wide tiles, cut in two
+        (1000, 100, 200, dict(width=128, whole=0, parts=2)),
+        # N <= 64: 64-wide tiles, never cut
+        (g * 128 + 1, 40, 64, dict(width=64, whole=g + 1, parts=1)),
+        # N = 257: a second column of tiles holding one column of C
+        (640, 257, 96, dict(width=256, whole=0, parts=4)),
+        # whole rounds only: nothing to cut
+        (2 * g * 128, 256, 64, dict(width=256, whole=2 * g, parts=1)),
+    ]
+
+
+def test_mixed_plan_cases():
+    for M, N, _, want in _split_cases():
+        got = G.mixed_plan(M, N)
+        assert {k: got[k] for k in want} == want, (M, N, got)
+        assert 1 <= got["grid"] <= _sms()
+
+
+@pytest.mark.parametrize("t", TYPES, ids=TYPE_IDS)
+@pytest.mark.parametrize("case", range(7))
+def test_mixed16_work_units_exact(t, case):
+    """Every cut (strips of the last round, narrow tiles, a ragged last
+    column of tiles) covers C exactly once: bit for bit on integers."""
+    M, N, K, plan = _split_cases()[case]
+    a, b = synth.make_operands(M, N, K, seed=100 + case, dist_a="int8")
+    want, _, _ = oracle.gemm_mixed(a, b, t)
+    assert_bitexact(run_mixed16(a, b, t), want, what=f"mixed16 {plan}")
+
+
+@pytest.mark.parametrize("case", [0, 1, 3])
+def test_mixed16_work_units_normal(case, monkeypatch):
+    """Normal operands through the cut and the uncut plan
+    (GEMM_F32_MIXED_NARROW=0): both within the tolerance."""
+    M, N, K, _ = _split_cases()[case]
+    a, b = synth.make_operands(M, N, K, seed=200 + case, dist_a="normal")
+    want, bound, _ = oracle.gemm_mixed(a, b, G.MIXED_BF16)
+    cut = run_mixed16(a, b, G.MIXED_BF16)
+    monkeypatch.setenv("GEMM_F32_MIXED_NARROW", "0")
+    assert G.mixed_plan(M, N)["parts"] == 1
+    assert G.mixed_plan(M, N)["width"] == 256
+    whole = run_mixed16(a, b, G.MIXED_BF16)
+    assert_within_tolerance(cut, want, bound, K, what="cut")
+    assert_within_tolerance(whole, want, bound, K, what="whole")
+
+
 # ------------------------------------------------------------- edges, errors
 def test_mixed_k_zero_and_empty():
     c = torch.full((5, 7), float("nan"), device=DEV)
