@@ -47,7 +47,7 @@ def parse_args():
     p.add_argument("--workload", default="sq4096")
     p.add_argument("--algo", default="auto", choices=list(ALGOS))
     p.add_argument("--op", default="nn", choices=["nn", "nt", "tn", "tt"],
-                   help="operand forms (gemm_f32_batched); nn = plain")
+                   help="operand forms (gemm_f32_batched_ws); nn = plain")
     p.add_argument("--batch", type=int, default=1,
                    help="independent products per step (gemm_f32_batched)")
     p.add_argument("--epilogue", default="none",
@@ -448,7 +448,16 @@ def run_ours(args, w, config):
         for _ in range(nsets - 1):
             bsets.append((bA.clone(), bB.clone(),
                           torch.empty(args.batch, w.M, w.N, device=dev)))
+        # scratch gemm_f32_batched_ws asks for: the transposed copy of A
+        # for Aᵀ·B (one more launch), split-K scratch for a single product
+        bws_bytes = G.batched_workspace_size(int(ta_), int(tb_), w.M, w.N,
+                                             w.K, args.batch)
+        bws = torch.empty(max(bws_bytes, 1), dtype=torch.uint8, device=dev)
         launches_per_step = 1
+        if ta_ and not tb_:
+            launches_per_step += 1
+        if args.batch == 1 and not tb_ and G.workspace_size(w.M, w.N, w.K):
+            launches_per_step += 1
 
     if batched:  # aligned operands: the tensor kernel takes every form
         ran = 3
@@ -474,7 +483,7 @@ def run_ours(args, w, config):
         if batched:
             xa, xb, xc = bsets[i % nsets]
             G.gemm_f32_batched(xa, xb, xc, trans_a=ta_, trans_b=tb_,
-                               stream=s_obj)
+                               stream=s_obj, workspace=bws)
             return
         ta, tb, tc = sets[i % nsets]
         if algo == 0:
@@ -515,7 +524,7 @@ def run_ours(args, w, config):
             xa.copy_(hba, non_blocking=True)
             xb.copy_(hbb, non_blocking=True)
             G.gemm_f32_batched(xa, xb, xc, trans_a=ta_, trans_b=tb_,
-                               stream=stream)
+                               stream=stream, workspace=bws)
             hbc.copy_(xc, non_blocking=True)
             return
         if algo == 0:

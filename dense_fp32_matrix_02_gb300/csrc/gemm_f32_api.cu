@@ -343,10 +343,21 @@ namespace {
 
 bool mult4(int64_t x) { return x % 4 == 0; }
 
+// Bytes of one transposed copy of a K×M stored A (op(A) = Aᵀ written M×K,
+// rows of K rounded up to a multiple of 4), rounded up to 256 bytes.
+int64_t transposed_copy_bytes(int64_t M, int64_t K) {
+  return (M * ((K + 3) / 4 * 4) * 4 + 255) / 256 * 256;
+}
+
+// `ws`/`ws_bytes`: optional scratch.  With opA = T, opB = N on the tensor
+// path and room for the transposed copies, A is transposed into it first
+// and the product runs as opA = N (for batch = 1 through run_gemm, whose
+// split-K scratch is the rest of ws).
 int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
                 const float* A, int64_t lda, int64_t sA, const float* B,
                 int64_t ldb, int64_t sB, float* C, int64_t ldc, int64_t sC,
-                int64_t batch, gemm_f32_stream_t stream) {
+                int64_t batch, gemm_f32_stream_t stream, void* ws,
+                int64_t ws_bytes) {
   if ((opA != GEMM_F32_OP_N && opA != GEMM_F32_OP_T) ||
       (opB != GEMM_F32_OP_N && opB != GEMM_F32_OP_T))
     return GEMM_F32_ERR_INVALID_ARG;
@@ -355,13 +366,14 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
   if (lda < (ta ? M : K) || ldb < (tb ? K : N) || ldc < N)
     return GEMM_F32_ERR_INVALID_ARG;
   if (sA < 0 || sB < 0 || sC < 0) return GEMM_F32_ERR_INVALID_ARG;
+  if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return GEMM_F32_ERR_INVALID_ARG;
   if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff || batch > 65535)
     return GEMM_F32_ERR_UNSUPPORTED;
   if (M == 0 || N == 0 || batch == 0) return GEMM_F32_OK;
   if (!C || (K > 0 && (!A || !B))) return GEMM_F32_ERR_INVALID_ARG;
   if (!ta && !tb && batch == 1)  // the plain product
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, stream,
-                    GEMM_F32_ALGO_AUTO, nullptr, 0);
+                    GEMM_F32_ALGO_AUTO, ws, ws_bytes);
   const DeviceInfo* d = nullptr;
   cudaError_t e = device_info(&d);
   if (e != cudaSuccess) return fail_cuda(e);
@@ -408,6 +420,24 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
       q.transB = 0;
       q.storeT = 1;
     }
+    // Aᵀ·B: a transposed copy of A, then the plain form, when ws has room
+    const int64_t copies = (batch == 1 || sA == 0) ? 1 : batch;
+    const int64_t one = transposed_copy_bytes(M, K);
+    if (ta && !tb && aligned16(ws) && ws_bytes / copies >= one) {
+      const int64_t ldt = (K + 3) / 4 * 4;
+      float* at = static_cast<float*>(ws);
+      e = launch_transpose(A, lda, sA, at, ldt, one / 4, K, M, copies,
+                           d->sm_count, s);
+      if (e != cudaSuccess) return fail_cuda(e);
+      if (batch == 1)
+        return run_gemm(M, N, K, at, ldt, B, ldb, C, ldc, stream,
+                        GEMM_F32_ALGO_AUTO, static_cast<char*>(ws) + one,
+                        ws_bytes - one);
+      q.A = at;
+      q.lda = ldt;
+      q.sA = copies == 1 ? 0 : one / 4;
+      q.transA = 0;
+    }
     WaitCfg wc;
     wc.limit = g_wait_ns.load();
     wc.debug = g_debug_flags.load();
@@ -439,7 +469,36 @@ int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
                      int64_t ldc, int64_t strideC, int64_t batch,
                      gemm_f32_stream_t stream) {
   return run_batched(opA, opB, M, N, K, A, lda, strideA, B, ldb, strideB, C,
-                     ldc, strideC, batch, stream);
+                     ldc, strideC, batch, stream, nullptr, 0);
+}
+
+int gemm_f32_batched_ws(int opA, int opB, int64_t M, int64_t N, int64_t K,
+                        const float* A, int64_t lda, int64_t strideA,
+                        const float* B, int64_t ldb, int64_t strideB,
+                        float* C, int64_t ldc, int64_t strideC,
+                        int64_t batch, void* workspace,
+                        int64_t workspace_bytes, gemm_f32_stream_t stream) {
+  return run_batched(opA, opB, M, N, K, A, lda, strideA, B, ldb, strideB, C,
+                     ldc, strideC, batch, stream, workspace, workspace_bytes);
+}
+
+int64_t gemm_f32_batched_workspace_size(int opA, int opB, int64_t M,
+                                        int64_t N, int64_t K,
+                                        int64_t batch) {
+  if ((opA != GEMM_F32_OP_N && opA != GEMM_F32_OP_T) ||
+      (opB != GEMM_F32_OP_N && opB != GEMM_F32_OP_T) || M < 0 || N < 0 ||
+      K < 0 || batch < 0)
+    return -GEMM_F32_ERR_INVALID_ARG;
+  if (M == 0 || N == 0 || K == 0 || batch == 0) return 0;
+  int64_t bytes = 0;
+  if (opA == GEMM_F32_OP_T && opB == GEMM_F32_OP_N)
+    bytes = transposed_copy_bytes(M, K) * batch;
+  if (batch == 1 && opB == GEMM_F32_OP_N) {
+    const int64_t split = gemm_f32_workspace_size(M, N, K);
+    if (split < 0) return split;
+    bytes += split;
+  }
+  return bytes;
 }
 
 int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,

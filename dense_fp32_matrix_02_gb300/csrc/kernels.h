@@ -135,6 +135,13 @@ cudaError_t launch_round16(int type, long long rows, long long cols,
                            const float* src, long long lds, uint16_t* dst,
                            long long ldd, int sm_count, cudaStream_t stream);
 
+// dst_b = src_bᵀ for b < batch: src_b = src + b·ss is rows×cols (row
+// stride lds), dst_b = dst + b·sd is cols×rows (row stride ldd).
+cudaError_t launch_transpose(const float* src, long long lds, long long ss,
+                             float* dst, long long ldd, long long sd,
+                             long long rows, long long cols, long long batch,
+                             int sm_count, cudaStream_t stream);
+
 // C[0:M, 0:N] = 0.
 cudaError_t launch_fill_zero(float* C, long long ldc, long long M, long long N,
                              int sm_count, cudaStream_t stream);

@@ -59,6 +59,13 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_batched.restype = ci
         L.gemm_f32_batched.argtypes = [ci, ci, i64, i64, i64, vp, i64, i64,
                                        vp, i64, i64, vp, i64, i64, i64, vp]
+        L.gemm_f32_batched_ws.restype = ci
+        L.gemm_f32_batched_ws.argtypes = [ci, ci, i64, i64, i64, vp, i64,
+                                          i64, vp, i64, i64, vp, i64, i64,
+                                          i64, vp, i64, vp]
+        L.gemm_f32_batched_workspace_size.restype = i64
+        L.gemm_f32_batched_workspace_size.argtypes = [ci, ci, i64, i64, i64,
+                                                      i64]
         L.gemm_f32_host.restype = ci
         L.gemm_f32_host.argtypes = args[:-1] + [vp, vp, vp, vp, i64, vp]
         L.gemm_f32_noalloc.restype = ci
@@ -205,12 +212,60 @@ def gemm_f32_batched_ptr(opA, opB, M, N, K, a_ptr, lda, sA, b_ptr, ldb, sB,
     _check(st, "gemm_f32_batched")
 
 
+def gemm_f32_batched_ws_ptr(opA, opB, M, N, K, a_ptr, lda, sA, b_ptr, ldb,
+                            sB, c_ptr, ldc, sC, batch, ws_ptr, ws_bytes,
+                            stream=0):
+    """Raw-pointer gemm_f32_batched_ws call (optional scratch)."""
+    st = lib().gemm_f32_batched_ws(int(opA), int(opB), int(M), int(N),
+                                   int(K), a_ptr or None, int(lda), int(sA),
+                                   b_ptr or None, int(ldb), int(sB),
+                                   c_ptr or None, int(ldc), int(sC),
+                                   int(batch), ws_ptr or None, int(ws_bytes),
+                                   stream or None)
+    _check(st, "gemm_f32_batched_ws")
+
+
+def batched_workspace_size(opA, opB, M, N, K, batch=1) -> int:
+    """Scratch bytes gemm_f32_batched_ws uses at most."""
+    n = int(lib().gemm_f32_batched_workspace_size(int(opA), int(opB), int(M),
+                                                  int(N), int(K), int(batch)))
+    if n < 0:
+        _check(-n, "gemm_f32_batched_workspace_size")
+    return n
+
+
+def _scratch(nbytes, device, stream):
+    """A device byte buffer for one call on `stream` (a torch stream, a raw
+    handle or None = current).  The caching allocator is told when the
+    stream is not the current one, so that the buffer is not handed out
+    again while that stream may still use it."""
+    import torch
+    buf = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+    if stream is None:
+        return buf
+    current = torch.cuda.current_stream(device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") \
+        else int(stream)
+    if handle == current.cuda_stream:
+        return buf
+    if isinstance(stream, torch.cuda.Stream):
+        buf.record_stream(stream)
+    elif handle == 0:
+        buf.record_stream(torch.cuda.default_stream(device))
+    else:
+        buf.record_stream(torch.cuda.ExternalStream(handle, device=device))
+    return buf
+
+
 def gemm_f32_batched(a, b, c=None, trans_a=False, trans_b=False,
-                     stream=None):
+                     stream=None, workspace=None):
     """C[i] = op(A[i]) · op(B[i]) for 3-D CUDA tensors (batch, rows, cols).
 
     op(X) is X or, with trans_*, X transposed (read in place, no copy).  A
-    2-D operand is used for every product (stride 0).
+    2-D operand is used for every product (stride 0).  For op(A) = Aᵀ with
+    op(B) = B the call goes through gemm_f32_batched_ws with `workspace`
+    (a CUDA tensor; allocated here when None) holding a transposed copy of
+    A; other forms use `workspace` only when given.
     """
     import torch
 
@@ -246,15 +301,35 @@ def gemm_f32_batched(a, b, c=None, trans_a=False, trans_b=False,
         raise ValueError("c has the wrong shape")
     if batch > 1 and sC == 0:
         raise ValueError("c must hold one matrix per product")
-    if stream is None:
-        stream = torch.cuda.current_stream(a.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
-    with torch.cuda.device(a.device):
-        gemm_f32_batched_ptr(OP_T if trans_a else OP_N,
-                             OP_T if trans_b else OP_N, M, N, K,
-                             a3.data_ptr(), lda, sA, b3.data_ptr(), ldb, sB,
-                             c3.data_ptr(), ldc, sC, batch, handle)
+    opa, opb = (OP_T if trans_a else OP_N), (OP_T if trans_b else OP_N)
+    _batched_call(opa, opb, M, N, K, a3.data_ptr(), lda, sA, b3.data_ptr(),
+                  ldb, sB, c3.data_ptr(), ldc, sC, batch, a.device, stream,
+                  workspace)
     return c
+
+
+def _batched_call(opa, opb, M, N, K, ap, lda, sA, bp, ldb, sB, cp, ldc, sC,
+                  batch, device, stream, workspace):
+    """gemm_f32_batched_ws with the given scratch, or with scratch allocated
+    for the Aᵀ·B form, else gemm_f32_batched."""
+    import torch
+    with torch.cuda.device(device):
+        handle = _handle(stream, device)
+        if workspace is None and opa == OP_T and opb == OP_N:
+            need = batched_workspace_size(opa, opb, M, N, K, batch)
+            if need > 0:
+                workspace = _scratch(need, device, stream)
+        if workspace is None:
+            gemm_f32_batched_ptr(opa, opb, M, N, K, ap, lda, sA, bp, ldb, sB,
+                                 cp, ldc, sC, batch, handle)
+            return
+        if not workspace.is_cuda:
+            raise ValueError("workspace must live on a CUDA device")
+        nbytes = workspace.numel() * workspace.element_size()
+        gemm_f32_batched_ws_ptr(opa, opb, M, N, K, ap, lda, sA, bp, ldb, sB,
+                                cp, ldc, sC, batch,
+                                workspace.data_ptr() if nbytes else 0, nbytes,
+                                handle)
 
 
 def gemm_f32_host(a, b, c, da, db, dc, workspace=None, stream=None):
@@ -544,8 +619,7 @@ def gemm_f32_mixed(a, b, half=MIXED_BF16, c=None, workspace=None,
         raise ValueError("c has the wrong shape")
     need = mixed_workspace_size(M, N, K)
     if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8,
-                                device=a.device)
+        workspace = _scratch(need, a.device, stream)
     ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(a.device):
         gemm_f32_mixed_ptr(t, M, N, K, ap, lda, bp, ldb, cp, ldc,
@@ -603,8 +677,10 @@ def matmul(a, b, out=None, stream=None):
     """The product a·b for float32 CUDA tensors, 2-D or batched 3-D (a 2-D
     operand is shared by every product), where each operand may be
     row-major or a transposed view of row-major storage (e.g. ``w.t()``):
-    the library reads it in place through gemm_f32_batched, without a copy.
-    Returns C (row-major, allocated if ``out`` is None)."""
+    the library reads it in place through gemm_f32_batched (for a
+    transposed ``a`` with a row-major ``b``, gemm_f32_batched_ws with a
+    transposed copy of ``a`` in scratch allocated here).  Returns C
+    (row-major, allocated if ``out`` is None)."""
     import torch
     opa, M, K, lda, ba, sa = _operand_form(a, "a")
     opb, K2, N, ldb, bb, sb = _operand_form(b, "b")
@@ -624,8 +700,7 @@ def matmul(a, b, out=None, stream=None):
         raise ValueError("out must be row-major")
     if batch > 1 and sc == 0:
         raise ValueError("out must hold one matrix per product")
-    with torch.cuda.device(a.device):
-        gemm_f32_batched_ptr(opa, opb, M, N, K, a.data_ptr(), lda, sa,
-                             b.data_ptr(), ldb, sb, out.data_ptr(), ldc, sc,
-                             batch, _handle(stream, a.device))
+    _batched_call(opa, opb, M, N, K, a.data_ptr(), lda, sa, b.data_ptr(),
+                  ldb, sb, out.data_ptr(), ldc, sc, batch, a.device, stream,
+                  None)
     return out

@@ -152,6 +152,36 @@ GEMM_F32_API int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N,
                                   int64_t strideC, int64_t batch,
                                   gemm_f32_stream_t stream);
 
+/*
+ * As gemm_f32_batched, with caller-lent scratch (`workspace`: 16-byte
+ * aligned device memory, or NULL with 0 bytes).  For the form
+ * opA = T, opB = N on the tensor kernel, when the workspace holds the
+ * transposed copies (M rows of K rounded up to a multiple of 4, one copy
+ * per product, or one for all when strideA = 0 or batch = 1, each on a
+ * 256-byte boundary), A is first transposed into it by an HBM-bound copy
+ * kernel and the product runs as opA = N: this costs one pass over A and
+ * saves the tensor kernel the transposition of every A tile in shared
+ * memory.  For batch = 1 the rest of the workspace is split-K scratch as
+ * in gemm_f32_ws (also for opA = opB = N).  With less scratch, and for the
+ * other forms, the call runs as gemm_f32_batched.  The workspace is in use
+ * until the stream passes this call.
+ */
+GEMM_F32_API int gemm_f32_batched_ws(int opA, int opB, int64_t M, int64_t N,
+                                     int64_t K, const float *A, int64_t lda,
+                                     int64_t strideA, const float *B,
+                                     int64_t ldb, int64_t strideB, float *C,
+                                     int64_t ldc, int64_t strideC,
+                                     int64_t batch, void *workspace,
+                                     int64_t workspace_bytes,
+                                     gemm_f32_stream_t stream);
+
+/* Scratch bytes gemm_f32_batched_ws uses at most for these sizes and forms
+ * on the current device (0: none; negative: minus a status). */
+GEMM_F32_API int64_t gemm_f32_batched_workspace_size(int opA, int opB,
+                                                     int64_t M, int64_t N,
+                                                     int64_t K,
+                                                     int64_t batch);
+
 /* 16-bit operand formats of the mixed-precision products. */
 typedef enum {
     GEMM_F32_MIXED_BF16 = 0, /* bfloat16: the upper half of a float32 */

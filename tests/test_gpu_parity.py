@@ -613,15 +613,18 @@ def test_tma_ffma_timeout_path_reports_and_recovers():
 
 # ------------------------------------------------------------- batched, op
 def _batched_case(form, M, N, K, batch, seed, gap=0, dist="uniform",
-                  broadcast_b=False):
+                  broadcast_b=False, broadcast_a=False, ws=None):
     """Operands stored as the form says, with `gap` extra floats between
-    rows and matrices; returns (host A list, host B list, device views)."""
+    rows and matrices; returns (host A list, host B list, device views).
+    ws: None calls gemm_f32_batched; "full" gemm_f32_batched_ws with the
+    scratch gemm_f32_batched_workspace_size asks for (NaN-filled), "short"
+    with 256 bytes less."""
     rng_seed = seed
     As, Bs = [], []
     for i in range(batch):
         a, b = synth.make_operands(M, N, K, seed=rng_seed + i, dist_a=dist,
                                    dist_b=dist)
-        As.append(a)
+        As.append(As[0] if (broadcast_a and i) else a)
         Bs.append(Bs[0] if (broadcast_b and i) else b)
     ta, tb = form[0] == "T", form[1] == "T"
     a_store = [x.T.copy() if ta else x for x in As]      # stored shapes
@@ -630,10 +633,11 @@ def _batched_case(form, M, N, K, batch, seed, gap=0, dist="uniform",
     rb, cb = b_store[0].shape
     lda, ldb = ca + gap, cb + gap
     sA, sB = ra * lda + gap, rb * ldb + gap
-    bufA = torch.full((batch * sA + 1,), float("nan"), device=DEV)
+    na = 1 if broadcast_a else batch
+    bufA = torch.full((na * sA + 1,), float("nan"), device=DEV)
     nb = 1 if broadcast_b else batch
     bufB = torch.full((nb * sB + 1,), float("nan"), device=DEV)
-    for i in range(batch):
+    for i in range(na):
         bufA[i * sA:i * sA + ra * lda].view(ra, lda)[:, :ca] = \
             torch.from_numpy(a_store[i]).to(DEV)
     for i in range(nb):
@@ -641,10 +645,18 @@ def _batched_case(form, M, N, K, batch, seed, gap=0, dist="uniform",
             torch.from_numpy(b_store[i]).to(DEV)
     ldc, sC = N + gap, M * (N + gap) + gap
     bufC = torch.full((batch * sC + 1,), -7.0, device=DEV)
-    G.gemm_f32_batched_ptr(int(ta), int(tb), M, N, K, bufA.data_ptr(), lda, sA,
-                           bufB.data_ptr(), ldb, 0 if broadcast_b else sB,
-                           bufC.data_ptr(), ldc, sC, batch,
-                           torch.cuda.current_stream().cuda_stream)
+    args = (int(ta), int(tb), M, N, K, bufA.data_ptr(), lda,
+            0 if broadcast_a else sA, bufB.data_ptr(), ldb,
+            0 if broadcast_b else sB, bufC.data_ptr(), ldc, sC, batch)
+    if ws is None:
+        G.gemm_f32_batched_ptr(*args, torch.cuda.current_stream().cuda_stream)
+    else:
+        need = G.batched_workspace_size(int(ta), int(tb), M, N, K, batch)
+        nbytes = need if ws == "full" else max(need - 256, 0)
+        scratch = torch.full((max(nbytes // 4, 1),), float("nan"), device=DEV)
+        G.gemm_f32_batched_ws_ptr(*args, scratch.data_ptr() if nbytes else 0,
+                                  nbytes,
+                                  torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     host = bufC.cpu().numpy()
     Cs = [host[i * sC:i * sC + M * ldc].reshape(M, ldc) for i in range(batch)]
@@ -673,6 +685,60 @@ def test_batched_forms(form, shape, batch, gap):
         check_full(Ai[i], Bi[i], Ci[i][:, :N], exact=True,
                    what=f"{form} b{i} {shape} int")
     assert G.device_status() == 0
+
+
+@pytest.mark.parametrize("form", ["TN", "NN", "NT", "TT"])
+@pytest.mark.parametrize("ws", ["full", "short"])
+@pytest.mark.parametrize("shape,batch,gap", [((300, 260, 77), 3, 0),
+                                             ((129, 65, 33), 2, 3),
+                                             ((64, 64, 64), 4, 4),
+                                             ((1000, 700, 300), 1, 0),
+                                             ((257, 384, 513), 2, 4),
+                                             ((1, 1, 1), 1, 0)])
+def test_batched_forms_with_workspace(form, ws, shape, batch, gap):
+    """gemm_f32_batched_ws: Aᵀ·B through a transposed copy of A when the
+    scratch holds it (else in place), every other form as without scratch;
+    padding and gaps untouched, integers exact."""
+    M, N, K = shape
+    As, Bs, Cs, host, sC, ldc = _batched_case(form, M, N, K, batch,
+                                              seed=M + 1, gap=gap, ws=ws)
+    for i in range(batch):
+        check_full(As[i], Bs[i], Cs[i][:, :N], what=f"{form} ws b{i}")
+        assert (Cs[i][:, N:] == -7.0).all()
+    if gap:
+        for i in range(batch):
+            assert (host[i * sC + M * ldc:(i + 1) * sC] == -7.0).all()
+    Ai, Bi, Ci, _, _, _ = _batched_case(form, M, N, K, batch, seed=K + 1,
+                                        gap=gap, dist="int", ws=ws)
+    for i in range(batch):
+        check_full(Ai[i], Bi[i], Ci[i][:, :N], exact=True,
+                   what=f"{form} ws b{i} int")
+    assert G.device_status() == 0
+
+
+def test_tn_workspace_shared_a():
+    """Aᵀ·B with strideA = 0: one transposed copy serves every product."""
+    As, Bs, Cs, _, _, _ = _batched_case("TN", 300, 200, 136, 4, seed=3,
+                                        broadcast_a=True, ws="full")
+    for i in range(4):
+        check_full(As[i], Bs[i], Cs[i][:, :200], what=f"shared A {i}")
+
+
+def test_batched_workspace_size():
+    M, N, K = 1000, 700, 300
+    t_bytes = (M * ((K + 3) // 4 * 4) * 4 + 255) // 256 * 256
+    split = G.workspace_size(M, N, K)
+    assert G.batched_workspace_size(G.OP_T, G.OP_N, M, N, K, 1) == \
+        t_bytes + split
+    assert G.batched_workspace_size(G.OP_T, G.OP_N, M, N, K, 3) == 3 * t_bytes
+    assert G.batched_workspace_size(G.OP_N, G.OP_N, M, N, K, 1) == split
+    assert G.batched_workspace_size(G.OP_N, G.OP_T, M, N, K, 1) == 0
+    assert G.batched_workspace_size(G.OP_T, G.OP_T, M, N, K, 2) == 0
+    assert G.batched_workspace_size(G.OP_T, G.OP_N, M, N, 0, 1) == 0
+    with pytest.raises(G.GemmError):
+        G.batched_workspace_size(2, 0, M, N, K, 1)
+    with pytest.raises(G.GemmError):
+        G.batched_workspace_size(0, 0, -1, N, K, 1)
 
 
 def test_batched_broadcast_operand():
@@ -710,11 +776,12 @@ def test_batched_forms_forced_simt(form):
         check_full(As[i], Bs[i], Cs[i][:, :260], what=f"simt {form} b{i}")
 
 
-@pytest.mark.parametrize("form", ["NT", "TT", "TN"])
-def test_transposed_forms_large_sampled(form):
+@pytest.mark.parametrize("form,ws", [("NT", None), ("TT", None),
+                                     ("TN", None), ("TN", "full")])
+def test_transposed_forms_large_sampled(form, ws):
     """op forms at 2048 x 1536 x 1024, sampled against the oracle."""
     M, N, K = 2048, 1536, 1024
-    As, Bs, Cs, _, _, _ = _batched_case(form, M, N, K, 1, seed=5)
+    As, Bs, Cs, _, _, _ = _batched_case(form, M, N, K, 1, seed=5, ws=ws)
     check_sampled_and_rowsums(As[0], Bs[0], np.ascontiguousarray(Cs[0][:, :N]),
                               what=f"{form} large")
 
