@@ -84,6 +84,7 @@ struct Plan {
   int tc_cfg;    // for ALGO_TF32X3
   int splits;    // split-K factor for ALGO_TF32X3 (1 = none)
   int full_tiles;  // tiles computed whole before the split ones
+  bool tc_stream;  // ALGO_TF32X3 on the streaming kernel (narrow B)
   long long ws_bytes;  // scratch the plan needs (0 = none)
   bool vec;      // 16-byte operand copies
   bool c_vec;    // 16-byte C stores
@@ -173,6 +174,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   plan->tc_cfg = choose_tc_cfg(M, N, d);
   plan->splits = 1;
   plan->full_tiles = 0;
+  plan->tc_stream = false;
   plan->ws_bytes = 0;
   const bool tcgen05_ok = d.cc_major == 10 && vec && K >= 1;
   switch (algo) {
@@ -195,8 +197,15 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
     default:
       return GEMM_F32_ERR_INVALID_ARG;
   }
-  if (plan->algo == GEMM_F32_ALGO_TF32X3)
-    choose_splits(M, N, K, tf32x3_tile_m(plan->tc_cfg), d, plan);
+  if (plan->algo == GEMM_F32_ALGO_TF32X3) {
+    // B narrow and shallow enough to live in TMEM, and at least one
+    // 128-row tile per SM: the persistent streaming kernel
+    if (tf32x3_stream_fits(N, K) && (M + 127) / 128 >= d.sm_count &&
+        env_int("GEMM_F32_STREAM", 1) != 0)
+      plan->tc_stream = true;
+    else
+      choose_splits(M, N, K, tf32x3_tile_m(plan->tc_cfg), d, plan);
+  }
   return GEMM_F32_OK;
 }
 
@@ -295,9 +304,12 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       wc.limit = g_wait_ns.load();
       wc.debug = g_debug_flags.load();
       wc.status = d->status;
-      e = launch_tf32x3(p, plan.tc_cfg, plan.full_tiles, plan.splits,
-                        plan.splits > 1 ? static_cast<float*>(ws) : nullptr,
-                        wc, s);
+      e = plan.tc_stream
+              ? launch_tf32x3_stream(p, d->sm_count, wc, s)
+              : launch_tf32x3(p, plan.tc_cfg, plan.full_tiles, plan.splits,
+                              plan.splits > 1 ? static_cast<float*>(ws)
+                                              : nullptr,
+                              wc, s);
       break;
     }
     default:

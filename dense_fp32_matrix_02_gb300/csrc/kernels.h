@@ -72,6 +72,17 @@ cudaError_t launch_tf32x3(const Problem& p, int cfg, int full_tiles,
                           int splits, float* partials, const WaitCfg& wc,
                           cudaStream_t stream);
 
+// Whether the streaming 3xTF32 kernel takes an N × K B (N <= 128,
+// K <= 128: B lives in TMEM).
+bool tf32x3_stream_fits(long long N, long long K);
+
+// Persistent 3xTF32 kernel for narrow, shallow B and many rows: single
+// plain products (no batch, transposes or split-K), A and B 16-byte aligned
+// with lda and ldb multiples of 4; C any alignment (TMA stores when it is
+// 16-byte aligned with ldc a multiple of 4); fused bias / GELU.
+cudaError_t launch_tf32x3_stream(const Problem& p, int sm_count,
+                                 const WaitCfg& wc, cudaStream_t stream);
+
 // Scratch bytes the automatic plan wants for these arguments on the current
 // device (0 = none), or minus a gemm_f32_status.
 long long auto_plan_scratch_bytes(int64_t M, int64_t N, int64_t K,

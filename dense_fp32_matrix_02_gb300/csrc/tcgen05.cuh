@@ -58,6 +58,13 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory");
 }
 
+// The split the tensor core sees when it reads x itself: big = x with its
+// 13 low mantissa bits dropped (TF32 truncation), small = x - big (exact).
+__device__ __forceinline__ uint32_t tf32_small_of_truncated(float x) {
+  const float big = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  return __float_as_uint(__fsub_rn(x, big));
+}
+
 // ------------------------------------------------------------ MMA
 // D[tmem] (+)= A[tmem] · B[smem]ᵀ, kind::tf32, one CTA.  `accumulate` = 0
 // overwrites D.

@@ -140,13 +140,6 @@ __device__ __forceinline__ void tf32_split(float x, uint32_t& big,
   small = __float_as_uint(__fsub_rn(x, __uint_as_float(b)));
 }
 
-// The split the tensor core sees when it reads x itself: big = x with its
-// 13 low mantissa bits dropped (TF32 truncation), small = x - big (exact).
-__device__ __forceinline__ uint32_t tf32_small_of_truncated(float x) {
-  const float big = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-  return __float_as_uint(__fsub_rn(x, big));
-}
-
 // Bounded wait on one phase of an mbarrier.  Gives up (false) when the CTA
 // abort flag is raised or `limit_ns` of %globaltimer time pass.  With
 // `sleep`, each probe lets the thread sleep until the phase completes (up to

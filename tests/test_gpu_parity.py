@@ -399,6 +399,89 @@ def test_tf32x3_timeout_path_reports_and_recovers(tc_cfg):
     assert G.device_status() == 0
 
 
+# ------------------------------------------------------------- streaming
+def _tile_rows():
+    """Rows that give every SM one 128-row tile: the smallest M for which
+    the automatic plan streams A past a B held in tensor memory."""
+    return torch.cuda.get_device_properties(DEV).multi_processor_count * 128
+
+
+def _stream_shapes():
+    r = _tile_rows()
+    return [(65536, 64, 64),         # the tall-skinny workload
+            (r + 77, 128, 128),      # B at the kernel's limits
+            (r, 1, 1),
+            (2 * r + 5, 100, 77),    # ragged N and K, a partial last tile
+            (r + 1, 33, 16),
+            (3 * r - 3, 65, 120)]
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_stream_kernel_shapes(case):
+    """N <= 128, K <= 128 and a tile per SM: the persistent kernel that
+    keeps Bᵀ in TMEM; every element against the oracle, and integers
+    exact."""
+    M, N, K = _stream_shapes()[case]
+    a, b = synth.make_operands(M, N, K, seed=case, dist_a="normal",
+                               dist_b="normal")
+    check_full(a, b, run_gpu(a, b, pad=True), what=f"stream {M}x{N}x{K}")
+    ai, bi = synth.make_operands(M, N, K, seed=case + 50, dist_a="int",
+                                 dist_b="int")
+    check_full(ai, bi, run_gpu(ai, bi, pad=True), exact=True,
+               what=f"stream int {M}x{N}x{K}")
+    assert G.device_status() == 0
+
+
+def test_stream_kernel_off_matches_oracle_too():
+    """GEMM_F32_STREAM=0 sends the same shapes to the tiled tensor kernel."""
+    for M, N, K in _stream_shapes()[:2]:
+        a, b = synth.make_operands(M, N, K, seed=9)
+        with _env("GEMM_F32_STREAM", 0):
+            c = run_gpu(a, b, pad=True)
+        check_full(a, b, c, what=f"tiled {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_stream_kernel_bias_act(act):
+    M, N, K = _stream_shapes()[3]
+    a, b = synth.make_operands(M, N, K, seed=4, dist_a="normal",
+                               dist_b="normal")
+    bias = synth.make_operands(1, N, 1, seed=8)[1][0]
+    c = G.gemm_f32_bias_act(_padded(a), _padded(b),
+                            torch.from_numpy(bias).to(DEV), act)
+    torch.cuda.synchronize()
+    _check_epilogue(a, b, bias, act, c.cpu().numpy(), what=f"stream act {act}")
+
+
+def test_stream_kernel_odd_ldc():
+    """C with an odd leading dimension (lane stores, no alignment needed);
+    the padding column is left alone."""
+    M, N, K = _tile_rows() + 3, 60, 40
+    a, b = synth.make_operands(M, N, K, seed=12)
+    store = torch.full((M, N + 1), -5.0, device=DEV)
+    G.gemm_f32_ex(_padded(a), _padded(b), store[:, :N])
+    torch.cuda.synchronize()
+    host = store.cpu().numpy()
+    check_full(a, b, host[:, :N], what="stream odd ldc")
+    assert (host[:, N] == -5.0).all()
+
+
+def test_stream_kernel_timeout_path_reports_and_recovers():
+    M, N, K = _tile_rows() + 5, 64, 64
+    a, b = synth.make_operands(M, N, K, seed=2)
+    old_t = G.set_wait_timeout_ns(2_000_000)
+    old_f = G.set_debug_flags(G.DEBUG_STALL_PRODUCER)
+    try:
+        run_gpu(a, b, pad=True)
+        assert G.device_status() == 4
+    finally:
+        G.set_debug_flags(old_f)
+        G.set_wait_timeout_ns(old_t)
+    assert G.device_status() == 0
+    check_full(a, b, run_gpu(a, b, pad=True), what="stream after timeout")
+    assert G.device_status() == 0
+
+
 # ------------------------------------------------------------- split-K
 def run_gpu_ws(a, b, ws_bytes=None):
     """C = A·B through gemm_f32_ws with a workspace of the size it asks."""
