@@ -224,6 +224,16 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src,
       : "memory");
 }
 
+// The same for a 3-D tensor (c2: the batch coordinate).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
+                                             int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, "
+      "%4}], [%1];\n" ::"l"(tmap),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
 }

@@ -25,8 +25,11 @@
 //   * the MMA's B operand is the A tile (TILE_M rows of C × k), K-major as
 //     TMA copies it from row-major A, 64-byte swizzled.
 // The fp32 accumulator D (TMEM lane = column n of C, TMEM column = row m of
-// C) is read back by the same converter warps, whose 32 lanes then store 32
-// consecutive columns of one row of C.
+// C) is read back by the same converter warps once every MMA has completed:
+// each 32-row block of a warp's 32 columns is staged in the (now idle) ring
+// in the 128-byte swizzle and written by a TMA bulk tensor store (to C, or
+// to the split-K scratch); for the transposed store, or a C no tensor map
+// can describe, the 32 lanes store 32 consecutive columns of one row.
 //
 // Tiles: TILE_M rows × 128 columns of C.  The default is 128 × 128 with a
 // 4-stage ring of 16-deep k stages (24 KB each) and 256 TMEM columns, so
@@ -56,6 +59,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -110,6 +115,8 @@ struct Cfg {
   static_assert(!TB || RAW_BIG, "transposed B only with the raw split");
   static_assert(!TA || (RAW_BIG && TILE_M == 128 && !TB && !TSTORE),
                 "transposed A: raw split, 128-row tiles, plain B and store");
+  // the epilogue stages 8 warps × TILE_M / 64 blocks of 4 KB in the ring
+  static_assert(8 * (TILE_M / 64) * 4096 <= kOffCtl, "epilogue staging");
 };
 
 constexpr int kMaxStages = 8;
@@ -166,11 +173,13 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
 template <class Cf>
 __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                       const __grid_constant__ CUtensorMap tmap_b, float* C,
+                       const __grid_constant__ CUtensorMap tmap_b,
+                       const __grid_constant__ CUtensorMap tmap_c,
+                       const __grid_constant__ CUtensorMap tmap_p, float* C,
                        long long ldc, int M, int N, int K, int tiles_m,
                        int tiles_n, int full_tiles, int tail_splits,
                        int kb_per_split, float* partials, long long sC,
-                       int batched_ab,
+                       int batched_ab, int store_tma,
                        const float* bias, int act, WaitCfg wc) {
   // batch: matrix blockIdx.z; tensor-map batch coordinates are z for a
   // batched operand and 0 for one shared by every product (batched_ab bits
@@ -451,8 +460,60 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         const bool epi = whole && (bias != nullptr || act != 0);
         const float bias_n =
             (epi && bias != nullptr && n < N) ? bias[n] : 0.f;
+        // TMA stores (store_tma bit 0: whole tiles to C, bit 1: partial
+        // tiles to the scratch): each 32-row block of this warp's half of
+        // the accumulator (rows c of the tile × the warp's 32 columns) is
+        // staged in the ring, idle now that every MMA has completed, row by
+        // row in the 128-byte swizzle, and stored by one bulk tensor copy
+        // that skips what lies past M or N
+        const bool tma = !Cf::kTStore && ((whole ? store_tma : store_tma >> 1) & 1);
+        if (tma) {
+          constexpr int kBlocks = kAccCols / 2 / 32;
+          unsigned char* stg = smem + (warp - 2) * kBlocks * 4096;
+          const uint32_t stg_s = sbase + (warp - 2) * kBlocks * 4096;
 #pragma unroll 1
-        for (int c0 = c_begin; c0 < c_begin + kAccCols / 2; c0 += 16) {
+          for (int j = 0; j < kBlocks; ++j) {
+            uint32_t v[32];
+            tmem_ld16(tmem + lane_bits + c_begin + 32 * j, v);
+            tmem_ld16(tmem + lane_bits + c_begin + 32 * j + 16, v + 16);
+            tmem_ld_wait();
+            if (epi) {
+#pragma unroll
+              for (int r = 0; r < 32; ++r) {
+                float x = __uint_as_float(v[r]);
+                if (bias != nullptr) x += bias_n;
+                v[r] = __float_as_uint(epilogue_act(x, act));
+              }
+            }
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              *reinterpret_cast<uint32_t*>(
+                  stg + j * 4096 + r * 128 +
+                  ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2))) =
+                  v[r];
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int x0 = bn + q * 32;  // first column of this warp
+            for (int j = 0; j < kBlocks; ++j) {
+              const int y0 = bm + c_begin + 32 * j;  // first row
+              if (whole) {
+                if (x0 < N && y0 < M)
+                  tma_store_3d(&tmap_c, stg_s + j * 4096, x0, y0, z);
+              } else {
+                tma_store_2d(&tmap_p, stg_s + j * 4096, q * 32,
+                             (jt * tail_splits + split) * kTileM + c_begin +
+                                 32 * j);
+              }
+            }
+            bulk_commit_group();
+            bulk_wait_group<0>();
+          }
+          __syncwarp();
+        }
+#pragma unroll 1
+        for (int c0 = c_begin; !tma && c0 < c_begin + kAccCols / 2; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tmem + lane_bits + c0, v);
           tmem_ld_wait();
@@ -556,6 +617,12 @@ __global__ void __launch_bounds__(256)
 
 namespace {
 
+// GEMM_F32_TMA_STORE=0 keeps the epilogue's per-lane stores (comparison).
+bool env_store_tma() {
+  const char* v = std::getenv("GEMM_F32_TMA_STORE");
+  return !(v && v[0] == '0');
+}
+
 // 3-D tensor map (x innermost, y rows, z batch) of fp32 with a box of
 // bx × by × 1.  A batch stride of 0 (one matrix shared by every product)
 // gives a batch extent of 1.
@@ -597,6 +664,31 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
               : encode_3d(encode, &tb, p.B, p.N, p.K, p.ldb, p.sB, p.batch,
                           Cf::kTileN, Cf::kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok_b) return cudaErrorInvalidValue;
+  // C (x = n, y = m, z = batch) and the partial tiles (x = n within the
+  // tile, y = slot·TILE_M + row): 32 × 32 boxes in the 128-byte swizzle,
+  // stored by TMA from the epilogue; C only where a tensor map can describe
+  // it (16-byte aligned, ldc and the batch stride multiples of 4), never
+  // for the transposed store
+  CUtensorMap tc, tp;
+  std::memset(&tc, 0, sizeof(tc));
+  std::memset(&tp, 0, sizeof(tp));
+  int store_tma = 0;
+  if (!Cf::kTStore && (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
+      p.ldc % 4 == 0 && (p.batch == 1 || p.sC % 4 == 0) &&
+      env_store_tma()) {
+    const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.M,
+                                (cuuint64_t)p.batch};
+    const long long zs = p.batch > 1 ? p.sC : (long long)p.M * p.ldc;
+    const cuuint64_t strides[2] = {(cuuint64_t)p.ldc * 4,
+                                   (cuuint64_t)((zs + 3) / 4 * 4) * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.C, dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      store_tma |= 1;
+  }
   auto fn = tf32x3_gemm_kernel<Cf>;
   constexpr int kSmem = smem_bytes<Cf>();
   cudaError_t e =
@@ -621,10 +713,21 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
     return cudaErrorInvalidConfiguration;
   const int batched_ab =
       (p.batch > 1 && p.sA != 0 ? 1 : 0) | (p.batch > 1 && p.sB != 0 ? 2 : 0);
+  if (tail > 0 && env_store_tma()) {
+    const cuuint64_t dims[2] = {128, (cuuint64_t)(tail * ts * Cf::kTileM)};
+    const cuuint64_t strides[1] = {128 * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, partials, dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      store_tma |= 2;
+  }
   fn<<<dim3((unsigned)grid, 1, (unsigned)p.batch), Cf::kThreads, kSmem,
-       stream>>>(ta, tb, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n,
+       stream>>>(ta, tb, tc, tp, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n,
                  (int)full, ts, kb_per_split, partials, p.sC, batched_ab,
-                 p.bias, p.act, wc);
+                 store_tma, p.bias, p.act, wc);
   e = cudaGetLastError();
   if (e != cudaSuccess || tail == 0) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
