@@ -189,6 +189,22 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------ programmatic launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running; griddep_wait blocks
+// until that kernel has completed and its memory operations are visible, so
+// every thread calls it before touching global memory the earlier kernel
+// may write or read.  Without that launch attribute it returns at once.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+// Lets the next kernel in the stream (launched programmatically) be
+// scheduled before this one ends; it still waits in griddep_wait.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled bulk tensor load into shared memory, completion counted on the
 // mbarrier in transaction bytes.  c0 is the innermost coordinate.

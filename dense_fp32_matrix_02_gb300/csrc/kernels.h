@@ -7,10 +7,31 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 #include "gemm_f32.h"
 
 namespace gemm_f32_impl {
+
+// Launches `kernel` with programmatic stream serialization: its CTAs may be
+// scheduled while the previous kernel in the stream finishes; the kernel
+// calls griddep_wait before it touches global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // SIMT tile configurations (BM x BN x BK); "Occ1" variants let a thread use
 // up to 255 registers at one CTA per SM instead of 128 at two.

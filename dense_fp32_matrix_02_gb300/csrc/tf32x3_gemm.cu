@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
+  griddep_wait();  // A, B, C and the scratch may belong to the kernel before
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -454,6 +455,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         if (lane == 0) record_status(wc.status, kStatusTimeoutMma);
       } else {
         tc_fence_after_sync();
+        griddep_launch_dependents();  // the main loop is over
         const int n = bn + n_loc;
         const int c_begin = h * (kAccCols / 2);
         // this lane's column n has one bias value; load it once
@@ -558,6 +560,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
     }
   }
 
+  griddep_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
@@ -577,6 +580,8 @@ __global__ void __launch_bounds__(256)
                        float* __restrict__ C, long long ldc, int vec,
                        const float* __restrict__ bias, int act) {
   constexpr int kCols = 128, kGroups = kCols / 4;
+  griddep_wait();  // the partial tiles of the kernel before
+  griddep_launch_dependents();
   const bool epi = bias != nullptr || act != 0;
   const long long slot = (long long)tile_m * kCols;
   const long long per_tile = (long long)tile_m * kGroups;
@@ -724,11 +729,11 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       store_tma |= 2;
   }
-  fn<<<dim3((unsigned)grid, 1, (unsigned)p.batch), Cf::kThreads, kSmem,
-       stream>>>(ta, tb, tc, tp, p.C, p.ldc, p.M, p.N, p.K, tiles_m, tiles_n,
-                 (int)full, ts, kb_per_split, partials, p.sC, batched_ab,
-                 store_tma, p.bias, p.act, wc);
-  e = cudaGetLastError();
+  e = launch_pdl(fn, dim3((unsigned)grid, 1, (unsigned)p.batch),
+                 dim3(Cf::kThreads), kSmem, stream, ta, tb, tc, tp, p.C,
+                 p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, (int)full, ts,
+                 kb_per_split, partials, p.sC, batched_ab, store_tma, p.bias,
+                 p.act, wc);
   if (e != cudaSuccess || tail == 0) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
                    p.ldc % 4 == 0)
@@ -737,10 +742,10 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
   const long long groups = tail * Cf::kTileM * (128 / 4);
   const int blocks = (int)((groups + 255) / 256 < 4096 ? (groups + 255) / 256
                                                       : 4096);
-  tail_reduce_kernel<<<blocks, 256, 0, stream>>>(
-      partials, ts, (int)full, (int)tail, Cf::kTileM, tiles_m, tiles_n, p.M,
-      p.N, p.C, p.ldc, vec, p.bias, p.act);
-  return cudaGetLastError();
+  return launch_pdl(tail_reduce_kernel, dim3(blocks), dim3(256), 0, stream,
+                    (const float*)partials, ts, (int)full, (int)tail,
+                    Cf::kTileM, tiles_m, tiles_n, p.M, p.N, p.C, p.ldc, vec,
+                    p.bias, p.act);
 }
 
 }  // namespace

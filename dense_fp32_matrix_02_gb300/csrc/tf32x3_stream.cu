@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
+  griddep_wait();  // A, B and C may belong to the kernel before
   const uint32_t bt_raw = tmem + 2 * kAccCols;
   const uint32_t bt_small = bt_raw + kp;
 
@@ -374,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (c_tma && lane == 0) bulk_wait_group<0>();  // C written
   }
 
+  griddep_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
@@ -443,10 +445,9 @@ cudaError_t launch_tf32x3_stream(const Problem& p, int sm_count,
   if (e != cudaSuccess) return e;
   const long long tiles = ((long long)p.M + kTileM - 1) / kTileM;
   const int grid = (int)(tiles < sm_count ? tiles : sm_count);
-  tf32x3_stream_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-      ta, tb, tc, p.C, p.ldc, p.M, p.N, p.K, nb, (int)tiles, c_tma, p.bias,
-      p.act, wc);
-  return cudaGetLastError();
+  return launch_pdl(tf32x3_stream_kernel, dim3(grid), dim3(kThreads),
+                    kSmemBytes, stream, ta, tb, tc, p.C, p.ldc, p.M, p.N, p.K,
+                    nb, (int)tiles, c_tma, p.bias, p.act, wc);
 }
 
 }  // namespace gemm_f32_impl
