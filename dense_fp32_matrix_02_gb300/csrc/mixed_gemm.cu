@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
+  griddep_wait();  // A, B and C may belong to the kernel before
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -310,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (c_mode == 2 && lane == 0) bulk_wait_group<0>();  // C written
   }
 
+  griddep_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
@@ -326,6 +328,8 @@ __global__ void __launch_bounds__(256)
     round16_kernel(long long rows, long long cols,
                    const float* __restrict__ src, long long lds,
                    uint16_t* __restrict__ dst, long long ldd, int vec) {
+  griddep_wait();  // src may belong to the kernel before
+  griddep_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long first = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (vec) {
@@ -369,6 +373,8 @@ __global__ void __launch_bounds__(256)
 // C[0:M, 0:N] = 0 (the empty sum of a K = 0 product).
 __global__ void __launch_bounds__(256)
     fill_zero_kernel(float* C, long long ldc, long long M, long long N) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long total = M * N;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x;
        g < total; g += (long long)gridDim.x * blockDim.x)
@@ -457,11 +463,10 @@ cudaError_t launch_mixed16(const Problem16& p, const Plan16& plan, bool c_vec,
       plan.tiles_m != (p.M + kBM - 1) / kBM ||
       plan.tiles_n != (p.N + plan.wn - 1) / plan.wn)
     return cudaErrorInvalidConfiguration;
-  fn<<<plan.grid, kThreads, kSmemBytes, stream>>>(
-      ta, tb, tc, p.C, p.ldc, p.M, p.N, p.K, (int)plan.tiles_m,
-      (int)plan.tiles_n, plan.wn, (int)plan.full, plan.parts,
-      (int)plan.units, c_mode, wc);
-  return cudaGetLastError();
+  return launch_pdl(fn, dim3(plan.grid), dim3(kThreads), kSmemBytes, stream,
+                    ta, tb, tc, p.C, p.ldc, p.M, p.N, p.K, (int)plan.tiles_m,
+                    (int)plan.tiles_n, plan.wn, (int)plan.full, plan.parts,
+                    (int)plan.units, c_mode, wc);
 }
 
 cudaError_t launch_round16(int type, long long rows, long long cols,
@@ -477,12 +482,10 @@ cudaError_t launch_round16(int type, long long rows, long long cols,
   const long long cap = 8LL * sm_count;
   if (blocks > cap) blocks = cap;
   if (type == GEMM_F32_MIXED_BF16)
-    round16_kernel<1><<<(int)blocks, 256, 0, stream>>>(rows, cols, src, lds,
-                                                       dst, ldd, vec ? 1 : 0);
-  else
-    round16_kernel<0><<<(int)blocks, 256, 0, stream>>>(rows, cols, src, lds,
-                                                       dst, ldd, vec ? 1 : 0);
-  return cudaGetLastError();
+    return launch_pdl(round16_kernel<1>, dim3((unsigned)blocks), dim3(256), 0,
+                      stream, rows, cols, src, lds, dst, ldd, vec ? 1 : 0);
+  return launch_pdl(round16_kernel<0>, dim3((unsigned)blocks), dim3(256), 0,
+                    stream, rows, cols, src, lds, dst, ldd, vec ? 1 : 0);
 }
 
 cudaError_t launch_fill_zero(float* C, long long ldc, long long M, long long N,
@@ -492,8 +495,8 @@ cudaError_t launch_fill_zero(float* C, long long ldc, long long M, long long N,
   long long blocks = (M * N + 255) / 256;
   const long long cap = 8LL * sm_count;
   if (blocks > cap) blocks = cap;
-  fill_zero_kernel<<<(int)blocks, 256, 0, stream>>>(C, ldc, M, N);
-  return cudaGetLastError();
+  return launch_pdl(fill_zero_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                    stream, C, ldc, M, N);
 }
 
 }  // namespace gemm_f32_impl

@@ -204,6 +204,7 @@ template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB, bool AKM,
           bool TA, bool TB>
 __global__ void __launch_bounds__(FfmaTileT<BM, BN, BK>::kThreads, MINB)
     simt_gemm_kernel(Problem p, int tiles_m, int tiles_n, int c_vec) {
+  griddep_wait();  // A, B and C may belong to the kernel before
   SimtKernel<BM, BN, BK, STAGES, VEC, AKM, TA, TB>::run(p, tiles_m, tiles_n,
                                                         c_vec);
 }
@@ -222,9 +223,9 @@ cudaError_t launch_cfg(const Problem& p, bool c_vec, cudaStream_t stream) {
   const long long grid = (long long)tiles_m * tiles_n;
   if (grid > 0x7fffffffLL || p.batch < 1 || p.batch > 65535)
     return cudaErrorInvalidConfiguration;
-  fn<<<dim3((unsigned)grid, 1, (unsigned)p.batch), K::kThreads, K::kSmemBytes,
-       stream>>>(p, tiles_m, tiles_n, c_vec);
-  return cudaGetLastError();
+  return launch_pdl(fn, dim3((unsigned)grid, 1, (unsigned)p.batch),
+                    dim3(K::kThreads), K::kSmemBytes, stream, p, tiles_m,
+                    tiles_n, (int)c_vec);
 }
 
 // Transposed operands: one tile configuration (128 x 128 x 32, 4 stages).

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_ffma_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, Problem p,
                     int tiles_m, int tiles_n, int c_vec, WaitCfg wc) {
+  griddep_wait();  // A, B and C may belong to the kernel before
   constexpr int kBK = Cf::kBK, kStages = Cf::kStages;
   constexpr int kStageBytesA = Cf::kStageBytesA;
   constexpr int kStageBytesB = Cf::kStageBytesB;
@@ -194,9 +195,8 @@ cudaError_t launch_cfg(const Problem& p, bool c_vec, const WaitCfg& wc,
   const int tiles_m = (p.M + kBM - 1) / kBM, tiles_n = (p.N + kBN - 1) / kBN;
   const long long grid = (long long)tiles_m * tiles_n;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fn<<<(unsigned)grid, kThreads, Cf::kSmemBytes, stream>>>(
-      ta, tb, p, tiles_m, tiles_n, c_vec ? 1 : 0, wc);
-  return cudaGetLastError();
+  return launch_pdl(fn, dim3((unsigned)grid), dim3(kThreads), Cf::kSmemBytes,
+                    stream, ta, tb, p, tiles_m, tiles_n, c_vec ? 1 : 0, wc);
 }
 
 }  // namespace

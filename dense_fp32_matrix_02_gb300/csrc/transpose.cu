@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256)
     transpose_kernel(const float* __restrict__ src, long long lds,
                      long long ss, float* __restrict__ dst, long long ldd,
                      long long sd, int rows, int cols, int batch) {
+  griddep_wait();  // src may belong to the kernel before
+  griddep_launch_dependents();
   __shared__ float tile[32][33];
   const int tiles_c = (cols + 31) / 32;
   const long long per = (long long)((rows + 31) / 32) * tiles_c;
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(256)
     transpose4_kernel(const float* __restrict__ src, long long lds,
                       long long ss, float* __restrict__ dst, long long ldd,
                       long long sd, int rows, int cols, int batch) {
+  griddep_wait();  // src may belong to the kernel before
+  griddep_launch_dependents();
   __shared__ float tile[64][65];
   const int tiles_c = (cols + 63) / 64;
   const long long per = (long long)((rows + 63) / 64) * tiles_c;
@@ -113,14 +117,11 @@ cudaError_t launch_transpose(const float* src, long long lds, long long ss,
   const long long wave = 8LL * (sm_count > 0 ? sm_count : 1);
   const int grid = (int)(tiles < wave ? tiles : wave);
   if (vec)
-    transpose4_kernel<<<grid, 256, 0, stream>>>(src, lds, ss, dst, ldd, sd,
-                                                (int)rows, (int)cols,
-                                                (int)batch);
-  else
-    transpose_kernel<<<grid, 256, 0, stream>>>(src, lds, ss, dst, ldd, sd,
-                                               (int)rows, (int)cols,
-                                               (int)batch);
-  return cudaGetLastError();
+    return launch_pdl(transpose4_kernel, dim3(grid), dim3(256), 0, stream,
+                      src, lds, ss, dst, ldd, sd, (int)rows, (int)cols,
+                      (int)batch);
+  return launch_pdl(transpose_kernel, dim3(grid), dim3(256), 0, stream, src,
+                    lds, ss, dst, ldd, sd, (int)rows, (int)cols, (int)batch);
 }
 
 }  // namespace gemm_f32_impl
