@@ -96,6 +96,8 @@ def load_peaks():
 # sources each kernel is built from (its counters go stale when one changes)
 KERNEL_SOURCES = {
     "tf32x3": ["tf32x3_gemm.cu", "tcgen05.cuh", "common.cuh", "kernels.h"],
+    "tf32x3_stream": ["tf32x3_stream.cu", "tcgen05.cuh", "common.cuh",
+                      "kernels.h"],
     "simt": ["simt_gemm.cu", "ffma_tile.cuh", "common.cuh", "kernels.h"],
     "tma": ["tma_ffma_gemm.cu", "ffma_tile.cuh", "common.cuh", "kernels.h"],
     "mixed16": ["mixed_gemm.cu", "tcgen05.cuh", "common.cuh", "kernels.h"],
@@ -110,6 +112,19 @@ def kernel_source_hash(kernel):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def hbm_roofline(flops, nbytes, kernel_ms, peaks, peaks_src, tensor_peak,
+                 achieved):
+    """Roofline entry of a memory-bound launch: algorithmic bytes per
+    launch over its time against the measured copy bandwidth, the tensor
+    figures beside it."""
+    gbs = nbytes / (kernel_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+            "peak_source": f"{peaks_src} HBM copy bandwidth",
+            "tensor_peak_tflops": tensor_peak,
+            "frac_tensor": achieved / tensor_peak}
 
 
 def recorded_traffic(kernel, workload):
@@ -563,7 +578,18 @@ def run_ours(args, w, config):
     fp32_peak = probe["tflops"]
     achieved = flops / (kernel_ms / 1e3) / 1e12
     algo_name = G.ALGO_NAMES.get(ran, str(ran))
-    if algo_name == "tf32x3":
+    if algo_name == "tf32x3" and not batched and algo == 0:
+        if G.plan(w.M, w.N, w.K)["variant"] == "streaming":
+            algo_name = "tf32x3_stream"  # B held in tensor memory
+    bw_roof = (flops / (w.bytes * args.batch)) * peaks["hbm_gbs"] / 1e3
+    if algo_name in ("tf32x3", "tf32x3_stream") and \
+            bw_roof < peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0:
+        # memory-bound shape: the copy bandwidth is the roof
+        roof = hbm_roofline(flops, w.bytes * args.batch, kernel_ms, peaks,
+                            peaks_src,
+                            peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0,
+                            achieved)
+    elif algo_name in ("tf32x3", "tf32x3_stream"):
         # three TF32 tensor products per algorithmic multiply-add; TF32
         # dense rate = bf16 rate x (1.1 / 2.25), the nominal ratio
         tf32 = peaks["bf16_tflops"] * (1.1 / 2.25)
@@ -589,7 +615,6 @@ def run_ours(args, w, config):
     roof["algorithmic_bytes"] = w.bytes * args.batch
     roof["kernel_ms"] = kernel_ms
 
-    bw_roof = (flops / (w.bytes * args.batch)) * peaks["hbm_gbs"] / 1e3
     fp32_roof = min(fp32_peak, bw_roof)
     fp32_roof_nameplate = min(fp32_nameplate, bw_roof)
     line = {
@@ -710,13 +735,17 @@ def run_mixed(args, w, config):
     peaks, peaks_src = load_peaks()
     achieved = flops / (kernel_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]  # binary16 has the same nominal dense rate
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak,
-            "unit": "TFLOP/s", "frac": achieved / peak,
-            "peak_source": f"{peaks_src} bf16 burst (cuBLAS bf16 GEMM)",
-            "traffic": None if args.from_f32
-            else recorded_traffic("mixed16", w.name),
-            "algorithmic_bytes": 2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N,
-            "kernel_ms": kernel_ms}
+    nbytes = 2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N
+    if flops / nbytes * peaks["hbm_gbs"] / 1e3 < peak and not args.from_f32:
+        roof = hbm_roofline(flops, nbytes, kernel_ms, peaks, peaks_src, peak,
+                            achieved)
+    else:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peaks_src} bf16 burst (cuBLAS bf16 GEMM)"}
+    roof.update({"traffic": None if args.from_f32
+                 else recorded_traffic("mixed16", w.name),
+                 "algorithmic_bytes": nbytes, "kernel_ms": kernel_ms})
     if args.from_f32:
         roof["note"] = ("step = two rounding kernels + the product; "
                         "achieved is over the whole step")

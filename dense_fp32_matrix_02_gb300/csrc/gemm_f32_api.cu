@@ -571,6 +571,26 @@ int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float* A,
   return plan.algo;
 }
 
+int gemm_f32_plan(int64_t M, int64_t N, int64_t K, const float* A,
+                  int64_t lda, const float* B, int64_t ldb, const float* C,
+                  int64_t ldc, int64_t out[4]) {
+  if (!out) return GEMM_F32_ERR_INVALID_ARG;
+  int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != GEMM_F32_OK) return st;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  Plan plan;
+  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, GEMM_F32_ALGO_AUTO, *d,
+                 &plan);
+  if (st != GEMM_F32_OK) return st;
+  out[0] = plan.algo;
+  out[1] = plan.tc_stream ? 1 : 0;
+  out[2] = plan.splits;
+  out[3] = plan.full_tiles;
+  return GEMM_F32_OK;
+}
+
 const char* gemm_f32_status_string(int status) {
   switch (status) {
     case GEMM_F32_OK:

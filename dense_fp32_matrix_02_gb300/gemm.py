@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_batched.restype = ci
         L.gemm_f32_batched.argtypes = [ci, ci, i64, i64, i64, vp, i64, i64,
                                        vp, i64, i64, vp, i64, i64, i64, vp]
+        L.gemm_f32_plan.restype = ci
+        L.gemm_f32_plan.argtypes = args[:-1] + [ctypes.POINTER(i64)]
         L.gemm_f32_batched_ws.restype = ci
         L.gemm_f32_batched_ws.argtypes = [ci, ci, i64, i64, i64, vp, i64,
                                           i64, vp, i64, i64, vp, i64, i64,
@@ -457,6 +459,23 @@ def gemm_f32(a, b, c=None, stream=None, workspace=None):
         gemm_f32_ws_ptr(M, N, K, ap, lda, bp, ldb, cp, ldc,
                         workspace.data_ptr() if nbytes else 0, nbytes, handle)
     return c
+
+
+def plan(M, N, K, a_ptr=16, lda=None, b_ptr=16, ldb=None, c_ptr=16,
+         ldc=None) -> dict:
+    """The automatic plan for these sizes (default: 16-byte aligned
+    pointers, leading dimensions = the row widths): kernel family, tensor
+    variant ("tiled" / "streaming"), split-K ways, whole tiles."""
+    out = (ctypes.c_int64 * 4)()
+    _check(lib().gemm_f32_plan(int(M), int(N), int(K), a_ptr or None,
+                               int(lda if lda is not None else max(K, 1)),
+                               b_ptr or None,
+                               int(ldb if ldb is not None else max(N, 1)),
+                               c_ptr or None,
+                               int(ldc if ldc is not None else max(N, 1)),
+                               out), "gemm_f32_plan")
+    return {"algo": out[0], "variant": "streaming" if out[1] else "tiled",
+            "splits": out[2], "whole_tiles": out[3]}
 
 
 def select_algo(M, N, K, a_ptr=0, lda=None, b_ptr=0, ldb=None, c_ptr=0,

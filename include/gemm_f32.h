@@ -350,6 +350,22 @@ GEMM_F32_API int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const flo
                          int64_t lda, const float *B, int64_t ldb, float *C,
                          int64_t ldc);
 
+/*
+ * The automatic plan gemm_f32_ws would run for these arguments and a
+ * workspace of gemm_f32_workspace_size bytes on the current device (no
+ * launch), for tests and tuning.  out[0]: kernel family (gemm_f32_algo);
+ * out[1]: tensor-kernel variant, 0 tiled, 1 streaming (B held in tensor
+ * memory: N <= 128, K <= 128 and at least one 128-row tile per SM; the
+ * environment variable GEMM_F32_STREAM=0 turns it off); out[2]: split-K
+ * ways of the split tiles (1: none); out[3]: tiles computed whole before
+ * the split ones.  Returns a status (GEMM_F32_ERR_INVALID_ARG also for
+ * out == NULL).
+ */
+GEMM_F32_API int gemm_f32_plan(int64_t M, int64_t N, int64_t K,
+                               const float *A, int64_t lda, const float *B,
+                               int64_t ldb, const float *C, int64_t ldc,
+                               int64_t out[4]);
+
 /* Static description of a status code. */
 GEMM_F32_API const char *gemm_f32_status_string(int status);
 

@@ -432,6 +432,25 @@ def test_stream_kernel_shapes(case):
     assert G.device_status() == 0
 
 
+def test_plan_reports_the_streaming_kernel():
+    """gemm_f32_plan: the streaming variant exactly for N, K <= 128 with a
+    128-row tile per SM (and not with GEMM_F32_STREAM=0); tiled otherwise."""
+    r = _tile_rows()
+    for M, N, K in _stream_shapes():
+        assert G.plan(M, N, K) == {"algo": G.ALGO_TF32X3,
+                                   "variant": "streaming", "splits": 1,
+                                   "whole_tiles": 0}, (M, N, K)
+    for M, N, K in [(r - 128, 64, 64), (r, 129, 64), (r, 64, 129),
+                    (4096, 4096, 4096)]:
+        assert G.plan(M, N, K)["variant"] == "tiled", (M, N, K)
+    with _env("GEMM_F32_STREAM", 0):
+        assert G.plan(65536, 64, 64)["variant"] == "tiled"
+    # unaligned operands: the FFMA kernel
+    assert G.plan(65536, 64, 64, a_ptr=20)["algo"] == G.ALGO_SIMT
+    with pytest.raises(G.GemmError):
+        G.plan(-1, 4, 4)
+
+
 def test_stream_kernel_off_matches_oracle_too():
     """GEMM_F32_STREAM=0 sends the same shapes to the tiled tensor kernel."""
     for M, N, K in _stream_shapes()[:2]:
