@@ -464,15 +464,18 @@ def gemm_f32(a, b, c=None, stream=None, workspace=None):
 def plan(M, N, K, a_ptr=16, lda=None, b_ptr=16, ldb=None, c_ptr=16,
          ldc=None) -> dict:
     """The automatic plan for these sizes (default: 16-byte aligned
-    pointers, leading dimensions = the row widths): kernel family, tensor
+    pointers, leading dimensions = the row widths rounded up to multiples
+    of 4, the layouts the tensor kernels take): kernel family, tensor
     variant ("tiled" / "streaming"), split-K ways, whole tiles."""
+    def pad4(x):
+        return max((int(x) + 3) // 4 * 4, 4)
     out = (ctypes.c_int64 * 4)()
     _check(lib().gemm_f32_plan(int(M), int(N), int(K), a_ptr or None,
-                               int(lda if lda is not None else max(K, 1)),
+                               int(lda if lda is not None else pad4(K)),
                                b_ptr or None,
-                               int(ldb if ldb is not None else max(N, 1)),
+                               int(ldb if ldb is not None else pad4(N)),
                                c_ptr or None,
-                               int(ldc if ldc is not None else max(N, 1)),
+                               int(ldc if ldc is not None else pad4(N)),
                                out), "gemm_f32_plan")
     return {"algo": out[0], "variant": "streaming" if out[1] else "tiled",
             "splits": out[2], "whole_tiles": out[3]}
