@@ -132,7 +132,9 @@ typedef enum {
 } gemm_f32_op;
 
 /*
- * Strided batch of products with optional transposes, without copies:
+ * Strided batch of products with optional transposes, without copies
+ * ("Rendre le GPU rapide" multiplies activations by transposed weight
+ * matrices in its layers; each product is the pages' C = A·B):
  *   for b in [0, batch):  C_b = op(A_b) · op(B_b)
  * where X_b = X + b·strideX (elements).  op(A) is M×K: with opA = N, A_b is
  * stored M×K row-major (lda >= K); with opA = T it is stored K×M (lda >= M)
@@ -164,7 +166,9 @@ GEMM_F32_API int gemm_f32_batched(int opA, int opB, int64_t M, int64_t N,
  * memory.  For batch = 1 the rest of the workspace is split-K scratch as
  * in gemm_f32_ws (also for opA = opB = N).  With less scratch, and for the
  * other forms, the call runs as gemm_f32_batched.  The workspace is in use
- * until the stream passes this call.
+ * until the stream passes this call.  GEMM_F32_ERR_INVALID_ARG for
+ * workspace_bytes < 0 or a NULL workspace with workspace_bytes > 0, and
+ * for everything gemm_f32_batched rejects.
  */
 GEMM_F32_API int gemm_f32_batched_ws(int opA, int opB, int64_t M, int64_t N,
                                      int64_t K, const float *A, int64_t lda,
