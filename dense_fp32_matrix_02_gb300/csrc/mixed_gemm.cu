@@ -29,6 +29,9 @@
 //               next.  Where C cannot be described by a tensor map (not
 //               16-byte aligned, or ldc not a multiple of 4) each lane
 //               stores its row directly instead.
+// Launched with programmatic stream serialization (the prologue overlaps
+// the end of the kernel before it; griddepcontrol.wait precedes every
+// global access).
 // Every mbarrier wait is bounded by %globaltimer.  A CTA that gives up sets
 // the status word, lets its copies and MMAs in flight land, frees TMEM and
 // returns without storing further tiles.

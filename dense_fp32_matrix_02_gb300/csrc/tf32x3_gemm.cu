@@ -52,6 +52,10 @@
 // transposed (TSTORE) for the swapped form of op(A)ᵀ·op(B)ᵀ; strided
 // batches run as gridDim.z; split-K writes partial tiles that a second
 // kernel adds in split order.
+// Launched with programmatic stream serialization: the prologue overlaps
+// the end of the kernel before it (every thread waits for it with
+// griddepcontrol.wait before touching global memory), and the converters
+// let the next kernel be scheduled once the main loop is over.
 // Every mbarrier wait is bounded by a %globaltimer deadline; a wait that
 // runs out sets the status word and a CTA-wide abort flag, the roles drain
 // their copies and MMAs in flight, TMEM is freed, and the CTA ends without

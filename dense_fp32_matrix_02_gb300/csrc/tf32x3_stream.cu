@@ -30,6 +30,10 @@
 //                cannot be described by a tensor map.
 // TMEM columns: accumulators [0, 256), Bᵀ raw [256, 256 + Kp), Bᵀ small
 // [256 + Kp, 256 + 2·Kp), Kp = K rounded up to 16.
+// Launched with programmatic stream serialization: the prologue (barriers,
+// TMEM, tensor-map prefetch) overlaps the end of the kernel before it, and
+// every thread waits for that kernel (griddepcontrol.wait) before touching
+// global memory.
 // Every mbarrier wait is bounded by %globaltimer; a role that gives up sets
 // the status word and the CTA's abort flag, copies and MMAs in flight are
 // waited for, TMEM is freed and the CTA ends.
