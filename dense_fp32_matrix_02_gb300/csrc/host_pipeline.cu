@@ -1,7 +1,8 @@
 // gemm_f32_host: C = A·B for matrices in host memory, with the copies to and
 // from the GPU overlapped with the multiply (see include/gemm_f32.h).
 //
-// Schedule on one device, for P row chunks of A and C:
+// Schedule on one device, for P row chunks of A and C (the first and last
+// small when M is large, see chunk_bounds):
 //   copy-in stream   B (whole) | A_0 | A_1 | ... | A_{P-1}
 //   caller's stream          wait B, A_c -> C_c = A_c·B   (one gemm per chunk)
 //   copy-out stream                        wait C_c -> C_c to the host
@@ -74,6 +75,49 @@ int chunk_count(int64_t M, int64_t N) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(p, M));
 }
 
+// First row of each chunk (bounds[c] .. bounds[c+1]); returns the count.
+// The pipeline's ends are serial: nothing is multiplied before B and the
+// first A chunk are in, and the last chunk's product and copy back follow
+// everything else.  So when M holds at least two waves of 128-row tiles
+// (a wave: two CTAs per SM), the first and last chunks are half a wave and
+// the chunks between at most one wave each, so that no chunk leaves a
+// nearly empty round of tiles behind; otherwise up to four equal chunks
+// that each still fill the GPU.
+int chunk_bounds(int64_t M, int64_t N, int sm_count, int64_t* bounds) {
+  const int64_t tiles_per_rb = (N + 127) / 128;  // tiles per 128 rows
+  const int64_t rbs = (M + 127) / 128;
+  const int64_t wave_rb =
+      std::max<int64_t>(1, 2 * (int64_t)sm_count / tiles_per_rb);
+  if (rbs >= 2 * wave_rb && wave_rb >= 2) {
+    const int64_t edge = wave_rb / 2;
+    const int64_t rest = rbs - 2 * edge;
+    int64_t n_mid = (rest + wave_rb - 1) / wave_rb;
+    n_mid = std::min<int64_t>(n_mid, kMaxChunks - 2);
+    const int64_t mid = (rest + n_mid - 1) / n_mid;
+    int n = 0;
+    int64_t rb = 0;
+    bounds[n++] = 0;
+    rb += edge;
+    bounds[n++] = rb * 128;
+    for (int64_t c = 0; c < n_mid; ++c) {
+      rb = std::min<int64_t>(rb + mid, rbs - edge);
+      if (rb * 128 > bounds[n - 1]) bounds[n++] = rb * 128;
+    }
+    bounds[n] = M;  // the last chunk: the final edge rows
+    return n;
+  }
+  const int chunks = chunk_count(M, N);
+  const int64_t rows = (M + chunks - 1) / chunks;
+  int n = 0;
+  for (int c = 0; c < chunks; ++c) {
+    const int64_t r0 = c * rows;
+    if (r0 >= M) break;
+    bounds[n++] = r0;
+  }
+  bounds[n] = M;
+  return n;
+}
+
 // rows × cols floats between a host matrix (row stride ld) and a dense
 // device block; one linear copy when the host rows are contiguous.
 cudaError_t copy_rows(float* dst, int64_t dst_ld, const float* src,
@@ -121,11 +165,16 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* hA,
         (e = cudaStreamWaitEvent(s, p.b_ready, 0)) != cudaSuccess)
       return gemm_f32_impl::record_cuda_error(e);
   }
-  const int chunks = chunk_count(M, N);
-  const int64_t rows = (M + chunks - 1) / chunks;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount,
+                                  dev)) != cudaSuccess)
+    return gemm_f32_impl::record_cuda_error(e);
+  int64_t bounds[kMaxChunks + 1];
+  const int chunks = chunk_bounds(M, N, sms, bounds);
   for (int c = 0; c < chunks; ++c) {
-    const int64_t r0 = c * rows, r1 = std::min<int64_t>(M, r0 + rows);
-    if (r0 >= r1) break;
+    const int64_t r0 = bounds[c], r1 = bounds[c + 1];
+    if (r0 >= r1) continue;
     if (K > 0) {
       if ((e = copy_rows(dA + r0 * K, K, hA + r0 * lda, lda, r1 - r0, K,
                          cudaMemcpyHostToDevice, p.in)) != cudaSuccess ||
