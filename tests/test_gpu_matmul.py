@@ -68,3 +68,31 @@ def test_matmul_rejects_other_layouts():
         G.matmul(x, torch.zeros(8, 8, device=DEV))
     with pytest.raises(ValueError):
         G.matmul(torch.zeros(4, 5, device=DEV), torch.zeros(6, 7, device=DEV))
+
+
+def test_matmul_transposed_a_on_a_side_stream():
+    """Aᵀ·B through a transposed copy in scratch the binding allocates: on
+    a stream other than the current one, repeated with fresh allocations in
+    between, every result stays right (the scratch is not handed out again
+    while the side stream may still use it)."""
+    M, N, K = 640, 512, 384
+    side = torch.cuda.Stream(DEV)
+    outs, wants = [], []
+    for i in range(4):
+        a, b = synth.make_operands(M, N, K, seed=60 + i, dist_a="normal")
+        at = _dev(a, True)
+        bt = _dev(b, False)
+        side.wait_stream(torch.cuda.current_stream(DEV))
+        with torch.cuda.stream(side):
+            c = torch.empty(M, N, device=DEV)
+        G.matmul(at, bt, out=c, stream=side)
+        # allocations on the current stream while the side stream runs
+        junk = torch.full((M * K,), float("nan"), device=DEV)
+        del junk
+        outs.append((c, a, b, at, bt))  # inputs stay alive until the end
+    side.synchronize()
+    for c, a, b, _, _ in outs:
+        want, bound, _ = oracle.gemm(a, b)
+        assert_within_tolerance(c.cpu().numpy(), want, bound, K,
+                                what="side-stream matmul")
+    assert G.device_status() == 0
