@@ -112,16 +112,17 @@ int choose_simt_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   return kSimtKm128x128x32Occ1;
 }
 
-int choose_tc_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
+int choose_tc_cfg(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {
   const int forced = env_int("GEMM_F32_TC_CFG", -1);
   if (forced >= 0 && forced < kTcCfgCount) return forced;
-  (void)M;
-  (void)N;
-  (void)d;
-  // 128 x 128 tiles at two CTAs per SM beat 256 x 128 at one on every
-  // measured shape (finer scheduling grain, one CTA's epilogue overlapping
-  // the other's main loop); letting the tensor core truncate the raw
-  // operands to TF32 halves the converters' work.
+  // Both let the tensor core truncate the raw operands to TF32 (half the
+  // converters' work).  256 x 128 tiles at one CTA per SM convert each B
+  // tile for twice the MMAs and win by 3-18 % once K >= 2048 and there is
+  // at least a full wave of them (4096^3: 341 against 310 TFLOP/s); below
+  // that, 128 x 128 tiles at two CTAs per SM (finer grain, one CTA's
+  // epilogue overlapping the other's main loop, split-K for small grids).
+  const int64_t tiles256 = ((M + 255) / 256) * ((N + 127) / 128);
+  if (K >= 2048 && tiles256 >= d.sm_count) return kTc256Raw;
   return kTc128Raw;
 }
 
@@ -171,7 +172,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   plan->vec = vec;
   plan->c_vec = aligned16(C) && ldc % 4 == 0;
   plan->simt_cfg = choose_simt_cfg(M, N, d);
-  plan->tc_cfg = choose_tc_cfg(M, N, d);
+  plan->tc_cfg = choose_tc_cfg(M, N, K, d);
   plan->splits = 1;
   plan->full_tiles = 0;
   plan->tc_stream = false;
@@ -573,7 +574,7 @@ int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const float* A,
 
 int gemm_f32_plan(int64_t M, int64_t N, int64_t K, const float* A,
                   int64_t lda, const float* B, int64_t ldb, const float* C,
-                  int64_t ldc, int64_t out[4]) {
+                  int64_t ldc, int64_t out[5]) {
   if (!out) return GEMM_F32_ERR_INVALID_ARG;
   int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM_F32_OK) return st;
@@ -588,6 +589,9 @@ int gemm_f32_plan(int64_t M, int64_t N, int64_t K, const float* A,
   out[1] = plan.tc_stream ? 1 : 0;
   out[2] = plan.splits;
   out[3] = plan.full_tiles;
+  out[4] = plan.algo != GEMM_F32_ALGO_TF32X3 ? 0
+           : plan.tc_stream                   ? 128
+                                              : tf32x3_tile_m(plan.tc_cfg);
   return GEMM_F32_OK;
 }
 

@@ -466,10 +466,11 @@ def plan(M, N, K, a_ptr=16, lda=None, b_ptr=16, ldb=None, c_ptr=16,
     """The automatic plan for these sizes (default: 16-byte aligned
     pointers, leading dimensions = the row widths rounded up to multiples
     of 4, the layouts the tensor kernels take): kernel family, tensor
-    variant ("tiled" / "streaming"), split-K ways, whole tiles."""
+    variant ("tiled" / "streaming"), split-K ways, whole tiles, rows of C
+    per tensor tile (0 for the FFMA kernels)."""
     def pad4(x):
         return max((int(x) + 3) // 4 * 4, 4)
-    out = (ctypes.c_int64 * 4)()
+    out = (ctypes.c_int64 * 5)()
     _check(lib().gemm_f32_plan(int(M), int(N), int(K), a_ptr or None,
                                int(lda if lda is not None else pad4(K)),
                                b_ptr or None,
@@ -478,7 +479,7 @@ def plan(M, N, K, a_ptr=16, lda=None, b_ptr=16, ldb=None, c_ptr=16,
                                int(ldc if ldc is not None else pad4(N)),
                                out), "gemm_f32_plan")
     return {"algo": out[0], "variant": "streaming" if out[1] else "tiled",
-            "splits": out[2], "whole_tiles": out[3]}
+            "splits": out[2], "whole_tiles": out[3], "tile_rows": out[4]}
 
 
 def select_algo(M, N, K, a_ptr=0, lda=None, b_ptr=0, ldb=None, c_ptr=0,

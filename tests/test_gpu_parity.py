@@ -439,7 +439,8 @@ def test_plan_reports_the_streaming_kernel():
     for M, N, K in _stream_shapes():
         assert G.plan(M, N, K) == {"algo": G.ALGO_TF32X3,
                                    "variant": "streaming", "splits": 1,
-                                   "whole_tiles": 0}, (M, N, K)
+                                   "whole_tiles": 0, "tile_rows": 128}, \
+            (M, N, K)
     for M, N, K in [(r - 128, 64, 64), (r, 129, 64), (r, 64, 129),
                     (4096, 4096, 4096)]:
         assert G.plan(M, N, K)["variant"] == "tiled", (M, N, K)
@@ -521,16 +522,28 @@ def _slots():
 
 
 def test_workspace_size_policy():
-    """Scratch = split tiles × splits × one 128 × 128 fp32 partial tile."""
+    """Scratch = split tiles × splits × one TILE_M × 128 fp32 partial
+    tile; TILE_M = 256 (one CTA per SM) for K >= 2048 with a 256-row tile
+    for every SM, else 128 (two CTAs per SM)."""
     slots = _slots()
+    sms = slots // 2
     tile = 128 * 128 * 4
     # few tiles: all split, slots // tiles ways (at least 8 k stages each)
+    assert G.plan(1024, 1024, 1024)["tile_rows"] == 128
     assert G.workspace_size(1024, 1024, 1024) == 64 * min(slots // 64, 8) * tile
-    # a partly filled last round: its tiles split slots // tail ways
-    tail = 1024 % slots
-    s = min(slots // tail, 4096 // 16 // 8, 16)
-    assert G.workspace_size(4096, 4096, 4096) == (tail * s * tile
+    # a partly filled last round of 256 x 128 tiles: its tiles split
+    # sms // tail ways
+    p = G.plan(4096, 4096, 4096)
+    assert p["tile_rows"] == 256
+    tail = 512 % sms
+    s = min(sms // tail, 4096 // 16 // 8, 16)
+    assert G.workspace_size(4096, 4096, 4096) == (tail * s * 2 * tile
                                                   if s > 1 else 0)
+    assert p["splits"] == (s if s > 1 else 1)
+    assert p["whole_tiles"] == (512 - tail if s > 1 else 0)
+    # K below 2048, or fewer 256-row tiles than SMs: 128-row tiles
+    assert G.plan(4096, 4096, 1024)["tile_rows"] == 128
+    assert G.plan(1024, 4096, 4096)["tile_rows"] == 128
     # whole rounds: nothing to split
     assert G.workspace_size(128 * (slots // 19), 128 * 19, 4096) == 0
     assert G.workspace_size(64, 64, 64) == 0               # K too short
