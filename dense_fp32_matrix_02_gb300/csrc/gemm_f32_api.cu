@@ -455,7 +455,16 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
     wc.limit = g_wait_ns.load();
     wc.debug = g_debug_flags.load();
     wc.status = d->status;
-    e = launch_tf32x3(q, kTc128Raw, 0, 1, nullptr, wc, s);
+    // the same tile choice as single products, over all the batch's tiles
+    int cfg = kTc128Raw;
+    const int forced = env_int("GEMM_F32_TC_CFG", -1);
+    if (forced == kTc128Raw || forced == kTc256Raw)
+      cfg = forced;
+    else if (forced < 0 && K >= 2048 && !q.transA &&
+             ((int64_t)(q.M + 255) / 256) * ((q.N + 127) / 128) * batch >=
+                 d->sm_count)
+      cfg = kTc256Raw;
+    e = launch_tf32x3(q, cfg, 0, 1, nullptr, wc, s);
   } else {
     e = launch_simt(p, choose_simt_cfg(M, N, *d), vec, c_vec, s);
   }

@@ -81,9 +81,10 @@ long long tf32x3_partials_bytes(int tile_m, long long split_tiles,
 // 3xTF32 tcgen05 kernel.  Needs A, B 16-byte aligned, lda and ldb multiples
 // of 4, K >= 1 and an sm_100-family device.  Batched problems (p.batch > 1,
 // strides multiples of 4 and either 0 or at least one whole matrix) and,
-// with configuration kTc128Raw, one of p.transB (B stored N×K), p.transA
-// (A stored K×M) or p.storeT (C stored transposed: the caller swapped the
-// operands, op(A)ᵀ·op(B)ᵀ computed as B·A).  With splits > 1 and a
+// with configuration kTc128Raw or kTc256Raw, one of p.transB (B stored
+// N×K), p.transA (A stored K×M; always 128-row tiles) or p.storeT (C stored
+// transposed: the caller swapped the operands, op(A)ᵀ·op(B)ᵀ computed as
+// B·A).  With splits > 1 and a
 // `partials` buffer of tf32x3_partials_bytes for the tiles past the first
 // full_tiles (grouped order), each of those tiles' K range is split over
 // `splits` CTAs and a second kernel sums the partial tiles into C in split

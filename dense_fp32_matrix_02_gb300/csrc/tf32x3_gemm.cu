@@ -788,6 +788,15 @@ cudaError_t launch_tf32x3(const Problem& p, int cfg, int full_tiles,
       return launch_cfg<Cfg<128, 4, true>>(p, full_tiles, splits, partials,
                                            wc, stream);
     case kTc256Raw:
+      if (p.transB)
+        return launch_cfg<Cfg<256, 5, true, true>>(p, full_tiles, splits,
+                                                   partials, wc, stream);
+      if (p.storeT)
+        return launch_cfg<Cfg<256, 5, true, false, true>>(
+            p, full_tiles, splits, partials, wc, stream);
+      if (p.transA)  // the transposed-A staging exists for 128-row tiles
+        return launch_tf32x3(p, kTc128Raw, full_tiles, splits, partials, wc,
+                             stream);
       return launch_cfg<Cfg<256, 5, true>>(p, full_tiles, splits, partials,
                                            wc, stream);
     default:

@@ -831,6 +831,30 @@ def test_batched_forms_with_workspace(form, ws, shape, batch, gap):
     assert G.device_status() == 0
 
 
+@pytest.mark.parametrize("form", ["NN", "NT", "TT", "TN"])
+@pytest.mark.parametrize("shape,batch,gap", [((300, 260, 77), 3, 0),
+                                             ((257, 384, 513), 2, 4)])
+def test_batched_forms_256_row_tiles(form, shape, batch, gap):
+    """The 256 × 128 tile configurations of every form (forced; the
+    automatic choice takes them for K >= 2048 with a tile per SM): ragged
+    edges, padding and gaps untouched, integers exact."""
+    M, N, K = shape
+    with _env("GEMM_F32_TC_CFG", 3):
+        As, Bs, Cs, host, sC, ldc = _batched_case(form, M, N, K, batch,
+                                                  seed=M + 3, gap=gap)
+        Ai, Bi, Ci, _, _, _ = _batched_case(form, M, N, K, batch, seed=K + 3,
+                                            gap=gap, dist="int")
+    for i in range(batch):
+        check_full(As[i], Bs[i], Cs[i][:, :N], what=f"{form} 256 b{i}")
+        assert (Cs[i][:, N:] == -7.0).all()
+        check_full(Ai[i], Bi[i], Ci[i][:, :N], exact=True,
+                   what=f"{form} 256 b{i} int")
+    if gap:
+        for i in range(batch):
+            assert (host[i * sC + M * ldc:(i + 1) * sC] == -7.0).all()
+    assert G.device_status() == 0
+
+
 def test_tn_workspace_shared_a():
     """Aᵀ·B with strideA = 0: one transposed copy serves every product."""
     As, Bs, Cs, _, _, _ = _batched_case("TN", 300, 200, 136, 4, seed=3,
@@ -891,11 +915,15 @@ def test_batched_forms_forced_simt(form):
         check_full(As[i], Bs[i], Cs[i][:, :260], what=f"simt {form} b{i}")
 
 
-@pytest.mark.parametrize("form,ws", [("NT", None), ("TT", None),
-                                     ("TN", None), ("TN", "full")])
-def test_transposed_forms_large_sampled(form, ws):
-    """op forms at 2048 x 1536 x 1024, sampled against the oracle."""
-    M, N, K = 2048, 1536, 1024
+@pytest.mark.parametrize("form,ws,shape", [
+    ("NT", None, (2048, 1536, 1024)), ("TT", None, (2048, 1536, 1024)),
+    ("TN", None, (2048, 1536, 1024)), ("TN", "full", (2048, 1536, 1024)),
+    # K >= 2048 and a 256-row tile per SM: the 256 × 128 configurations
+    ("NT", None, (2560, 2048, 2048)), ("TT", None, (2048, 2560, 2048)),
+    ("TN", "full", (2560, 2048, 2048))])
+def test_transposed_forms_large_sampled(form, ws, shape):
+    """op forms on large shapes, sampled against the oracle."""
+    M, N, K = shape
     As, Bs, Cs, _, _, _ = _batched_case(form, M, N, K, 1, seed=5, ws=ws)
     check_sampled_and_rowsums(As[0], Bs[0], np.ascontiguousarray(Cs[0][:, :N]),
                               what=f"{form} large")
