@@ -117,13 +117,14 @@ int choose_tc_cfg(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {
   if (forced >= 0 && forced < kTcCfgCount) return forced;
   // Both let the tensor core truncate the raw operands to TF32 (half the
   // converters' work).  256 x 128 tiles at one CTA per SM convert each B
-  // tile for twice the MMAs and win by 3-18 % once K >= 2048 and there is
-  // at least a full wave of them (4096^3: 341 against 310 TFLOP/s); below
-  // that, 128 x 128 tiles at two CTAs per SM (finer grain, one CTA's
-  // epilogue overlapping the other's main loop, split-K for small grids).
-  const int64_t tiles256 = ((M + 255) / 256) * ((N + 127) / 128);
-  if (K >= 2048 && tiles256 >= d.sm_count) return kTc256Raw;
-  return kTc128Raw;
+  // tile for twice the MMAs and won on every measured shape with K >= 2048
+  // (by 2-18 %, from 32 such tiles up to 8192^3; 4096^3: 341 against 310
+  // TFLOP/s); for shorter K, 128 x 128 tiles at two CTAs per SM (finer
+  // grain, one CTA's epilogue overlapping the other's main loop).
+  (void)M;
+  (void)N;
+  (void)d;
+  return K >= 2048 ? kTc256Raw : kTc128Raw;
 }
 
 // Split-K for the tensor path, so that the CTAs fill the GPU:
@@ -455,14 +456,12 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
     wc.limit = g_wait_ns.load();
     wc.debug = g_debug_flags.load();
     wc.status = d->status;
-    // the same tile choice as single products, over all the batch's tiles
+    // the same tile choice as single products
     int cfg = kTc128Raw;
     const int forced = env_int("GEMM_F32_TC_CFG", -1);
     if (forced == kTc128Raw || forced == kTc256Raw)
       cfg = forced;
-    else if (forced < 0 && K >= 2048 && !q.transA &&
-             ((int64_t)(q.M + 255) / 256) * ((q.N + 127) / 128) * batch >=
-                 d->sm_count)
+    else if (forced < 0 && K >= 2048 && !q.transA)
       cfg = kTc256Raw;
     e = launch_tf32x3(q, cfg, 0, 1, nullptr, wc, s);
   } else {

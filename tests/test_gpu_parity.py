@@ -523,8 +523,8 @@ def _slots():
 
 def test_workspace_size_policy():
     """Scratch = split tiles × splits × one TILE_M × 128 fp32 partial
-    tile; TILE_M = 256 (one CTA per SM) for K >= 2048 with a 256-row tile
-    for every SM, else 128 (two CTAs per SM)."""
+    tile; TILE_M = 256 (one CTA per SM) for K >= 2048, else 128 (two CTAs
+    per SM)."""
     slots = _slots()
     sms = slots // 2
     tile = 128 * 128 * 4
@@ -541,9 +541,13 @@ def test_workspace_size_policy():
                                                   if s > 1 else 0)
     assert p["splits"] == (s if s > 1 else 1)
     assert p["whole_tiles"] == (512 - tail if s > 1 else 0)
-    # K below 2048, or fewer 256-row tiles than SMs: 128-row tiles
+    # K below 2048: 128-row tiles; few 256-row tiles are split over K
     assert G.plan(4096, 4096, 1024)["tile_rows"] == 128
-    assert G.plan(1024, 4096, 4096)["tile_rows"] == 128
+    assert G.plan(4096, 4096, 2047)["tile_rows"] == 128
+    p = G.plan(1024, 1024, 4096)
+    assert p["tile_rows"] == 256
+    assert p["splits"] == min(sms // 32, 4096 // 16 // 8, 16)
+    assert G.workspace_size(1024, 1024, 4096) == 32 * p["splits"] * 2 * tile
     # whole rounds: nothing to split
     assert G.workspace_size(128 * (slots // 19), 128 * 19, 4096) == 0
     assert G.workspace_size(64, 64, 64) == 0               # K too short
