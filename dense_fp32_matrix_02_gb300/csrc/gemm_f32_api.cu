@@ -654,6 +654,26 @@ unsigned int gemm_f32_set_debug_flags(unsigned int flags) {
 }
 
 // ------------------------------------------------ mixed precision (16-bit)
+}  // extern "C"
+
+namespace {
+
+// Rows per 16-bit tile: 256 (two M = 128 MMAs per k-step sharing each B
+// stage, one accumulator filling TMEM) when K >= 2048 and there is a
+// 256 × 256 tile for every SM (4096^3 bf16: 1548 against 1378 TFLOP/s);
+// else 128 (two accumulators, so one tile's epilogue overlaps the next
+// tile's MMAs: ahead on few tiles and short K).  GEMM_F32_MIXED_BM=128 or
+// 256 forces it.
+int mixed_tile_rows(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {
+  const int forced = env_int("GEMM_F32_MIXED_BM", 0);
+  if (forced == 128 || forced == 256) return forced;
+  const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256);
+  return (K >= 2048 && N > 128 && tiles256 >= d.sm_count) ? 256 : 128;
+}
+
+}  // namespace
+
+extern "C" {
 
 int64_t gemm_f32_mixed_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return -GEMM_F32_ERR_INVALID_ARG;
@@ -720,23 +740,26 @@ int gemm_f32_mixed16(int type, int64_t M, int64_t N, int64_t K,
   wc.debug = g_debug_flags.load();
   wc.status = d->status;
   const gemm_f32_impl::Plan16 plan = gemm_f32_impl::plan_mixed16(
-      M, N, d->sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0);
+      M, N, d->sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0,
+      mixed_tile_rows(M, N, K, *d));
   e = gemm_f32_impl::launch_mixed16(p, plan, aligned16(C) && ldc % 4 == 0,
                                     wc, s);
   return e == cudaSuccess ? GEMM_F32_OK : fail_cuda(e);
 }
 
-int gemm_f32_mixed_plan(int64_t M, int64_t N, int64_t out[4]) {
-  if (M < 1 || N < 1 || !out) return GEMM_F32_ERR_INVALID_ARG;
+int gemm_f32_mixed_plan(int64_t M, int64_t N, int64_t K, int64_t out[5]) {
+  if (M < 1 || N < 1 || K < 0 || !out) return GEMM_F32_ERR_INVALID_ARG;
   const DeviceInfo* d = nullptr;
   cudaError_t e = device_info(&d);
   if (e != cudaSuccess) return fail_cuda(e);
   const gemm_f32_impl::Plan16 plan = gemm_f32_impl::plan_mixed16(
-      M, N, d->sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0);
+      M, N, d->sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0,
+      mixed_tile_rows(M, N, K, *d));
   out[0] = plan.wn;
   out[1] = plan.full;
   out[2] = plan.parts;
   out[3] = plan.grid;
+  out[4] = plan.bm;
   return GEMM_F32_OK;
 }
 

@@ -147,6 +147,7 @@ struct Problem16 {
 // columns, so that the last round spreads over the GPU instead of leaving
 // most SMs idle while one tile per busy SM runs its whole length.
 struct Plan16 {
+  int bm;  // rows per tile: 128, or 256 (two MMAs of M = 128 per k-step)
   int wn;
   long long tiles_m, tiles_n;
   long long full;  // whole tiles; the rest are split
@@ -156,7 +157,8 @@ struct Plan16 {
 };
 
 // narrow = false keeps every tile whole and 256 wide.
-Plan16 plan_mixed16(long long M, long long N, int sm_count, bool narrow);
+Plan16 plan_mixed16(long long M, long long N, int sm_count, bool narrow,
+                    int bm = 128);
 
 // tcgen05 kind::f16 kernel, persistent over plan.grid CTAs.
 // Needs A, B 16-byte aligned, lda and ldb multiples of 8, K >= 1.

@@ -49,34 +49,44 @@
 namespace gemm_f32_impl {
 namespace mixed16 {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;  // kBK: 128-byte rows
-constexpr int kStages = 4;
+constexpr int kBN = 256, kBK = 64;  // kBK: 128-byte rows
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
-constexpr int kStageBytesA = kBM * kBK * 2;    // 16 KB
 constexpr int kBoxBytesB = 64 * kBK * 2;       // 8 KB: 64 n × 64 k
 constexpr int kStageBytesB = kBN * kBK * 2;    // 32 KB
-constexpr int kOffB = kStages * kStageBytesA;
 constexpr int kStagingBytes = 32 * 32 * 4;     // one warp's 32×32 fp32 block
-constexpr int kOffStaging = kOffB + kStages * kStageBytesB;
-constexpr int kOffCtl = kOffStaging + kEpiWarps * kStagingBytes;
-constexpr int kAccCols = kBN;                  // fp32 columns per accumulator
-constexpr int kTmemCols = 2 * kAccCols;        // 512: the whole TMEM
+constexpr int kTmemCols = 512;                 // the whole TMEM
 constexpr long long kDrainNs = 2000000000LL;
 constexpr uint32_t kSleepNs = 100000;
 
-struct __align__(8) Control {
-  uint64_t full[kStages];   // TMA -> MMA (transaction bytes)
-  uint64_t empty[kStages];  // MMA completion -> producer
-  uint64_t acc_full[2];     // last MMA of a tile -> epilogue
-  uint64_t acc_empty[2];    // epilogue warps -> MMA (one arrival per warp)
-  uint64_t mma_done;        // every MMA issued has completed
-  uint32_t tmem_base;
-  int abort;
+// Tile rows BM: 128 (4 stages of 48 KB; two 128 × 256 accumulators, so
+// one tile accumulates while the other is stored) or 256 (3 stages of
+// 64 KB; two MMAs of M = 128 per k-step into the halves of one 256 × 256
+// accumulator that fills TMEM: each B stage feeds twice the MMAs).
+template <int BM>
+struct Shape {
+  static constexpr int kBM = BM;
+  static constexpr int kStages = BM == 128 ? 4 : 3;
+  static constexpr int kStageBytesA = BM * kBK * 2;  // 16 or 32 KB
+  static constexpr int kOffB = kStages * kStageBytesA;
+  static constexpr int kOffStaging = kOffB + kStages * kStageBytesB;
+  static constexpr int kOffCtl = kOffStaging + kEpiWarps * kStagingBytes;
+  static constexpr int kHalves = BM / 128;         // M = 128 MMAs per k-step
+  static constexpr int kBufs = BM == 128 ? 2 : 1;  // accumulators
+  static constexpr int kAccCols = 256 * kHalves;   // TMEM columns of one
+  struct __align__(8) Control {
+    uint64_t full[kStages];   // TMA -> MMA (transaction bytes)
+    uint64_t empty[kStages];  // MMA completion -> producer
+    uint64_t acc_full[2];     // last MMA of a tile -> epilogue
+    uint64_t acc_empty[2];    // epilogue warps -> MMA (one arrival per warp)
+    uint64_t mma_done;        // every MMA issued has completed
+    uint32_t tmem_base;
+    int abort;
+  };
+  static constexpr int kSmemBytes = kOffCtl + (int)sizeof(Control) + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kBufs * kAccCols <= kTmemCols, "TMEM budget");
 };
-
-constexpr int kSmemBytes = kOffCtl + (int)sizeof(Control) + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // sleep: the epilogue warps, idle while a tile accumulates; the producer
 // and the MMA issuer poll.
@@ -106,7 +116,7 @@ __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int tiles_n,
 }
 
 // ab_type: 0 binary16, 1 bfloat16 (the kind::f16 operand format code).
-template <int AB_TYPE>
+template <int AB_TYPE, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     mixed16_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
@@ -116,6 +126,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    int c_mode, WaitCfg wc) {
   // c_mode: 2 = TMA stores through staging, 1 = direct 16-byte stores,
   // 0 = direct scalar stores
+  using Sh = Shape<BM>;
+  constexpr int kBM = Sh::kBM, kStages = Sh::kStages;
+  constexpr int kStageBytesA = Sh::kStageBytesA, kOffB = Sh::kOffB;
+  constexpr int kOffStaging = Sh::kOffStaging, kOffCtl = Sh::kOffCtl;
+  constexpr int kHalves = Sh::kHalves, kBufs = Sh::kBufs;
+  constexpr int kAccCols = Sh::kAccCols;
+  using Control = typename Sh::Control;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kBufs; ++b) {
       mbar_init(acc_full(b), 1);
       mbar_init(acc_empty(b), kEpiWarps);
     }
@@ -201,12 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x, i = 0; ok && u < units; u += gridDim.x, ++i) {
-        const int b = i & 1;
+        const int b = i % kBufs;
         const uint32_t idesc = idesc_f16(
-            kBM, unit_of(u, tiles_m, tiles_n, wn, whole, parts).width,
+            128, unit_of(u, tiles_m, tiles_n, wn, whole, parts).width,
             AB_TYPE, true);
-        if (i >= 2 && !wait_phase(acc_empty(b), ((i >> 1) - 1) & 1, wc.limit,
-                                  abort, false)) {
+        if (i >= kBufs &&
+            !wait_phase(acc_empty(b), ((i / kBufs) - 1) & 1, wc.limit, abort,
+                        false)) {
           *abort = 1;
           record_status(wc.status, kStatusTimeoutMma);
           break;
@@ -227,11 +245,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = sbase + kOffB + s * kStageBytesB;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // A: 16 k = 32 bytes along the swizzled row; B: 16 k rows
-            const uint64_t ad = smem_desc_sw128(a0 + 32 * kk, 16, 1024);
+            // A: 16 k = 32 bytes along the swizzled row (rows 128·hm..
+            // from 16 KB·hm); B: 16 k rows
             const uint64_t bd =
                 smem_desc_sw128(b0 + 2048 * kk, kBoxBytesB, 1024);
-            mma_f16_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+#pragma unroll
+            for (int hm = 0; hm < kHalves; ++hm) {
+              const uint64_t ad =
+                  smem_desc_sw128(a0 + hm * 16384 + 32 * kk, 16, 1024);
+              mma_f16_ss(d_tmem + hm * 256, ad, bd, idesc, (kb | kk) != 0);
+            }
           }
           tc_commit(empty(s));
         }
@@ -252,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* stg = smem + kOffStaging + (warp - 2) * kStagingBytes;
     const uint32_t stg_s = sbase + kOffStaging + (warp - 2) * kStagingBytes;
     for (int u = blockIdx.x, i = 0; u < units; u += gridDim.x, ++i) {
-      const int b = i & 1;
+      const int b = i % kBufs;
       const bool ok =
-          wait_phase(acc_full(b), (i >> 1) & 1, wc.limit, abort, true);
+          wait_phase(acc_full(b), (i / kBufs) & 1, wc.limit, abort, true);
       if (!__all_sync(0xffffffffu, ok)) {
         *abort = 1;
         if (lane == 0) record_status(wc.status, kStatusTimeoutMma);
@@ -263,16 +286,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const Unit w = unit_of(u, tiles_m, tiles_n, wn, whole, parts);
       const int half = w.width / 2;  // 32, 64 or 128 columns per warp
-      const int m0 = w.tm * kBM + q * 32;
-      const int m = m0 + lane;
       const int n0 = w.n0 + h * half;
-      float* crow = C + (long long)m * ldc;
+#pragma unroll 1
+      for (int hm = 0; hm < kHalves; ++hm)
 #pragma unroll 1
       for (int c0 = 0; c0 < half; c0 += 32) {
+        const int m0 = w.tm * kBM + hm * 128 + q * 32;
+        const int m = m0 + lane;
+        float* crow = C + (long long)m * ldc;
         uint32_t v[32];
-        tmem_ld32(tmem + lane_bits + b * kAccCols + h * half + c0, v);
+        tmem_ld32(tmem + lane_bits + b * kAccCols + hm * 256 + h * half + c0,
+                  v);
         tmem_ld_wait();
-        if (c0 + 32 == half) {
+        if (hm == kHalves - 1 && c0 + 32 == half) {
           // all of this warp's part of the accumulator is in registers
           tc_fence_before_sync();
           __syncwarp();
@@ -404,10 +430,12 @@ bool encode_16(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
 
 }  // namespace mixed16
 
-Plan16 plan_mixed16(long long M, long long N, int sm_count, bool narrow) {
+Plan16 plan_mixed16(long long M, long long N, int sm_count, bool narrow,
+                    int bm) {
   Plan16 p;
+  p.bm = bm == 256 ? 256 : 128;
   p.wn = (!narrow || N > 128) ? 256 : (N > 64 ? 128 : 64);
-  p.tiles_m = (M + 127) / 128;
+  p.tiles_m = (M + p.bm - 1) / p.bm;
   p.tiles_n = (N + p.wn - 1) / p.wn;
   const long long total = p.tiles_m * p.tiles_n;
   const long long g = sm_count > 0 ? sm_count : 1;
@@ -430,13 +458,17 @@ Plan16 plan_mixed16(long long M, long long N, int sm_count, bool narrow) {
   return p;
 }
 
-cudaError_t launch_mixed16(const Problem16& p, const Plan16& plan, bool c_vec,
-                           const WaitCfg& wc, cudaStream_t stream) {
+namespace {
+
+template <int BM>
+cudaError_t launch_bm(const Problem16& p, const Plan16& plan, bool c_vec,
+                      const WaitCfg& wc, cudaStream_t stream) {
   using namespace mixed16;
+  using Sh = Shape<BM>;
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
-  if (!encode_16(encode, &ta, p.type, p.A, p.K, p.M, p.lda, kBM) ||
+  if (!encode_16(encode, &ta, p.type, p.A, p.K, p.M, p.lda, BM) ||
       !encode_16(encode, &tb, p.type, p.B, p.N, p.K, p.ldb, kBK))
     return cudaErrorInvalidValue;
   // C: fp32 M×N, 32×32 boxes in the 128-byte swizzle (rows of 128 bytes)
@@ -454,22 +486,31 @@ cudaError_t launch_mixed16(const Problem16& p, const Plan16& plan, bool c_vec,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       c_mode = 2;
   }
-  auto fn = p.type == GEMM_F32_MIXED_BF16 ? mixed16_kernel<1>
-                                          : mixed16_kernel<0>;
+  auto fn = p.type == GEMM_F32_MIXED_BF16 ? mixed16_kernel<1, BM>
+                                          : mixed16_kernel<0, BM>;
   cudaError_t e =
-      ensure_smem_attr(reinterpret_cast<const void*>(fn), kSmemBytes);
+      ensure_smem_attr(reinterpret_cast<const void*>(fn), Sh::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (plan.units > 0x7fffffffLL || plan.units < 1 || plan.grid < 1 ||
       (plan.wn != 64 && plan.wn != 128 && plan.wn != 256) ||
       (plan.parts != 1 && plan.parts != 2 && plan.parts != 4) ||
       plan.wn / plan.parts < 64 ||
-      plan.tiles_m != (p.M + kBM - 1) / kBM ||
+      plan.bm != BM || plan.tiles_m != (p.M + BM - 1) / BM ||
       plan.tiles_n != (p.N + plan.wn - 1) / plan.wn)
     return cudaErrorInvalidConfiguration;
-  return launch_pdl(fn, dim3(plan.grid), dim3(kThreads), kSmemBytes, stream,
+  return launch_pdl(fn, dim3(plan.grid), dim3(kThreads), Sh::kSmemBytes,
+                    stream,
                     ta, tb, tc, p.C, p.ldc, p.M, p.N, p.K, (int)plan.tiles_m,
                     (int)plan.tiles_n, plan.wn, (int)plan.full, plan.parts,
                     (int)plan.units, c_mode, wc);
+}
+
+}  // namespace
+
+cudaError_t launch_mixed16(const Problem16& p, const Plan16& plan, bool c_vec,
+                           const WaitCfg& wc, cudaStream_t stream) {
+  return plan.bm == 256 ? launch_bm<256>(p, plan, c_vec, wc, stream)
+                        : launch_bm<128>(p, plan, c_vec, wc, stream);
 }
 
 cudaError_t launch_round16(int type, long long rows, long long cols,

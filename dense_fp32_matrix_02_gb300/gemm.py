@@ -105,7 +105,7 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_mixed_workspace_size.restype = i64
         L.gemm_f32_mixed_workspace_size.argtypes = [i64, i64, i64]
         L.gemm_f32_mixed_plan.restype = ci
-        L.gemm_f32_mixed_plan.argtypes = [i64, i64, ctypes.POINTER(i64)]
+        L.gemm_f32_mixed_plan.argtypes = [i64, i64, i64, ctypes.POINTER(i64)]
         _lib = L
         return L
 
@@ -605,12 +605,15 @@ def mixed_workspace_size(M, N, K) -> int:
     return n
 
 
-def mixed_plan(M, N) -> dict:
-    """How the 16-bit product cuts an M×N result on the current device:
-    tile width, tiles run whole, strips per remaining tile, CTAs."""
-    out = (ctypes.c_int64 * 4)()
-    _check(lib().gemm_f32_mixed_plan(int(M), int(N), out), "gemm_f32_mixed_plan")
-    return {"width": out[0], "whole": out[1], "parts": out[2], "grid": out[3]}
+def mixed_plan(M, N, K=0) -> dict:
+    """How the 16-bit product cuts an M×N×K product on the current device:
+    tile width, tiles run whole, strips per remaining tile, CTAs, tile
+    rows."""
+    out = (ctypes.c_int64 * 5)()
+    _check(lib().gemm_f32_mixed_plan(int(M), int(N), int(K), out),
+           "gemm_f32_mixed_plan")
+    return {"width": out[0], "whole": out[1], "parts": out[2], "grid": out[3],
+            "rows": out[4]}
 
 
 def gemm_f32_mixed_ptr(type_, M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,

@@ -246,18 +246,21 @@ GEMM_F32_API int64_t gemm_f32_mixed_workspace_size(int64_t M, int64_t N,
                                                    int64_t K);
 
 /*
- * How gemm_f32_mixed16 (and gemm_f32_mixed) cut an M×N product on the
+ * How gemm_f32_mixed16 (and gemm_f32_mixed) cut an M×N×K product on the
  * current device, for tests and tuning.  out[0]: tile width in columns
  * (256, or 128 / 64 when N is at most that); out[1]: tiles run whole;
  * out[2]: column strips each remaining tile is cut into (1, 2 or 4: the
  * tiles of the last, partly filled round of the persistent grid, or all of
- * them when there are fewer tiles than SMs); out[3]: persistent CTAs.
- * Every unit runs the whole K.  Setting the environment variable
- * GEMM_F32_MIXED_NARROW=0 keeps every tile whole and 256 wide.  Returns
- * GEMM_F32_OK, GEMM_F32_ERR_INVALID_ARG (M or N < 1, out NULL) or
+ * them when there are fewer tiles than SMs); out[3]: persistent CTAs;
+ * out[4]: tile rows (256 when K >= 2048, N > 128 and there is a 256 × 256
+ * tile for every SM, else 128).  Every unit runs the whole K.  The
+ * environment variable GEMM_F32_MIXED_NARROW=0 keeps every tile whole and
+ * 256 wide; GEMM_F32_MIXED_BM=128 or 256 forces the tile rows.  Returns
+ * GEMM_F32_OK, GEMM_F32_ERR_INVALID_ARG (M or N < 1, K < 0, out NULL) or
  * GEMM_F32_ERR_CUDA.
  */
-GEMM_F32_API int gemm_f32_mixed_plan(int64_t M, int64_t N, int64_t out[4]);
+GEMM_F32_API int gemm_f32_mixed_plan(int64_t M, int64_t N, int64_t K,
+                                     int64_t out[5]);
 
 /*
  * FP32 FMA throughput probe (measurement, not part of any product): launches

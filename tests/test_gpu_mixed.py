@@ -217,6 +217,38 @@ def _split_cases():
     ]
 
 
+def test_mixed_tile_rows_rule():
+    """256-row tiles for K >= 2048, N > 128 and a 256 × 256 tile per SM."""
+    g = _sms()
+    assert G.mixed_plan(4096, 4096, 4096)["rows"] == 256
+    assert G.mixed_plan(4096, 4096, 1024)["rows"] == 128
+    assert G.mixed_plan(1024, 1024, 4096)["rows"] == 128      # 16 tiles
+    assert G.mixed_plan(65536, 64, 4096)["rows"] == 128       # narrow N
+    p = G.mixed_plan(256 * g, 256, 2048)                       # one wave
+    assert p["rows"] == 256 and p["whole"] == g and p["parts"] == 1
+
+
+@pytest.mark.parametrize("t", TYPES, ids=TYPE_IDS)
+@pytest.mark.parametrize("shape", [(300, 520, 136), (600, 1000, 2064),
+                                   (257, 255, 1000), (1000, 100, 200)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_mixed16_256_row_tiles_exact(t, shape, monkeypatch):
+    """The 256-row tiles (two MMAs of M = 128 per k-step into one
+    accumulator that fills TMEM), forced: ragged rows and columns, strips
+    and narrow tiles, integers bit for bit; normal operands within the
+    tolerance."""
+    monkeypatch.setenv("GEMM_F32_MIXED_BM", "256")
+    M, N, K = shape
+    assert G.mixed_plan(M, N, K)["rows"] == 256
+    a, b = synth.make_operands(M, N, K, seed=M + 1, dist_a="int8")
+    want, _, _ = oracle.gemm_mixed(a, b, t)
+    assert_bitexact(run_mixed16(a, b, t), want, what=f"mixed16 256 {shape}")
+    a, b = synth.make_operands(M, N, K, seed=M + 2, dist_a="normal")
+    want, bound, _ = oracle.gemm_mixed(a, b, t)
+    assert_within_tolerance(run_mixed16(a, b, t), want, bound, K,
+                            what=f"mixed16 256 normal {shape}")
+
+
 def test_mixed_plan_cases():
     for M, N, _, want in _split_cases():
         got = G.mixed_plan(M, N)
