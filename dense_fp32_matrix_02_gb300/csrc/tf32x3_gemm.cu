@@ -602,6 +602,9 @@ __global__ void __launch_bounds__(256)
     const float* src = partials + (long long)j * tail_splits * slot +
                        (long long)r * kCols + c4;
     float4 acc = *reinterpret_cast<const float4*>(src);
+    // the loads of several splits in flight at once; the sums still run in
+    // split order
+#pragma unroll 4
     for (int s = 1; s < tail_splits; ++s) {
       const float4 v = *reinterpret_cast<const float4*>(src + s * slot);
       acc.x += v.x;
