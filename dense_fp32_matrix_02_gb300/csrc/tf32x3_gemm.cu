@@ -31,10 +31,12 @@
 // to the split-K scratch); for the transposed store, or a C no tensor map
 // can describe, the 32 lanes store 32 consecutive columns of one row.
 //
-// Tiles: TILE_M rows × 128 columns of C.  The default is 128 × 128 with a
-// 4-stage ring of 16-deep k stages (24 KB each) and 256 TMEM columns, so
-// two CTAs share each SM and one CTA's epilogue overlaps the other's main
-// loop; TILE_M = 256 (5 stages, one CTA per SM) is the alternative.
+// Tiles: TILE_M rows × 128 columns of C.  For K >= 2048 the dispatcher
+// takes TILE_M = 256 (5 stages of 40 KB, 512 TMEM columns, one CTA per SM:
+// each B stage converted into TMEM feeds twice the MMAs); below that,
+// 128 × 128 with a 4-stage ring of 16-deep k stages (24 KB each) and 256
+// TMEM columns, so two CTAs share each SM and one CTA's epilogue overlaps
+// the other's main loop.
 // Warp roles (320 threads):
 //   warp 0     TMA producer (one thread): the A tile TILE_M×16 and the B
 //              tile 16×128 of each stage, completion counted on full[s];
@@ -47,9 +49,10 @@
 //              in shared memory (the small part into its own buffer; with
 //              the rounded split also big, written back in place), then
 //              stores half of its quarter's columns of D in the epilogue.
-// Operand forms (128 × 128 tiles): B stored N×K (TB), A stored K×M (TA,
-// transposed by the converters from a staging buffer), and C stored
-// transposed (TSTORE) for the swapped form of op(A)ᵀ·op(B)ᵀ; strided
+// Operand forms: B stored N×K (TB), C stored transposed (TSTORE) for the
+// swapped form of op(A)ᵀ·op(B)ᵀ (both at either tile size), and A stored
+// K×M (TA, 128-row tiles: transposed by the converters from a staging
+// buffer); strided
 // batches run as gridDim.z; split-K writes partial tiles that a second
 // kernel adds in split order.
 // Launched with programmatic stream serialization: the prologue overlaps
