@@ -554,6 +554,26 @@ def test_workspace_size_policy():
     assert G.workspace_size(0, 5, 5) == 0
 
 
+@pytest.mark.parametrize("shape", [(512, 384, 2048), (1000, 1000, 2100),
+                                   (300, 700, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_splitk_256_row_tiles(shape):
+    """K >= 2048 with few tiles: 256 × 128 tiles split over K (the split
+    count the plan reports), every element against the oracle, integers
+    exact."""
+    M, N, K = shape
+    p = G.plan(M, N, K)
+    assert p["tile_rows"] == 256 and p["splits"] > 1, p
+    a, b = synth.make_operands(M, N, K, seed=K, dist_a="normal")
+    c, need = run_gpu_ws(a, b)
+    assert need > 0
+    check_full(a, b, c, what=f"256 split {shape}")
+    ai, bi = synth.make_operands(M, N, K, seed=K + 1, dist_a="int",
+                                 dist_b="int")
+    ci, _ = run_gpu_ws(ai, bi)
+    check_full(ai, bi, ci, exact=True, what=f"256 split {shape} int")
+
+
 @pytest.mark.parametrize("name", ["sq1024", "rag1000"])
 def test_splitk_workloads(name):
     w = synth.WORKLOADS[name]
