@@ -86,6 +86,35 @@ def test_argument_checks_need_no_gpu(built_lib):
         gemm.gemm_f32_ptr(-1, 1, 1, 8, 1, 8, 1, 8, 1)
 
 
+def test_query_argument_checks_need_no_gpu(built_lib):
+    """The plan and workspace queries reject bad arguments before any
+    device call (status 1 = invalid argument)."""
+    from dense_fp32_matrix_02_gb300 import gemm
+    lib = gemm.lib()
+    i64 = ctypes.c_int64
+    out = (i64 * 5)()
+    # gemm_f32_plan: NULL out, negative sizes, leading dimensions too small
+    assert lib.gemm_f32_plan(4, 4, 4, 16, 4, 16, 4, 16, 4, None) == 1
+    assert lib.gemm_f32_plan(-1, 4, 4, 16, 4, 16, 4, 16, 4, out) == 1
+    assert lib.gemm_f32_plan(4, 4, 8, 16, 7, 16, 4, 16, 4, out) == 1
+    # gemm_f32_mixed_plan: M or N < 1, K < 0, NULL out
+    assert lib.gemm_f32_mixed_plan(0, 4, 4, out) == 1
+    assert lib.gemm_f32_mixed_plan(4, 0, 4, out) == 1
+    assert lib.gemm_f32_mixed_plan(4, 4, -1, out) == 1
+    assert lib.gemm_f32_mixed_plan(4, 4, 4, None) == 1
+    # gemm_f32_batched_workspace_size: unknown form or negative size
+    assert lib.gemm_f32_batched_workspace_size(2, 0, 4, 4, 4, 1) == -1
+    assert lib.gemm_f32_batched_workspace_size(0, 0, -1, 4, 4, 1) == -1
+    assert lib.gemm_f32_batched_workspace_size(0, 0, 4, 4, 4, -1) == -1
+    # nothing to do: no scratch, no device call
+    assert lib.gemm_f32_batched_workspace_size(1, 0, 4, 4, 0, 1) == 0
+    assert lib.gemm_f32_batched_workspace_size(1, 0, 4, 4, 4, 0) == 0
+    # gemm_f32_batched_ws: negative scratch or NULL scratch with bytes
+    args = (1, 0, 4, 4, 4, 16, 4, 16, 16, 4, 16, 16, 4, 16, 1)
+    assert lib.gemm_f32_batched_ws(*args, None, -1, None) == 1
+    assert lib.gemm_f32_batched_ws(*args, None, 64, None) == 1
+
+
 def test_test_hooks_roundtrip(built_lib):
     from dense_fp32_matrix_02_gb300 import gemm
     old = gemm.set_wait_timeout_ns(1000)
