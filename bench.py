@@ -143,18 +143,121 @@ def recorded_traffic(kernel, workload):
     return rec.get("dram_bytes_per_launch")
 
 
+# clock-event reason bits of the NVML API (nvml.h, "ClocksEventReasons")
+NVML_REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8,
+                "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+                "hw_power_brake_slowdown": 0x80}
+NVML_CLOCK_SM = 1
+
+
+class _Nvml:
+    """The few read-only NVML queries the clock record needs, through
+    ctypes (libnvidia-ml ships with the driver).  Raises OSError when the
+    library or the device is not there."""
+
+    def __init__(self, uuid):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        for name, args in (
+                ("nvmlInit_v2", []),
+                ("nvmlShutdown", []),
+                ("nvmlDeviceGetHandleByUUID",
+                 [ctypes.c_char_p, ctypes.POINTER(ctypes.c_void_p)]),
+                ("nvmlDeviceGetClockInfo",
+                 [ctypes.c_void_p, ctypes.c_int,
+                  ctypes.POINTER(ctypes.c_uint)]),
+                ("nvmlDeviceGetMaxClockInfo",
+                 [ctypes.c_void_p, ctypes.c_int,
+                  ctypes.POINTER(ctypes.c_uint)]),
+                ("nvmlDeviceGetPowerUsage",
+                 [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint)]),
+                ("nvmlDeviceGetCurrentClocksEventReasons",
+                 [ctypes.c_void_p, ctypes.POINTER(ctypes.c_ulonglong)])):
+            fn = getattr(self.lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.dev = ctypes.c_void_p()
+        if not uuid or self.lib.nvmlDeviceGetHandleByUUID(
+                uuid.encode(), ctypes.byref(self.dev)) != 0:
+            self.lib.nvmlShutdown()
+            raise OSError("no NVML handle for this device")
+        v = ctypes.c_uint()
+        self.max_mhz = (float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.dev, NVML_CLOCK_SM, ctypes.byref(v)) == 0 else None)
+
+    def sample(self):
+        """(SM MHz, watts, reason bits); None for a query that failed."""
+        ct = self.ct
+        mhz, mw, bits = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok1 = self.lib.nvmlDeviceGetClockInfo(
+            self.dev, NVML_CLOCK_SM, ct.byref(mhz)) == 0
+        ok2 = self.lib.nvmlDeviceGetPowerUsage(self.dev, ct.byref(mw)) == 0
+        ok3 = self.lib.nvmlDeviceGetCurrentClocksEventReasons(
+            self.dev, ct.byref(bits)) == 0
+        return (float(mhz.value) if ok1 else None,
+                mw.value / 1e3 if ok2 else None,
+                int(bits.value) if ok3 else None)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+def summarize_clocks(samples, t0, t1, max_mhz=None):
+    """Clock record of the samples (time, SM MHz, watts, reason names)
+    taken between t0 and t1 (the timed region); when none fell inside
+    (a region shorter than the sampling period), the ones nearest to it."""
+    inside = [x for x in samples if t0 <= x[0] <= t1]
+    where = "timed region"
+    if not inside and samples:
+        mid = 0.5 * (t0 + t1)
+        inside = sorted(samples, key=lambda x: abs(x[0] - mid))[:2]
+        where = "nearest to the timed region (shorter than the period)"
+    sm = [x[1] for x in inside if x[1] is not None]
+    power = [x[2] for x in inside if x[2] is not None]
+    reasons = sorted({r for x in inside for r in x[3]})
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_min_mhz": min(sm) if sm else None,
+            "sm_max_mhz": max_mhz,
+            "power_w_median": statistics.median(power) if power else None,
+            "power_w_max": max(power) if power else None,
+            "samples": len(inside), "window": where,
+            "reasons": reasons}
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    """SM clock, power and clock-event reasons, sampled while the timed
+    region runs: NVML every 2 ms from a thread, else nvidia-smi every
+    200 ms.  `stop(t0, t1)` keeps the samples taken between the
+    time.perf_counter() stamps t0 and t1."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
 
     def __init__(self, gpu_id=None):
+        import threading
         self.proc = None
+        self.nvml = None
         self.error = None
+        self.samples = []
+        self.smi_max = []
+        self.source = None
+        try:
+            self.nvml = _Nvml(gpu_id)
+        except (OSError, AttributeError) as e:
+            self.error = f"NVML: {e}"
+        if self.nvml is not None:
+            self.source = "nvml, every 2 ms"
+            self.done = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}",
                "--format=csv,noheader,nounits", "-lms", "200"]
         if gpu_id:
@@ -162,40 +265,65 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, every 200 ms"
+            self.done = threading.Event()
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
+            self.thread.start()
         except OSError as e:
-            self.error = str(e)
+            self.error = f"{self.error}; nvidia-smi: {e}"
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
-                    "error": self.error or "nvidia-smi unavailable"}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, power, reasons = [], [], [], set()
+    def _poll(self):
+        while not self.done.is_set():
+            mhz, watts, bits = self.nvml.sample()
+            names = ([n for n, b in NVML_REASONS.items() if bits & b]
+                     if bits is not None else [])
+            self.samples.append((time.perf_counter(), mhz, watts, names))
+            self.done.wait(self.PERIOD_S)
+
+    def _read_smi(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
-        for line in out.splitlines():
+        for line in self.proc.stdout:
+            t = time.perf_counter()
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                mhz, smax, watts = (float(parts[1]), float(parts[2]),
+                                    float(parts[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+            self.smi_max.append(smax)
+            active = [n for n, v in zip(names, parts[5:9])
+                      if v.lower().startswith("active")]
+            self.samples.append((t, mhz, watts, active))
+
+    def stop(self, t0=None, t1=None):
+        """The clock record of the samples between t0 and t1 (all of them
+        when no window is given)."""
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "error": self.error or "no clock source"}
+        if self.nvml is not None:
+            self.done.set()
+            self.thread.join(timeout=5)
+            self.nvml.close()
+            max_mhz = self.nvml.max_mhz
+        else:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.proc.wait()
+            self.thread.join(timeout=5)
+            max_mhz = max(self.smi_max) if self.smi_max else None
+        if t0 is None:
+            t0, t1 = float("-inf"), float("inf")
+        rec = summarize_clocks(list(self.samples), t0, t1, max_mhz)
+        rec["source"] = self.source
+        return rec
 
 
 def reduce_max_over_ranks(value, device=None):
@@ -295,7 +423,7 @@ def run_reference(args, w, config):
 
 def timed_region(step, args, stream, dev, world):
     """W warm-up steps, then K steps between CUDA events on `stream`, with
-    a barrier and a synchronize on both sides and nvidia-smi clocks sampled
+    a barrier and a synchronize on both sides and SM clocks sampled
     meanwhile.  Returns (ms, max ms over ranks, clocks, wall seconds)."""
     import torch
     import torch.distributed as dist
@@ -311,7 +439,8 @@ def timed_region(step, args, stream, dev, world):
     except Exception:  # noqa: BLE001 - older torch
         gpu_uuid = None
     sampler = ClockSampler(gpu_uuid)
-    time.sleep(0.3)
+    if sampler.nvml is None:
+        time.sleep(0.3)  # nvidia-smi's first sample
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -347,10 +476,11 @@ def timed_region(step, args, stream, dev, world):
                 step(i)
         events[c + 1].record(stream)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
+    wall1 = time.perf_counter()
+    wall = wall1 - wall0
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(wall0, wall1)
     ms = events[0].elapsed_time(events[-1])
     ms_max = reduce_max_over_ranks(ms, dev)
     if G.device_status() != 0:
@@ -404,9 +534,11 @@ def measure_ffma_peak(dev, stream, target_ms=60.0):
     except Exception:  # noqa: BLE001 - older torch
         uuid = None
     sampler = ClockSampler(uuid)
-    time.sleep(0.3)
+    if sampler.nvml is None:
+        time.sleep(0.3)  # nvidia-smi's first sample
+    t0 = time.perf_counter()
     best = min(run(iters) for _ in range(3))
-    clocks = sampler.stop()
+    clocks = sampler.stop(t0, time.perf_counter())
     flops = G.ffma_peak_flops(iters)
     return {"tflops": flops / (best / 1e3) / 1e12, "ms": best,
             "iters": iters, "sm_mhz": clocks.get("sm_mhz"),
@@ -602,6 +734,13 @@ def run_ours(args, w, config):
         hw = TF32_FLOP_PER_CLK_PER_SM * sms * smax * 1e6 / 1e12 / 3.0
         roof["peak_tensor_pipe_at_clock"] = hw
         roof["frac_tensor_pipe_at_clock"] = achieved / hw
+        if clocks.get("sm_mhz"):
+            # the same at the median SM clock sampled in the timed region
+            # (lower than the maximum once the power cap acts)
+            run = TF32_FLOP_PER_CLK_PER_SM * sms * clocks["sm_mhz"] * 1e6 \
+                / 1e12 / 3.0
+            roof["peak_tensor_pipe_at_run_clock"] = run
+            roof["frac_tensor_pipe_at_run_clock"] = achieved / run
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak,
                 "unit": "TFLOP/s", "frac": achieved / fp32_peak,

@@ -43,3 +43,43 @@ def test_weak_scaling_value_counts_every_rank():
     b = _bench()
     # 4 ranks, 10 steps of 1e12 flop each, slowest rank 20 ms
     assert b.weak_scaling_value(1e12, 10, 4, 20.0) == pytest.approx(2000.0)
+
+
+def test_clock_record_keeps_the_timed_region():
+    """Only samples taken inside the timed region enter the clock record:
+    the idle clocks before and after it, and their reasons, do not."""
+    b = _bench()
+    samples = [(0.0, 2070.0, 150.0, []), (0.1, 2070.0, 160.0, []),
+               (1.0, 1800.0, 1300.0, ["sw_power_cap"]),
+               (1.5, 1700.0, 1400.0, ["sw_power_cap"]),
+               (2.0, 1750.0, 1380.0, ["sw_power_cap"]),
+               (3.0, 2070.0, 170.0, ["hw_slowdown"])]
+    rec = b.summarize_clocks(samples, 0.9, 2.1, max_mhz=2070.0)
+    assert rec["samples"] == 3 and rec["window"] == "timed region"
+    assert rec["sm_mhz"] == 1750.0 and rec["sm_min_mhz"] == 1700.0
+    assert rec["power_w_max"] == 1400.0 and rec["power_w_median"] == 1380.0
+    assert rec["reasons"] == ["sw_power_cap"] and rec["sm_max_mhz"] == 2070.0
+
+
+def test_clock_record_of_a_region_shorter_than_the_period():
+    """A region between two samples takes the two nearest to its middle."""
+    b = _bench()
+    samples = [(0.0, 2070.0, 150.0, []), (1.0, 1900.0, 900.0, []),
+               (1.2, 1850.0, 950.0, ["sw_power_cap"]),
+               (5.0, 2070.0, 150.0, [])]
+    rec = b.summarize_clocks(samples, 1.05, 1.1)
+    assert rec["samples"] == 2 and rec["window"].startswith("nearest")
+    assert rec["sm_mhz"] == 1875.0 and rec["reasons"] == ["sw_power_cap"]
+    empty = b.summarize_clocks([], 0.0, 1.0)
+    assert empty["samples"] == 0 and empty["sm_mhz"] is None
+
+
+def test_clock_sampler_without_a_driver():
+    """With neither NVML nor nvidia-smi reachable the record says so and
+    carries no clocks; with either, a stop() returns a record."""
+    b = _bench()
+    s = b.ClockSampler("GPU-00000000-0000-0000-0000-000000000000")
+    rec = s.stop(0.0, 1.0)
+    assert "reasons" in rec and "sm_mhz" in rec
+    if s.source is None:
+        assert rec["sm_mhz"] is None and rec["error"]
