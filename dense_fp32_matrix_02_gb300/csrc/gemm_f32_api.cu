@@ -471,6 +471,24 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
   return GEMM_F32_OK;
 }
 
+// out[] of gemm_f32_plan for the AUTO plan on device d.
+int report_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                const float* B, int64_t ldb, const float* C, int64_t ldc,
+                const DeviceInfo& d, int64_t out[5]) {
+  Plan plan;
+  const int st = make_plan(M, N, K, A, lda, B, ldb, C, ldc,
+                           GEMM_F32_ALGO_AUTO, d, &plan);
+  if (st != GEMM_F32_OK) return st;
+  out[0] = plan.algo;
+  out[1] = plan.tc_stream ? 1 : 0;
+  out[2] = plan.splits;
+  out[3] = plan.full_tiles;
+  out[4] = plan.algo != GEMM_F32_ALGO_TF32X3 ? 0
+           : plan.tc_stream                   ? 128
+                                              : tf32x3_tile_m(plan.tc_cfg);
+  return GEMM_F32_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -584,23 +602,25 @@ int gemm_f32_plan(int64_t M, int64_t N, int64_t K, const float* A,
                   int64_t lda, const float* B, int64_t ldb, const float* C,
                   int64_t ldc, int64_t out[5]) {
   if (!out) return GEMM_F32_ERR_INVALID_ARG;
-  int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+  const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM_F32_OK) return st;
   const DeviceInfo* d = nullptr;
   cudaError_t e = device_info(&d);
   if (e != cudaSuccess) return fail_cuda(e);
-  Plan plan;
-  st = make_plan(M, N, K, A, lda, B, ldb, C, ldc, GEMM_F32_ALGO_AUTO, *d,
-                 &plan);
+  return report_plan(M, N, K, A, lda, B, ldb, C, ldc, *d, out);
+}
+
+int gemm_f32_plan_sms(int64_t M, int64_t N, int64_t K, const float* A,
+                      int64_t lda, const float* B, int64_t ldb,
+                      const float* C, int64_t ldc, int sm_count, int cc_major,
+                      int64_t out[5]) {
+  if (!out || sm_count < 1) return GEMM_F32_ERR_INVALID_ARG;
+  const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (st != GEMM_F32_OK) return st;
-  out[0] = plan.algo;
-  out[1] = plan.tc_stream ? 1 : 0;
-  out[2] = plan.splits;
-  out[3] = plan.full_tiles;
-  out[4] = plan.algo != GEMM_F32_ALGO_TF32X3 ? 0
-           : plan.tc_stream                   ? 128
-                                              : tf32x3_tile_m(plan.tc_cfg);
-  return GEMM_F32_OK;
+  DeviceInfo d;  // facts given, not queried; never used to launch
+  d.sm_count = sm_count;
+  d.cc_major = cc_major;
+  return report_plan(M, N, K, A, lda, B, ldb, C, ldc, d, out);
 }
 
 const char* gemm_f32_status_string(int status) {
@@ -669,6 +689,19 @@ int mixed_tile_rows(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {
   if (forced == 128 || forced == 256) return forced;
   const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256);
   return (K >= 2048 && N > 128 && tiles256 >= d.sm_count) ? 256 : 128;
+}
+
+// out[] of gemm_f32_mixed_plan on device d.
+void report_mixed_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo& d,
+                       int64_t out[5]) {
+  const gemm_f32_impl::Plan16 plan = gemm_f32_impl::plan_mixed16(
+      M, N, d.sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0,
+      mixed_tile_rows(M, N, K, d));
+  out[0] = plan.wn;
+  out[1] = plan.full;
+  out[2] = plan.parts;
+  out[3] = plan.grid;
+  out[4] = plan.bm;
 }
 
 }  // namespace
@@ -752,14 +785,18 @@ int gemm_f32_mixed_plan(int64_t M, int64_t N, int64_t K, int64_t out[5]) {
   const DeviceInfo* d = nullptr;
   cudaError_t e = device_info(&d);
   if (e != cudaSuccess) return fail_cuda(e);
-  const gemm_f32_impl::Plan16 plan = gemm_f32_impl::plan_mixed16(
-      M, N, d->sm_count, env_int("GEMM_F32_MIXED_NARROW", 1) != 0,
-      mixed_tile_rows(M, N, K, *d));
-  out[0] = plan.wn;
-  out[1] = plan.full;
-  out[2] = plan.parts;
-  out[3] = plan.grid;
-  out[4] = plan.bm;
+  report_mixed_plan(M, N, K, *d, out);
+  return GEMM_F32_OK;
+}
+
+int gemm_f32_mixed_plan_sms(int64_t M, int64_t N, int64_t K, int sm_count,
+                            int64_t out[5]) {
+  if (M < 1 || N < 1 || K < 0 || !out || sm_count < 1)
+    return GEMM_F32_ERR_INVALID_ARG;
+  DeviceInfo d;  // facts given, not queried; never used to launch
+  d.sm_count = sm_count;
+  d.cc_major = 10;
+  report_mixed_plan(M, N, K, d, out);
   return GEMM_F32_OK;
 }
 

@@ -81,8 +81,10 @@ int chunk_count(int64_t M, int64_t N) {
 // everything else.  So when M holds at least two waves of 128-row tiles
 // (a wave: two CTAs per SM), the first and last chunks are half a wave and
 // the chunks between at most one wave each, so that no chunk leaves a
-// nearly empty round of tiles behind; otherwise up to four equal chunks
-// that each still fill the GPU.
+// nearly empty round of tiles behind; otherwise up to four chunks of
+// equal whole 128-row tiles (the last one shorter) that each still fill
+// the GPU, so every chunk starts on a tile row and its A and C rows keep
+// the 16-byte alignment of the whole matrices.
 int chunk_bounds(int64_t M, int64_t N, int sm_count, int64_t* bounds) {
   const int64_t tiles_per_rb = (N + 127) / 128;  // tiles per 128 rows
   const int64_t rbs = (M + 127) / 128;
@@ -107,7 +109,7 @@ int chunk_bounds(int64_t M, int64_t N, int sm_count, int64_t* bounds) {
     return n;
   }
   const int chunks = chunk_count(M, N);
-  const int64_t rows = (M + chunks - 1) / chunks;
+  const int64_t rows = ((M + chunks - 1) / chunks + 127) / 128 * 128;
   int n = 0;
   for (int c = 0; c < chunks; ++c) {
     const int64_t r0 = c * rows;
@@ -132,6 +134,13 @@ cudaError_t copy_rows(float* dst, int64_t dst_ld, const float* src,
 }  // namespace
 
 extern "C" {
+
+int gemm_f32_host_chunks(int64_t M, int64_t N, int sm_count,
+                         int64_t bounds[17]) {
+  if (M < 1 || N < 1 || sm_count < 1 || !bounds)
+    return -GEMM_F32_ERR_INVALID_ARG;
+  return chunk_bounds(M, N, sm_count, bounds);
+}
 
 int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float* hA,
                   int64_t lda, const float* hB, int64_t ldb, float* hC,

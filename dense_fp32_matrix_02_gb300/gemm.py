@@ -106,6 +106,14 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_mixed_workspace_size.argtypes = [i64, i64, i64]
         L.gemm_f32_mixed_plan.restype = ci
         L.gemm_f32_mixed_plan.argtypes = [i64, i64, i64, ctypes.POINTER(i64)]
+        L.gemm_f32_plan_sms.restype = ci
+        L.gemm_f32_plan_sms.argtypes = args[:-1] + [ci, ci,
+                                                    ctypes.POINTER(i64)]
+        L.gemm_f32_mixed_plan_sms.restype = ci
+        L.gemm_f32_mixed_plan_sms.argtypes = [i64, i64, i64, ci,
+                                              ctypes.POINTER(i64)]
+        L.gemm_f32_host_chunks.restype = ci
+        L.gemm_f32_host_chunks.argtypes = [i64, i64, ci, ctypes.POINTER(i64)]
         _lib = L
         return L
 
@@ -462,22 +470,26 @@ def gemm_f32(a, b, c=None, stream=None, workspace=None):
 
 
 def plan(M, N, K, a_ptr=16, lda=None, b_ptr=16, ldb=None, c_ptr=16,
-         ldc=None) -> dict:
+         ldc=None, sm_count=None, cc_major=10) -> dict:
     """The automatic plan for these sizes (default: 16-byte aligned
     pointers, leading dimensions = the row widths rounded up to multiples
     of 4, the layouts the tensor kernels take): kernel family, tensor
     variant ("tiled" / "streaming"), split-K ways, whole tiles, rows of C
-    per tensor tile (0 for the FFMA kernels)."""
+    per tensor tile (0 for the FFMA kernels).  On the current device, or,
+    with `sm_count` given, on a device of that many SMs and compute
+    capability major `cc_major` without any CUDA call."""
     def pad4(x):
         return max((int(x) + 3) // 4 * 4, 4)
     out = (ctypes.c_int64 * 5)()
-    _check(lib().gemm_f32_plan(int(M), int(N), int(K), a_ptr or None,
-                               int(lda if lda is not None else pad4(K)),
-                               b_ptr or None,
-                               int(ldb if ldb is not None else pad4(N)),
-                               c_ptr or None,
-                               int(ldc if ldc is not None else pad4(N)),
-                               out), "gemm_f32_plan")
+    args = (int(M), int(N), int(K), a_ptr or None,
+            int(lda if lda is not None else pad4(K)), b_ptr or None,
+            int(ldb if ldb is not None else pad4(N)), c_ptr or None,
+            int(ldc if ldc is not None else pad4(N)))
+    if sm_count is None:
+        _check(lib().gemm_f32_plan(*args, out), "gemm_f32_plan")
+    else:
+        _check(lib().gemm_f32_plan_sms(*args, int(sm_count), int(cc_major),
+                                       out), "gemm_f32_plan_sms")
     return {"algo": out[0], "variant": "streaming" if out[1] else "tiled",
             "splits": out[2], "whole_tiles": out[3], "tile_rows": out[4]}
 
@@ -605,15 +617,31 @@ def mixed_workspace_size(M, N, K) -> int:
     return n
 
 
-def mixed_plan(M, N, K=0) -> dict:
-    """How the 16-bit product cuts an M×N×K product on the current device:
-    tile width, tiles run whole, strips per remaining tile, CTAs, tile
-    rows."""
+def mixed_plan(M, N, K=0, sm_count=None) -> dict:
+    """How the 16-bit product cuts an M×N×K product on the current device
+    (or, with `sm_count` given, on a device of that many SMs, without any
+    CUDA call): tile width, tiles run whole, strips per remaining tile,
+    CTAs, tile rows."""
     out = (ctypes.c_int64 * 5)()
-    _check(lib().gemm_f32_mixed_plan(int(M), int(N), int(K), out),
-           "gemm_f32_mixed_plan")
+    if sm_count is None:
+        _check(lib().gemm_f32_mixed_plan(int(M), int(N), int(K), out),
+               "gemm_f32_mixed_plan")
+    else:
+        _check(lib().gemm_f32_mixed_plan_sms(int(M), int(N), int(K),
+                                             int(sm_count), out),
+               "gemm_f32_mixed_plan_sms")
     return {"width": out[0], "whole": out[1], "parts": out[2], "grid": out[3],
             "rows": out[4]}
+
+
+def host_chunks(M, N, sm_count) -> list:
+    """The first row of each row chunk gemm_f32_host cuts an M×N product
+    into on a device of `sm_count` SMs, then M (no CUDA call)."""
+    bounds = (ctypes.c_int64 * 17)()
+    n = lib().gemm_f32_host_chunks(int(M), int(N), int(sm_count), bounds)
+    if n < 0:
+        _check(-n, "gemm_f32_host_chunks")
+    return [int(bounds[i]) for i in range(n + 1)]
 
 
 def gemm_f32_mixed_ptr(type_, M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc,

@@ -374,6 +374,36 @@ GEMM_F32_API int gemm_f32_plan(int64_t M, int64_t N, int64_t K,
                                int64_t ldb, const float *C, int64_t ldc,
                                int64_t out[5]);
 
+/*
+ * Host logic only, no CUDA call (tests of the planner, and planning on a
+ * machine without the GPU): the plan gemm_f32_plan would make on a device
+ * with `sm_count` SMs and compute capability major `cc_major` (10 for the
+ * tcgen05 family).  A, B and C are only checked for 16-byte alignment and
+ * NULL, never read.  out[] as for gemm_f32_plan.  GEMM_F32_ERR_INVALID_ARG
+ * for bad sizes, out == NULL or sm_count < 1.
+ */
+GEMM_F32_API int gemm_f32_plan_sms(int64_t M, int64_t N, int64_t K,
+                                   const float *A, int64_t lda,
+                                   const float *B, int64_t ldb,
+                                   const float *C, int64_t ldc, int sm_count,
+                                   int cc_major, int64_t out[5]);
+
+/* Host logic only, no CUDA call: the plan gemm_f32_mixed_plan would make on
+ * a device with `sm_count` SMs.  out[] and errors as for
+ * gemm_f32_mixed_plan (GEMM_F32_ERR_INVALID_ARG also for sm_count < 1). */
+GEMM_F32_API int gemm_f32_mixed_plan_sms(int64_t M, int64_t N, int64_t K,
+                                         int sm_count, int64_t out[5]);
+
+/*
+ * Host logic only, no CUDA call: the row chunks gemm_f32_host cuts an M × N
+ * product into on a device with `sm_count` SMs.  Writes the first row of
+ * each chunk to bounds[0..n-1] and M to bounds[n] (bounds holds at least 17
+ * entries) and returns n (1 to 16), or GEMM_F32_ERR_INVALID_ARG negated
+ * (M or N < 1, sm_count < 1, bounds NULL).
+ */
+GEMM_F32_API int gemm_f32_host_chunks(int64_t M, int64_t N, int sm_count,
+                                      int64_t bounds[17]);
+
 /* Static description of a status code. */
 GEMM_F32_API const char *gemm_f32_status_string(int status);
 

@@ -432,6 +432,20 @@ def test_stream_kernel_shapes(case):
     assert G.device_status() == 0
 
 
+def test_device_free_plans_equal_the_device_plans():
+    """The planner given this GPU's SM count (no CUDA call) decides as the
+    one that queries the device."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    major = torch.cuda.get_device_properties(DEV).major
+    for M, N, K in [(4096, 4096, 4096), (8192, 3072, 768), (1024,) * 3,
+                    (1000,) * 3, (65536, 64, 64), (64, 64, 64),
+                    (300, 700, 4096), (19456, 1, 1), (517, 300, 77)]:
+        assert G.plan(M, N, K) == G.plan(M, N, K, sm_count=sms,
+                                         cc_major=major), (M, N, K)
+        assert G.mixed_plan(M, N, K) == G.mixed_plan(M, N, K,
+                                                     sm_count=sms), (M, N, K)
+
+
 def test_plan_reports_the_streaming_kernel():
     """gemm_f32_plan: the streaming variant exactly for N, K <= 128 with a
     128-row tile per SM (and not with GEMM_F32_STREAM=0); tiled otherwise."""
@@ -673,7 +687,11 @@ def test_splitk_deterministic():
 @pytest.mark.parametrize("shape,pinned,pad", [
     ((1000, 1000, 1000), True, 0), ((2048, 1536, 512), True, 0),
     ((517, 300, 77), True, 3), ((517, 300, 77), False, 5),
-    ((9, 7, 0), True, 0), ((1, 1, 1), False, 0)])
+    ((9, 7, 0), True, 0), ((1, 1, 1), False, 0),
+    # several chunks: equal tile rows with an odd K ([0, 256, 512, 600]),
+    # and half-wave ends around wave-sized chunks ([0, 512, 1280, 2048,
+    # 2500] on 152 SMs)
+    ((600, 30000, 33), True, 0), ((2500, 4096, 24), True, 1)])
 def test_host_pipeline(shape, pinned, pad):
     """gemm_f32_host: host operands (strided or not, pinned or not) through
     lent device buffers, chunked and overlapped, equal the oracle."""

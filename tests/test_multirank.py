@@ -43,7 +43,9 @@ def _rank_main(rank, world, port, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
     port = _free_port()
-    with mp.Manager() as manager:
+    # every process of the test (the ranks and the manager holding their
+    # results) is spawned, never forked from this multi-threaded process
+    with mp.get_context("spawn").Manager() as manager:
         out = manager.dict()
         mp.start_processes(_rank_main, args=(world, port, out), nprocs=world,
                            join=True, start_method="spawn")
