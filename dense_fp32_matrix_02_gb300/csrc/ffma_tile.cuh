@@ -4,6 +4,9 @@
 // Both are the third tiling level of "3 · La mémoire partagée", §3.4 ("Le
 // registre comme troisième niveau de tuile"): each thread keeps an 8×8 block
 // of C in registers and, per k, does 64 multiply-adds for 16 loaded values.
+// FfmaTile issues them as 32 packed two-lane FMAs (PTX fma.rn.f32x2, the
+// Blackwell FP32 pair instruction: each lane an fmaf, round to nearest,
+// no flush to zero), so the FMA pipe is fed with half the instructions.
 //
 // FfmaTile keeps A in its global row-major (K-contiguous) order, so TMA can
 // copy it without a transpose, and each thread reads A along K with 16-byte
@@ -36,6 +39,25 @@ __host__ __device__ constexpr int a_swizzle(int m) {
   return ((m * BK * 4) >> 7) & (BK / 4 - 1);
 }
 
+// Two fp32 values in one 64-bit register pair (lo = first).
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(unsigned long long v, float& lo,
+                                             float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a·b + d in each of the two lanes.
+__device__ __forceinline__ void fma_f32x2(unsigned long long& d,
+                                          unsigned long long a,
+                                          unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 template <int BM, int BN, int BK>
 struct FfmaTile {
   static_assert(BM % 64 == 0 && BN % 32 == 0, "warp tile is 64 x 32");
@@ -46,6 +68,16 @@ struct FfmaTile {
   static constexpr int kStageFloatsA = BM * BK;
   static constexpr int kStageFloatsB = BK * BN;
   static constexpr int kStageBytes = 4 * (kStageFloatsA + kStageFloatsB);
+  // The 8×8 accumulators as pairs: acc[i][p] holds columns 2p and 2p + 1
+  // of row i (in the column order of `store`).
+  using Acc = unsigned long long[8][4];
+
+  static __device__ __forceinline__ void zero(Acc& acc) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;  // two +0.0f
+  }
 
   // Per-thread fixed offsets (floats) into a stage.
   int a_row_off;      // (wm*64 + lm) * BK
@@ -70,7 +102,7 @@ struct FfmaTile {
   // acc += A_stage · B_stage for this thread's 8×8 block.
   __device__ __forceinline__ void compute(const float* __restrict__ As,
                                           const float* __restrict__ Bs,
-                                          float (&acc)[8][8]) const {
+                                          Acc& acc) const {
     const float* a_base = As + a_row_off;
     const float* b_base = Bs + b_col_off;
 #pragma unroll
@@ -86,15 +118,18 @@ struct FfmaTile {
         const float4 b0 = *reinterpret_cast<const float4*>(b_base + k * BN);
         const float4 b1 =
             *reinterpret_cast<const float4*>(b_base + k * BN + 16);
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const unsigned long long bp[4] = {
+            pack_f32x2(b0.x, b0.y), pack_f32x2(b0.z, b0.w),
+            pack_f32x2(b1.x, b1.y), pack_f32x2(b1.z, b1.w)};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float av = kk == 0 ? a[i].x
                            : kk == 1 ? a[i].y
                            : kk == 2 ? a[i].z
                                      : a[i].w;
+          const unsigned long long aa = pack_f32x2(av, av);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+          for (int j = 0; j < 4; ++j) fma_f32x2(acc[i][j], aa, bp[j]);
         }
       }
     }
@@ -104,8 +139,13 @@ struct FfmaTile {
   // Interior tiles with a 16-byte-aligned C and ldc % 4 == 0 use float4
   // stores; every other case checks each element against M and N.
   __device__ __forceinline__ void store(const Problem& p, int bm, int bn,
-                                        bool c_vec,
-                                        const float (&acc)[8][8]) const {
+                                        bool c_vec, const Acc& acc2) const {
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        unpack_f32x2(acc2[i][j], acc[i][2 * j], acc[i][2 * j + 1]);
     const bool interior = (bm + BM <= p.M) && (bn + BN <= p.N);
     const bool epi = p.bias != nullptr || p.act != kActNone;
     // the bias of the thread's 8 columns, loaded once (C stores may alias it)
@@ -186,6 +226,14 @@ struct FfmaTileT {
   static constexpr int kStageFloatsA = BM * BK;
   static constexpr int kStageFloatsB = BK * BN;
   static constexpr int kStageBytes = 4 * (kStageFloatsA + kStageFloatsB);
+  using Acc = float[8][8];
+
+  static __device__ __forceinline__ void zero(Acc& acc) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  }
 
   int a_off[8];  // (c ^ g) * 4 for g = 0..7, c = row0 / 4
   int b_off[BSWZ ? 8 : 1];  // (c ^ g) * 4 for g = 0..7, c = col0 / 4

@@ -167,11 +167,8 @@ struct SimtKernel {
 
     Tile tile;
     tile.init(tid);
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    typename Tile::Acc acc;
+    Tile::zero(acc);
 
     const int kt_count = (p.K + BK - 1) / BK;
 #pragma unroll

@@ -106,11 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   Tile tile;
   tile.init(tid);
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  typename Tile::Acc acc;
+  Tile::zero(acc);
 
   bool ok = true;
   for (int kt = 0; kt < nk; ++kt) {
