@@ -83,3 +83,40 @@ def test_clock_sampler_without_a_driver():
     assert "reasons" in rec and "sm_mhz" in rec
     if s.source is None:
         assert rec["sm_mhz"] is None and rec["error"]
+
+
+def test_hbm_roofline_arithmetic():
+    """Algorithmic bytes per launch over the launch time, against the
+    measured copy bandwidth."""
+    b = _bench()
+    peaks = {"hbm_gbs": 6784.5}
+    # 33,570,816 B (65536 x 64 x 64 fp32 A, B, C) in 12.5 us
+    r = b.hbm_roofline(5.37e8, 33570816, 0.0125, peaks, "measured", 302.3,
+                       42.9)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(33570816 / 12.5e-6 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6784.5)
+    assert r["frac_tensor"] == pytest.approx(42.9 / 302.3)
+
+
+def test_traffic_records_follow_the_sources(monkeypatch):
+    """A DRAM-traffic record counts only while its kernel's sources hash to
+    the value stored with it; every record names an existing summary."""
+    import json
+    b = _bench()
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    records = json.load(open(path))
+    for key, rec in records.items():
+        kernel, workload = key.split(":")
+        assert kernel in b.KERNEL_SOURCES, key
+        assert rec["dram_bytes_per_launch"] > 0
+        assert os.path.exists(os.path.join(ROOT, rec["summary"])), key
+        got = b.recorded_traffic(kernel, workload)
+        if rec["source_hash"] == b.kernel_source_hash(kernel):
+            assert got == rec["dram_bytes_per_launch"]
+        else:
+            assert got is None
+    # a changed source invalidates the record
+    monkeypatch.setattr(b, "kernel_source_hash", lambda k: "0" * 16)
+    assert b.recorded_traffic("tf32x3", "sq4096") is None
+    assert b.recorded_traffic("tf32x3", "no-such-workload") is None
