@@ -366,8 +366,8 @@ GEMM_F32_API int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const flo
  * environment variable GEMM_F32_STREAM=0 turns it off); out[2]: split-K
  * ways of the split tiles (1: none); out[3]: tiles computed whole before
  * the split ones; out[4]: rows of C per tensor tile (256 when K >= 2048,
- * else 128; 0 for the FFMA kernels).  Returns a status (GEMM_F32_ERR_INVALID_ARG also for
- * out == NULL).
+ * else 128; 0 for the FFMA kernels).  Returns a status
+ * (GEMM_F32_ERR_INVALID_ARG also for out == NULL).
  */
 GEMM_F32_API int gemm_f32_plan(int64_t M, int64_t N, int64_t K,
                                const float *A, int64_t lda, const float *B,
