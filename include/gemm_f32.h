@@ -314,7 +314,11 @@ GEMM_F32_API int gemm_f32_ws(int64_t M, int64_t N, int64_t K, const float *A,
  * it keeps whatever the last call left there; nothing in it needs to start
  * at zero (every split writes the whole partial tile it later adds), but
  * calls that may overlap on the GPU (different streams, or not yet
- * finished) race on it and must be serialised by the caller.
+ * finished) race on it and must be serialised by the caller.  The device
+ * address is looked up once per device and kept for the life of the
+ * process: do not call this entry after a cudaDeviceReset of a device it
+ * has already run on (the reset unloads the library's device code, and the
+ * kept address would no longer name the buffer).
  */
 GEMM_F32_API int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
                                   const float *A, int64_t lda, const float *B,

@@ -2,9 +2,8 @@
 
 All calls go through the C ABI (ctypes binding).  Acceptance per element:
 |C - C_ref| <= 1e-5·sqrt(K)·(|A|·|B|)_ij + 1e-30; on small-integer inputs
-the result must equal the oracle bit for bit.  Full-size cases compare
-sampled elements with the oracle one by one and check every row sum of C
-against A·(B·1) computed by the oracle.
+the result must equal the oracle bit for bit.  Every case, the full-size
+workloads included, compares every element of C with the oracle.
 """
 
 from __future__ import annotations
@@ -89,43 +88,51 @@ def check_full(a, b, c, exact=False, what=""):
         assert_within_tolerance(c, ref, bound, a.shape[1], what)
 
 
-def sample_positions(M, N, count=1024, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = list(rng.integers(0, M, count))
-    cols = list(rng.integers(0, N, count))
-    # corners and tile edges
-    for r in {0, M - 1, min(M - 1, 127), min(M - 1, 128), M // 2}:
-        for c in {0, N - 1, min(N - 1, 127), min(N - 1, 128), N // 2}:
-            rows.append(r)
-            cols.append(c)
-    return np.array(rows), np.array(cols)
+_WORKLOAD_REF = {}
 
 
-def check_sampled_and_rowsums(a, b, c, exact=False, what=""):
+def workload_reference(w):
+    """(A, B, C_ref, bound) of a named workload; the oracle's product is
+    computed once and kept for the next test (the two latest workloads)."""
+    if w.name not in _WORKLOAD_REF:
+        while len(_WORKLOAD_REF) >= 2:
+            _WORKLOAD_REF.pop(next(iter(_WORKLOAD_REF)))
+        a, b = w.operands()
+        ref, bound, _ = oracle.gemm(a, b)
+        _WORKLOAD_REF[w.name] = (a, b, ref, bound)
+    return _WORKLOAD_REF[w.name]
+
+
+def run_like_bench(a, b):
+    """C = A·B the way bench.py times it: unpadded operands (ld = row
+    width), gemm_f32_ws with exactly the scratch gemm_f32_workspace_size
+    asks for, on the current stream.  Returns (C, scratch bytes)."""
     M, K = a.shape
     N = b.shape[1]
-    rows, cols = sample_positions(M, N)
-    ref, bound, _ = oracle.entries(a, b, rows, cols)
-    got = c[rows, cols]
-    if exact:
-        assert_bitexact(got, ref, what + " (sampled)")
-    else:
-        assert_within_tolerance(got, ref, bound, K, what + " (sampled)")
-    # every row: sum_j C[i, j] = (A·(B·1))_i
-    ones = np.ones((N, 1), np.float32)
-    b1, b1bound, _ = oracle.gemm(b, ones)          # exact for these inputs?
-    b1_32 = b1.astype(np.float32)
-    arow, _, _ = oracle.gemm(a, b1_32)
-    absrow, _, _ = oracle.gemm(np.abs(a), b1bound.astype(np.float32))
-    rs = c.astype(np.float64).sum(axis=1)
-    if exact:
-        assert np.array_equal(rs, arow[:, 0]), what + " row sums"
-    else:
-        # rounding B·1 to float32 and summing C in float64 both add a little
-        tol = (1e-5 * np.sqrt(K) + N * 2.0**-52 + 2.0**-23) * absrow[:, 0] \
-            + 1e-30
-        err = np.abs(rs - arow[:, 0])
-        assert (err <= tol).all(), what + f" row sums, worst {err.max():.3e}"
+    need = G.workspace_size(M, N, K)
+    ws = torch.empty(max(need // 4, 1), device=DEV) if need else None
+    ta = torch.from_numpy(a).to(DEV)
+    tb = torch.from_numpy(b).to(DEV)
+    tc = torch.full((M, N), float("nan"), device=DEV)
+    G.gemm_f32_ws_ptr(M, N, K, ta.data_ptr(), K, tb.data_ptr(), N,
+                      tc.data_ptr(), N, ws.data_ptr() if ws is not None else 0,
+                      need, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return tc.cpu().numpy(), need
+
+
+def expected_tail_plan(M, N, K):
+    """The split the planner must choose for a product whose tiles fill
+    at least half of the CTA slots: (tile rows, splits, whole tiles)."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    rows = 256 if K >= 2048 else 128
+    slots = sms * (1 if rows == 256 else 2)
+    tiles = -(-M // rows) * -(-N // 128)
+    tail = tiles % slots
+    if 2 * tiles < slots or tail == 0:
+        return None
+    s = min(slots // tail, -(-K // 16) // 8, 16)
+    return (rows, s, tiles - tail) if s >= 2 else (rows, 1, tiles)
 
 
 # ------------------------------------------------------------- workloads
@@ -135,9 +142,12 @@ LARGE = ["sq4096", "mlp"]
 
 @pytest.mark.parametrize("name", SMALL)
 def test_workload_full_auto(name):
+    """gemm_f32 and the path bench.py times (gemm_f32_ws with its
+    scratch), every element against the oracle."""
     w = synth.WORKLOADS[name]
     a, b = w.operands()
     check_full(a, b, run_gpu(a, b), what=name)
+    check_full(a, b, run_like_bench(a, b)[0], what=name + " bench path")
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -145,19 +155,37 @@ def test_workload_integer_bitexact(name):
     w = synth.WORKLOADS[name].integer_variant()
     a, b = w.operands()
     check_full(a, b, run_gpu(a, b), exact=True, what=w.name)
+    check_full(a, b, run_like_bench(a, b)[0], exact=True,
+               what=w.name + " bench path")
 
 
+@pytest.mark.parametrize("integer", [False, True], ids=["float", "int"])
 @pytest.mark.parametrize("name", LARGE)
-def test_workload_large_sampled(name):
+def test_workload_large_full(name, integer):
+    """The full-size workloads, every element against the oracle (the
+    small-integer variants bit for bit), through two entry points:
+
+    * the path bench.py times: gemm_f32_ws with the scratch it asks for
+      (whole tiles, then the last, partly filled round split over K and
+      reduced), with the split the planner must choose;
+    * gemm_f32 itself (no scratch, nothing split)."""
     w = synth.WORKLOADS[name]
-    a, b = w.operands()
-    check_sampled_and_rowsums(a, b, run_gpu(a, b), what=name)
-
-
-def test_large_integer_bitexact_sampled():
-    w = synth.WORKLOADS["sq4096"].integer_variant()
-    a, b = w.operands()
-    check_sampled_and_rowsums(a, b, run_gpu(a, b), exact=True, what=w.name)
+    if integer:
+        w = w.integer_variant()
+    a, b, ref, bound = workload_reference(w)
+    want = expected_tail_plan(w.M, w.N, w.K)
+    p = G.plan(w.M, w.N, w.K)
+    if want is not None:
+        assert (p["tile_rows"], p["splits"], p["whole_tiles"]) == want, p
+    c, need = run_like_bench(a, b)
+    assert (need > 0) == (p["splits"] > 1)
+    plain = run_gpu(a, b)
+    for got, path in ((c, "bench path"), (plain, "gemm_f32")):
+        if integer:
+            assert_bitexact(got, ref, f"{w.name} {path}")
+        else:
+            assert_within_tolerance(got, ref, bound, w.K, f"{w.name} {path}")
+    assert G.device_status() == 0
 
 
 # ------------------------------------------------------------- every kernel
@@ -652,13 +680,30 @@ def test_tail_split_shapes(shape):
     assert G.device_status() == 0
 
 
-def test_tail_split_mlp_sampled():
-    """8192 x 3072 x 768: 1536 tiles, the last 16 split over the GPU."""
-    w = synth.WORKLOADS["mlp"]
-    a, b = w.operands()
+def test_tail_split_256_row_tiles():
+    """256 × 128 tiles (K >= 2048) with whole tiles in front of a split
+    tail: 8 tile columns and enough tile rows to leave a 16-tile or larger
+    last round (152 SMs: 21 × 8 = 168 tiles, 152 whole and 16 split 9
+    ways).  M, N and K are ragged.  Every element against the oracle,
+    integers bit for bit, a repeat bit-identical."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    rows = -(-(sms + 16) // 8)
+    M, N, K = rows * 256 - 77, 8 * 128 - 50, 2048 + 13
+    p = G.plan(M, N, K)
+    assert p["tile_rows"] == 256 and p["splits"] > 1, p
+    assert p["whole_tiles"] == sms, p
+    assert (p["tile_rows"], p["splits"], p["whole_tiles"]) == \
+        expected_tail_plan(M, N, K)
+    a, b = synth.make_operands(M, N, K, seed=21, dist_a="normal")
     c, need = run_gpu_ws(a, b)
     assert need > 0
-    check_sampled_and_rowsums(a, b, c, what="mlp tail split")
+    check_full(a, b, c, what="256-row tail split")
+    c2, _ = run_gpu_ws(a, b)
+    assert np.array_equal(c.view(np.uint32), c2.view(np.uint32))
+    ai, bi = synth.make_operands(M, N, K, seed=22, dist_a="int", dist_b="int")
+    ci, _ = run_gpu_ws(ai, bi)
+    check_full(ai, bi, ci, exact=True, what="256-row tail split int")
+    assert G.device_status() == 0
 
 
 def test_tail_split_fused_epilogue():
@@ -740,10 +785,11 @@ def test_tma_ffma_shapes(shape):
     assert G.device_status() == 0
 
 
-def test_tma_ffma_sq4096_sampled():
+def test_tma_ffma_sq4096_full():
     w = synth.WORKLOADS["sq4096"]
-    a, b = w.operands()
-    check_sampled_and_rowsums(a, b, run_gpu(a, b, G.ALGO_TMA), what="tma")
+    a, b, ref, bound = workload_reference(w)
+    assert_within_tolerance(run_gpu(a, b, G.ALGO_TMA), ref, bound, w.K,
+                            "tma sq4096")
 
 
 def test_tma_ffma_unsupported_when_misaligned():
@@ -963,12 +1009,12 @@ def test_batched_forms_forced_simt(form):
     # K >= 2048 and a 256-row tile per SM: the 256 × 128 configurations
     ("NT", None, (2560, 2048, 2048)), ("TT", None, (2048, 2560, 2048)),
     ("TN", "full", (2560, 2048, 2048))])
-def test_transposed_forms_large_sampled(form, ws, shape):
-    """op forms on large shapes, sampled against the oracle."""
+def test_transposed_forms_large_full(form, ws, shape):
+    """op forms on large shapes, every element against the oracle."""
     M, N, K = shape
     As, Bs, Cs, _, _, _ = _batched_case(form, M, N, K, 1, seed=5, ws=ws)
-    check_sampled_and_rowsums(As[0], Bs[0], np.ascontiguousarray(Cs[0][:, :N]),
-                              what=f"{form} large")
+    check_full(As[0], Bs[0], np.ascontiguousarray(Cs[0][:, :N]),
+               what=f"{form} large")
 
 
 # ------------------------------------------------------------- epilogue

@@ -3,11 +3,15 @@ inside the library, for callers that must not allocate device memory (code
 whose device memory all comes from a framework's own pool, or paths where
 an allocation's synchronisation and latency are not acceptable).
 
-The entry point is called through the C ABI and its output compared with
-that of gemm_f32_ws (the same product with caller-owned scratch), within
-the tolerance the other tests use, on two calls in a row.  This file sorts
-last so that a run stopping at the first failure has already run every
-other test; it also passes on its own in a fresh process.
+The entry point is called through the C ABI, twice in a row, and its
+output is checked three ways: against the float64 oracle within the
+tolerance the other tests use (bit for bit on small-integer inputs), and
+bit for bit against gemm_f32_ws (the same product with caller-owned
+scratch, which runs the same deterministic split).  The shapes used are
+ones whose plan splits over K, so the static buffer is really written and
+read.  This file sorts last so that a run stopping at the first failure
+has already run every other test; it also passes on its own in a fresh
+process.
 """
 
 from __future__ import annotations
@@ -17,6 +21,7 @@ import pytest
 
 import oracle
 from dense_fp32_matrix_02_gb300 import synth
+from helpers import assert_bitexact, assert_within_tolerance
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -37,11 +42,15 @@ def _noalloc(ta, tb, tc):
                            torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("name", ["sq1024", "rag1000", "sq64"])
-def test_noalloc_matches_workspace_entry_point_twice(name):
-    w = synth.WORKLOADS[name]
+@pytest.mark.parametrize("name", ["sq1024", "rag1000", "rag1000_int",
+                                  "sq64"])
+def test_noalloc_matches_oracle_and_workspace_entry_point_twice(name):
+    w = (synth.WORKLOADS[name[:-4]].integer_variant() if name.endswith("_int")
+         else synth.WORKLOADS[name])
     a, b = w.operands()
     need = G.workspace_size(w.M, w.N, w.K)
+    # 1024^3 and 1000^3 are split over K: the static scratch is used
+    assert (need > 0) == (name != "sq64")
     assert need <= G.noalloc_scratch_bytes()
     ta = torch.from_numpy(a).to(DEV)
     tb = torch.from_numpy(b).to(DEV)
@@ -49,9 +58,8 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
     ws = torch.empty(max(need // 4, 1), device=DEV)
     c_ws = G.gemm_f32(ta, tb, workspace=ws)
     torch.cuda.synchronize()
-    c_ws = c_ws.cpu().numpy().astype(np.float64)
-    _, bound, _ = oracle.gemm(a, b)
-    tol = 1e-5 * np.sqrt(w.K) * bound + 1e-30
+    c_ws = c_ws.cpu().numpy()
+    ref, bound, _ = oracle.gemm(a, b)
     tc = torch.empty(w.M, w.N, device=DEV)
     free_after = []
     for call in range(2):
@@ -60,9 +68,13 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
         torch.cuda.synchronize()
         free_after.append(torch.cuda.mem_get_info(DEV)[0])
         c = tc.cpu().numpy()
-        err = np.abs(c - c_ws)
-        assert (err <= tol).all(), \
-            f"{name} call {call}: worst |diff| {np.nanmax(err):.3e}"
+        what = f"{w.name} call {call}"
+        if w.dist_a == "int":
+            assert_bitexact(c, ref, what)
+        else:
+            assert_within_tolerance(c, ref, bound, w.K, what)
+        # same plan, same split, same summation order as gemm_f32_ws
+        assert np.array_equal(c.view(np.uint32), c_ws.view(np.uint32)), what
     # the second call took no device memory
     assert free_after[1] == free_after[0]
     assert G.device_status() == 0
