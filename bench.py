@@ -15,6 +15,14 @@ the value is all ranks' flops over the slowest rank's time.
 ``--impl reference`` times the float64 CPU oracle on this machine's host
 cores instead (rank 0 only), each step a bounded block of rows of the same
 workload.
+
+The 3xTF32 kernel's roof is the TF32 tensor rate that cuBLAS reaches in the
+same run (``tf32_probe``), divided by the three TF32 products per
+multiply-add; the FFMA kernels' roof is the library's FMA-chain probe
+(``ffma_probe``).  The default 4096^3 run also adds ``sub_records``:
+secondary figures, each timed on its own with its own clock record (the
+plain gemm_f32 call, the two FFMA kernels forced, and the other workloads
+through gemm_f32_ws); none of them enters the headline value.
 """
 
 from __future__ import annotations
@@ -69,6 +77,10 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sub-records", action="store_true",
+                   help="skip the secondary timings the default run adds "
+                        "(the plain call, the FFMA kernels, the other "
+                        "workloads)")
     args = p.parse_args()
     if args.epilogue != "none" and (args.algo != "auto" or args.op != "nn"
                                     or args.batch != 1):
@@ -545,6 +557,190 @@ def measure_ffma_peak(dev, stream, target_ms=60.0):
             "reasons": clocks.get("reasons")}
 
 
+def _gpu_uuid(dev):
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001 - older torch
+        return None
+
+
+def measure_tf32_peak(dev, stream, n=8192, reps=10):
+    """cuBLAS's dense TF32 tensor rate on this GPU, measured in this run:
+    an n x n x n float32 torch.matmul with TF32 tensor math allowed (one
+    TF32 product, fp32 accumulation), best of `reps` launches timed one
+    at a time with CUDA events, with the SM clocks seen meanwhile.  It is
+    the denominator of the 3xTF32 kernel (which does three TF32 products
+    per multiply-add), the way the bf16 GEMM is for the 16-bit one."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        a = torch.rand(n, n, device=dev, generator=g)
+        b = torch.rand(n, n, device=dev, generator=g)
+        c = torch.empty(n, n, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        sampler = ClockSampler(_gpu_uuid(dev))
+        if sampler.nvml is None:
+            time.sleep(0.3)  # nvidia-smi's first sample
+        t0 = time.perf_counter()
+        times = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                torch.matmul(a, b, out=c)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        clocks = sampler.stop(t0, time.perf_counter())
+        del a, b, c
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    best = min(times)
+    return {"tflops": 2.0 * n ** 3 / (best / 1e3) / 1e12, "ms": best,
+            "n": n, "reps": reps, "sm_mhz": clocks.get("sm_mhz"),
+            "reasons": clocks.get("reasons"),
+            "how": f"cuBLAS float32 matmul {n}^3 with TF32 tensor math "
+                   f"(torch allow_tf32), best of {reps}, CUDA events"}
+
+
+def time_steps(step, stream, dev, warmup=5, target_ms=40.0, min_steps=20,
+               max_steps=4000):
+    """Secondary timing of one step function: `warmup` untimed steps, a
+    short calibration, then enough steps for about target_ms (at least
+    min_steps) between CUDA events on `stream`, with the SM clocks seen
+    meanwhile.  Returns (ms per step, steps, clock record)."""
+    import torch
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(5):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est = max(e0.elapsed_time(e1) / 5, 1e-4)
+    steps = int(min(max_steps, max(min_steps, target_ms / est)))
+    sampler = ClockSampler(_gpu_uuid(dev))
+    if sampler.nvml is None:
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop(t0, time.perf_counter())
+    return e0.elapsed_time(e1) / steps, steps, clocks
+
+
+def sub_record(w, ms, steps, clocks, kernel, entry, peaks, tf32_peak,
+               fp32_peak):
+    """One secondary figure: TFLOP/s over the step time, with the roof that
+    bounds the kernel (tensor/3 for 3xTF32, the FFMA probe for the FFMA
+    kernels, the copy bandwidth where intensity x bandwidth is lower)."""
+    tflops = w.flops / (ms / 1e3) / 1e12
+    rec = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+           "entry": entry, "kernel": kernel, "value": tflops,
+           "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+           "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_min_mhz",
+                                                 "samples", "reasons")}}
+    bw_roof = w.flops / w.bytes * peaks["hbm_gbs"] / 1e3
+    if kernel.startswith("tf32x3"):
+        if bw_roof < tf32_peak / 3.0:
+            gbs = w.bytes / (ms / 1e3) / 1e9
+            rec["roofline"] = {"bound": "hbm", "achieved": gbs,
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": gbs / peaks["hbm_gbs"]}
+        else:
+            rec["roofline"] = {"bound": "tensor", "achieved": tflops,
+                               "peak": tf32_peak / 3.0, "unit": "TFLOP/s",
+                               "frac": tflops / (tf32_peak / 3.0)}
+    else:
+        rec["roofline"] = {"bound": "alu", "achieved": tflops,
+                           "peak": fp32_peak, "unit": "TFLOP/s",
+                           "frac": tflops / fp32_peak}
+    return rec
+
+
+def run_sub_records(dev, stream, head_sets, peaks, tf32_peak, fp32_peak):
+    """Secondary figures of the default run, each timed on its own (CUDA
+    events, its own clock record), none of them part of the headline:
+
+    * 4096^3 through gemm_f32 itself (no lent scratch: nothing split);
+    * 4096^3 on the two FFMA kernels, forced (TMA-fed and cp.async);
+    * the other workloads through gemm_f32_ws with the scratch it asks
+      for, as the headline runs 4096^3.
+    Inputs rotate over sets together larger than 2x the L2."""
+    import torch
+
+    from dense_fp32_matrix_02_gb300 import gemm as G
+    from dense_fp32_matrix_02_gb300 import synth
+
+    w = synth.WORKLOADS["sq4096"]
+    h = stream.cuda_stream
+    out = []
+
+    def forced(algo):
+        def step(i):
+            ta, tb, tc = head_sets[i % len(head_sets)]
+            G.gemm_f32_ptr(w.M, w.N, w.K, ta.data_ptr(), w.K, tb.data_ptr(),
+                           w.N, tc.data_ptr(), w.N, h, algo)
+        return step
+
+    for algo, entry, kernel in ((0, "gemm_f32", "tf32x3"),
+                                (2, "gemm_f32_ex(TMA)", "tma"),
+                                (1, "gemm_f32_ex(SIMT)", "simt")):
+        ms, steps, clocks = time_steps(forced(algo), stream, dev)
+        out.append(sub_record(w, ms, steps, clocks, kernel, entry, peaks,
+                              tf32_peak, fp32_peak))
+        if algo == 0:
+            out[-1]["note"] = "no scratch lent: the last round of tiles " \
+                              "runs whole"
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    for name in ("mlp", "sq1024", "rag1000", "skinny", "sq64"):
+        v = synth.WORKLOADS[name]
+        a, b = v.operands()
+        ta0 = torch.from_numpy(a).to(dev)
+        tb0 = torch.from_numpy(b).to(dev)
+        n = rotating_sets(v.bytes, l2)
+        sets = [(ta0 if i == 0 else ta0.clone(),
+                 tb0 if i == 0 else tb0.clone(),
+                 torch.empty(v.M, v.N, device=dev)) for i in range(n)]
+        need = G.workspace_size(v.M, v.N, v.K)
+        ws = torch.empty(max(need // 4, 1), device=dev) if need else None
+        p = G.plan(v.M, v.N, v.K)
+        kernel = G.ALGO_NAMES.get(p["algo"], str(p["algo"]))
+        if kernel == "tf32x3" and p["variant"] == "streaming":
+            kernel = "tf32x3_stream"
+
+        def step(i, v=v, sets=sets, ws=ws, need=need):
+            ta, tb, tc = sets[i % len(sets)]
+            G.gemm_f32_ws_ptr(v.M, v.N, v.K, ta.data_ptr(), v.K,
+                              tb.data_ptr(), v.N, tc.data_ptr(), v.N,
+                              ws.data_ptr() if ws is not None else 0, need, h)
+
+        ms, steps, clocks = time_steps(step, stream, dev)
+        rec = sub_record(v, ms, steps, clocks, kernel, "gemm_f32_ws", peaks,
+                         tf32_peak, fp32_peak)
+        rec["plan"] = p
+        out.append(rec)
+        del sets, ws
+    if G.device_status() != 0:
+        raise SystemExit("kernel status word set during the sub-records")
+    return out
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args, w, config):
     import torch
@@ -708,27 +904,33 @@ def run_ours(args, w, config):
     probe = measure_ffma_peak(dev, stream)
     fp32_nameplate = 2.0 * sms * FP32_LANES_PER_SM * smax * 1e6 / 1e12
     fp32_peak = probe["tflops"]
+    # the TF32 tensor rate, measured here (cuBLAS), for the 3xTF32 roof
+    tf32_probe = measure_tf32_peak(dev, stream)
+    tf32 = tf32_probe["tflops"]
     achieved = flops / (kernel_ms / 1e3) / 1e12
     algo_name = G.ALGO_NAMES.get(ran, str(ran))
     if algo_name == "tf32x3" and not batched and algo == 0:
         if G.plan(w.M, w.N, w.K)["variant"] == "streaming":
             algo_name = "tf32x3_stream"  # B held in tensor memory
     bw_roof = (flops / (w.bytes * args.batch)) * peaks["hbm_gbs"] / 1e3
-    if algo_name in ("tf32x3", "tf32x3_stream") and \
-            bw_roof < peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0:
+    if algo_name in ("tf32x3", "tf32x3_stream") and bw_roof < tf32 / 3.0:
         # memory-bound shape: the copy bandwidth is the roof
         roof = hbm_roofline(flops, w.bytes * args.batch, kernel_ms, peaks,
-                            peaks_src,
-                            peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0,
-                            achieved)
+                            peaks_src, tf32 / 3.0, achieved)
     elif algo_name in ("tf32x3", "tf32x3_stream"):
-        # three TF32 tensor products per algorithmic multiply-add; TF32
-        # dense rate = bf16 rate x (1.1 / 2.25), the nominal ratio
-        tf32 = peaks["bf16_tflops"] * (1.1 / 2.25)
+        # three TF32 tensor products per algorithmic multiply-add: the roof
+        # is the TF32 rate cuBLAS reached in this run, / 3
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf32 / 3.0,
                 "unit": "TFLOP/s", "frac": achieved / (tf32 / 3.0),
-                "peak_source": f"{peaks_src} bf16 burst {peaks['bf16_tflops']}"
-                               " x 1.1/2.25 (nominal TF32/bf16), / 3 products"}
+                "peak_source": "measured in this run: cuBLAS TF32 burst "
+                               f"{tf32:.1f} TFLOP/s at "
+                               f"{tf32_probe['sm_mhz']} MHz median, / 3 "
+                               "products"}
+        # the earlier derived figure, for comparison: the driver's bf16
+        # burst x the nominal TF32/bf16 ratio (1.1/2.25), / 3
+        derived = peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0
+        roof["peak_derived_from_bf16"] = derived
+        roof["frac_derived_from_bf16"] = achieved / derived
         # the tensor pipe's own TF32 rate (ncu peak_sustained: 4096 flop per
         # clock per SM) at the run's maximum clock, / 3 products
         hw = TF32_FLOP_PER_CLK_PER_SM * sms * smax * 1e6 / 1e12 / 3.0
@@ -769,6 +971,7 @@ def run_ours(args, w, config):
         "pct_fp32_roofline_nameplate":
             100.0 * (value / world) / fp32_roof_nameplate,
         "ffma_probe": probe,
+        "tf32_probe": tf32_probe,
         "samples": samples,
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
@@ -779,6 +982,11 @@ def run_ours(args, w, config):
         "clocks": clocks,
         "wall_s_timed": wall,
     }
+    if (rank == 0 and world == 1 and not args.no_sub_records
+            and w.name == "sq4096" and algo == 0 and not batched
+            and not fused and not args.graph):
+        line["sub_records"] = run_sub_records(dev, stream, sets, peaks, tf32,
+                                              fp32_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, a, b, args.cpu_seconds)
     if rank == 0:
