@@ -199,7 +199,8 @@ struct FfmaTile {
 // Same 8×8 register tile with A stored transposed, as in "3 · La mémoire
 // partagée", §3.4 (As[BK][BM]): per k a thread reads its eight A values as
 // two 16-byte loads and its eight B values as two more, so 4 shared loads
-// feed 64 FFMA and only 16 operand registers are live per k step.
+// feed 64 multiply-adds (32 packed two-lane FMAs, as in FfmaTile) and only
+// 16 operand registers are live per k step.
 //
 // Shared-memory layout of one stage (fp32):
 //   A: BK rows (k) × BM floats (m).  The 16-byte chunk c = m/4 of row k sits
@@ -226,13 +227,15 @@ struct FfmaTileT {
   static constexpr int kStageFloatsA = BM * BK;
   static constexpr int kStageFloatsB = BK * BN;
   static constexpr int kStageBytes = 4 * (kStageFloatsA + kStageFloatsB);
-  using Acc = float[8][8];
+  // The 8×8 accumulators as pairs: acc[i][p] holds columns 2p and 2p + 1
+  // of row_of(i) (in the column order of `store`).
+  using Acc = unsigned long long[8][4];
 
   static __device__ __forceinline__ void zero(Acc& acc) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;  // two +0.0f
   }
 
   int a_off[8];  // (c ^ g) * 4 for g = 0..7, c = row0 / 4
@@ -270,7 +273,7 @@ struct FfmaTileT {
 
   __device__ __forceinline__ void compute(const float* __restrict__ As,
                                           const float* __restrict__ Bs,
-                                          float (&acc)[8][8]) const {
+                                          Acc& acc) const {
     const float* b_base = Bs + b_col_off;
 #pragma unroll
     for (int k = 0; k < BK; ++k) {
@@ -289,11 +292,15 @@ struct FfmaTileT {
         b1 = *reinterpret_cast<const float4*>(b_base + k * BN + 16);
       }
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const unsigned long long bp[4] = {
+          pack_f32x2(b0.x, b0.y), pack_f32x2(b0.z, b0.w),
+          pack_f32x2(b1.x, b1.y), pack_f32x2(b1.z, b1.w)};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+        const unsigned long long aa = pack_f32x2(av[i], av[i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) fma_f32x2(acc[i][j], aa, bp[j]);
+      }
     }
   }
 
@@ -302,8 +309,13 @@ struct FfmaTileT {
   }
 
   __device__ __forceinline__ void store(const Problem& p, int bm, int bn,
-                                        bool c_vec,
-                                        const float (&acc)[8][8]) const {
+                                        bool c_vec, const Acc& acc2) const {
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        unpack_f32x2(acc2[i][j], acc[i][2 * j], acc[i][2 * j + 1]);
     const bool interior = (bm + BM <= p.M) && (bn + BN <= p.N);
     const bool epi = p.bias != nullptr || p.act != kActNone;
     // the bias of the thread's 8 columns, loaded once (C stores may alias it)

@@ -109,7 +109,11 @@ int choose_simt_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   if (N <= 64) return kSimt128x64x16;
   const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
   if (tiles < d.sm_count) return kSimt128x64x16;
-  return kSimtKm128x128x32Occ1;
+  // A transposed on its way into shared memory (4-byte copies) measured
+  // ahead of the K-major copy once both tiles issue packed two-lane FMAs:
+  // 4096^3 aligned 46.9 against 44.1 TFLOP/s (unaligned operands take
+  // this tile either way: 41.8)
+  return kSimt128x128x32Occ1;
 }
 
 int choose_tc_cfg(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {

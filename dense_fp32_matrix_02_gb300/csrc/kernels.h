@@ -33,20 +33,19 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block,
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// SIMT tile configurations (BM x BN x BK); "Occ1" variants let a thread use
-// up to 255 registers at one CTA per SM instead of 128 at two.
+// SIMT tile configurations (BM x BN x BK).  "Occ1" variants let a thread
+// use up to 255 registers at one 256-thread CTA per SM; the 128 x 64 and
+// 64 x 64 tiles run 128-thread CTAs, three and four per SM.  Every one
+// compiles without register spills (128 x 128 tiles at two CTAs per SM,
+// capped at 128 registers a thread, spilled and are not offered).
 enum SimtCfg {
-  kSimt128x128x16 = 0,
-  kSimt128x64x16 = 1,
-  kSimt128x128x32 = 2,
-  kSimt64x64x16 = 3,
-  kSimt128x128x16Occ1 = 4,
-  kSimt128x128x8 = 5,
-  kSimt128x128x32Occ1 = 6,
-  kSimt128x128x16Occ1S6 = 7,
-  kSimtKm128x128x32Occ1 = 8,  // A kept K-major (16-byte copies)
-  kSimtKm128x128x16Occ1 = 9,
-  kSimtCfgCount = 10
+  kSimt128x64x16 = 0,
+  kSimt64x64x16 = 1,
+  kSimt128x128x16Occ1 = 2,
+  kSimt128x128x32Occ1 = 3,
+  kSimt128x128x16Occ1S6 = 4,
+  kSimtKm128x128x32Occ1 = 5,  // A kept K-major (16-byte copies)
+  kSimtCfgCount = 6
 };
 
 // The driver's cuTensorMapEncodeTiled, looked up once (thread-safe); null

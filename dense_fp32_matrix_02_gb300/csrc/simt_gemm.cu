@@ -242,18 +242,12 @@ template <bool VEC>
 cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
                        cudaStream_t stream) {
   switch (cfg) {
-    case kSimt128x128x16:
-      return launch_cfg<128, 128, 16, 4, VEC, 2>(p, c_vec, stream);
     case kSimt128x64x16:
       return launch_cfg<128, 64, 16, 4, VEC, 3>(p, c_vec, stream);
-    case kSimt128x128x32:
-      return launch_cfg<128, 128, 32, 3, VEC, 2>(p, c_vec, stream);
     case kSimt64x64x16:
       return launch_cfg<64, 64, 16, 4, VEC, 4>(p, c_vec, stream);
     case kSimt128x128x16Occ1:
       return launch_cfg<128, 128, 16, 4, VEC, 1>(p, c_vec, stream);
-    case kSimt128x128x8:
-      return launch_cfg<128, 128, 8, 6, VEC, 2>(p, c_vec, stream);
     case kSimt128x128x32Occ1:
       return launch_cfg<128, 128, 32, 4, VEC, 1>(p, c_vec, stream);
     case kSimt128x128x16Occ1S6:
@@ -262,9 +256,6 @@ cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
       // 16-byte copies of A need VEC (aligned A, lda % 4 == 0)
       return VEC ? launch_cfg<128, 128, 32, 4, true, 1, true>(p, c_vec, stream)
                  : launch_cfg<128, 128, 32, 4, false, 1>(p, c_vec, stream);
-    case kSimtKm128x128x16Occ1:
-      return VEC ? launch_cfg<128, 128, 16, 6, true, 1, true>(p, c_vec, stream)
-                 : launch_cfg<128, 128, 16, 6, false, 1>(p, c_vec, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -24,7 +24,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 from dense_fp32_matrix_02_gb300 import gemm as G  # noqa: E402
 
 DEV = torch.device("cuda:0")
-SIMT_CFGS = list(range(10))
+SIMT_CFGS = list(range(6))  # kSimtCfgCount
 
 
 def _env(name, value):
