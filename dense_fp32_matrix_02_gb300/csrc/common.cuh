@@ -58,6 +58,56 @@ __device__ __forceinline__ float apply_epilogue(float v, const float* bias,
   return epilogue_act(v, act);
 }
 
+// The operands as plain row-major arrays, for the tensor kernels' repair of
+// non-finite outputs: element (m, k) of the product's left operand is
+// A[m·lda + k] (A[k·lda + m] when transA), element (k, n) of the right one
+// B[k·ldb + n] (B[n·ldb + k] when transB); matrix z of a batch starts sA,
+// sB elements further.
+struct RawOperands {
+  const float* A;
+  long long lda, sA;
+  const float* B;
+  long long ldb, sB;
+  int transA, transB;
+};
+
+// Σ_k a(m, k)·b(k, n) over k in [k0, k1), ascending, with fmaf: the IEEE
+// single-precision value of one element of the product (o.A, o.B already
+// at the matrix of the batch in question).
+//
+// The three-TF32 split cannot follow IEEE arithmetic when an operand is
+// infinite: x = ±Inf gives small = Inf − Inf = NaN, so every output that
+// operand reaches comes out NaN, where IEEE gives ±Inf (or NaN only for
+// Inf·0 or Inf − Inf).  Finite operands never produce a NaN there, so an
+// output that is NaN has a non-finite operand in its row of A or column of
+// B, and its IEEE value is non-finite too; the tensor kernels recompute
+// exactly those elements with this loop before storing them (no cost on
+// the main loop: one compare per output and one warp vote in the
+// epilogue, and the loop runs only where a NaN appeared).
+__device__ __forceinline__ float ieee_dot(const RawOperands& o, int m, int n,
+                                          int k0, int k1) {
+  const float* a = o.A;
+  const float* b = o.B;
+  float s = 0.f;
+  for (int k = k0; k < k1; ++k) {
+    const float x = o.transA ? a[(long long)k * o.lda + m]
+                             : a[(long long)m * o.lda + k];
+    const float y = o.transB ? b[(long long)n * o.ldb + k]
+                             : b[(long long)k * o.ldb + n];
+    s = fmaf(x, y, s);
+  }
+  return s;
+}
+
+// true if any of the CNT values (fp32 bit patterns) is a NaN.
+template <int CNT>
+__device__ __forceinline__ bool any_nan(const uint32_t (&v)[CNT]) {
+  bool any = false;
+#pragma unroll
+  for (int r = 0; r < CNT; ++r) any |= (v[r] & 0x7fffffffu) > 0x7f800000u;
+  return any;
+}
+
 // Bounded-wait configuration shared by all pipelined kernels.
 struct WaitCfg {
   long long limit;        // ns of %globaltimer before a wait gives up

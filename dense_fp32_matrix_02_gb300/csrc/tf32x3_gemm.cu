@@ -145,7 +145,8 @@ constexpr int smem_bytes() {
 
 // Rounds x to the nearest TF32 value (ties to even) and returns the exact
 // remainder x - big.  Values TF32 holds exactly give small = 0; NaN stays
-// NaN; ±Inf gives small = NaN (so an Inf input yields non-finite outputs).
+// NaN; ±Inf gives small = NaN (so an Inf input turns the outputs it reaches
+// into NaN, which the epilogue then recomputes in IEEE arithmetic).
 __device__ __forceinline__ void tf32_split(float x, uint32_t& big,
                                            uint32_t& small) {
   const uint32_t u = __float_as_uint(x);
@@ -187,7 +188,8 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                        int tiles_n, int full_tiles, int tail_splits,
                        int kb_per_split, float* partials, long long sC,
                        int batched_ab, int store_tma,
-                       const float* bias, int act, WaitCfg wc) {
+                       const float* bias, int act, RawOperands raw,
+                       WaitCfg wc) {
   // batch: matrix blockIdx.z; tensor-map batch coordinates are z for a
   // batched operand and 0 for one shared by every product (batched_ab bits
   // 0 = A, 1 = B); C advances by sC per product.
@@ -465,6 +467,12 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         griddep_launch_dependents();  // the main loop is over
         const int n = bn + n_loc;
         const int c_begin = h * (kAccCols / 2);
+        // NaN outputs (an infinite operand) are recomputed in IEEE
+        // arithmetic over this CTA's k range (see ieee_dot)
+        RawOperands ro = raw;
+        ro.A += za * raw.sA;
+        ro.B += zb * raw.sB;
+        const int k0 = kb0 * kBK, k1 = min(K, (kb0 + nk) * kBK);
         // this lane's column n has one bias value; load it once
         const bool epi = whole && (bias != nullptr || act != 0);
         const float bias_n =
@@ -486,6 +494,8 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
             tmem_ld16(tmem + lane_bits + c_begin + 32 * j, v);
             tmem_ld16(tmem + lane_bits + c_begin + 32 * j + 16, v + 16);
             tmem_ld_wait();
+            const bool nan_here = any_nan(v);
+            const bool fix = __any_sync(0xffffffffu, nan_here);
             if (epi) {
 #pragma unroll
               for (int r = 0; r < 32; ++r) {
@@ -500,6 +510,23 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                   stg + j * 4096 + r * 128 +
                   ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2))) =
                   v[r];
+            if (fix && nan_here && n < N) {
+#pragma unroll 1
+              for (int r = 0; r < 32; ++r) {
+                uint32_t* slot = reinterpret_cast<uint32_t*>(
+                    stg + j * 4096 + r * 128 +
+                    ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2)));
+                const float x = __uint_as_float(*slot);
+                const int m = bm + c_begin + 32 * j + r;
+                if (x == x || m >= M) continue;
+                float y = ieee_dot(ro, m, n, k0, k1);
+                if (epi) {
+                  if (bias != nullptr) y += bias_n;
+                  y = epilogue_act(y, act);
+                }
+                *slot = __float_as_uint(y);
+              }
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -526,6 +553,8 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
           uint32_t v[16];
           tmem_ld16(tmem + lane_bits + c0, v);
           tmem_ld_wait();
+          const bool nan_here = any_nan(v);
+          const bool fix = __any_sync(0xffffffffu, nan_here) && nan_here;
           if constexpr (Cf::kTStore) {
             // this lane holds 16 consecutive rows m of column n: they are
             // 16 consecutive elements of row n of the stored transpose
@@ -542,6 +571,12 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                   if (bm + c0 + i < M) dst[i] = __uint_as_float(v[i]);
+              }
+              if (fix) {
+#pragma unroll 1
+                for (int i = 0; i < 16 && bm + c0 + i < M; ++i)
+                  if (dst[i] != dst[i])
+                    dst[i] = ieee_dot(ro, bm + c0 + i, n, k0, k1);
               }
             }
           } else if (n < N) {
@@ -560,6 +595,20 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
               if (m < M)
                 out[(long long)(m - mo) * ldo + (n - no)] =
                     __uint_as_float(v[i]);
+            }
+            if (fix) {
+#pragma unroll 1
+              for (int i = 0; i < 16 && bm + c0 + i < M; ++i) {
+                const int m = bm + c0 + i;
+                float* d = out + (long long)(m - mo) * ldo + (n - no);
+                if (*d == *d) continue;
+                float y = ieee_dot(ro, m, n, k0, k1);
+                if (epi) {
+                  if (bias != nullptr) y += bias_n;
+                  y = epilogue_act(y, act);
+                }
+                *d = y;
+              }
             }
           }
         }
@@ -739,11 +788,20 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       store_tma |= 2;
   }
+  RawOperands raw;
+  raw.A = p.A;
+  raw.lda = p.lda;
+  raw.sA = p.sA;
+  raw.B = p.B;
+  raw.ldb = p.ldb;
+  raw.sB = p.sB;
+  raw.transA = Cf::kTA ? 1 : 0;
+  raw.transB = Cf::kTB ? 1 : 0;
   e = launch_pdl(fn, dim3((unsigned)grid, 1, (unsigned)p.batch),
                  dim3(Cf::kThreads), kSmem, stream, ta, tb, tc, tp, p.C,
                  p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, (int)full, ts,
                  kb_per_split, partials, p.sC, batched_ab, store_tma, p.bias,
-                 p.act, wc);
+                 p.act, raw, wc);
   if (e != cudaSuccess || tail == 0) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
                    p.ldc % 4 == 0)

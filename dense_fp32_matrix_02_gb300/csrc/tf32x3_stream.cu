@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmap_c, float* C,
                          long long ldc, int M, int N, int K, int nb,
                          int tiles, int c_tma, const float* bias, int act,
-                         WaitCfg wc) {
+                         RawOperands raw, WaitCfg wc) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -341,6 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(b));
       const int m0 = t * kTileM + c_begin;
+      // NaN outputs (an infinite operand) are recomputed in IEEE
+      // arithmetic after staging or storing (see ieee_dot)
+      const bool nan_here = any_nan(v);
+      const bool fix = __any_sync(0xffffffffu, nan_here) && nan_here && n < N;
       if (epi) {
 #pragma unroll
         for (int r = 0; r < kAccCols / 2; ++r)
@@ -362,6 +366,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint32_t*>(
                 stg + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
                                  ((lane & 3) << 2))) = v[32 * j + r];
+          if (fix) {
+#pragma unroll 1
+            for (int r = 0; r < 32; ++r) {
+              uint32_t* slot = reinterpret_cast<uint32_t*>(
+                  stg + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
+                                   ((lane & 3) << 2)));
+              const float x = __uint_as_float(*slot);
+              const int m = m0 + 32 * j + r;
+              if (x == x || m >= M) continue;
+              float y = ieee_dot(raw, m, n, 0, K);
+              if (epi) y = epilogue_act(y + bias_n, act);
+              *slot = __float_as_uint(y);
+            }
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && m0 + 32 * j < M) {
@@ -374,6 +392,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < kAccCols / 2; ++r)
           if (m0 + r < M) C[(long long)(m0 + r) * ldc + n] = __uint_as_float(v[r]);
+        if (fix) {
+#pragma unroll 1
+          for (int r = 0; r < kAccCols / 2 && m0 + r < M; ++r) {
+            float* d = C + (long long)(m0 + r) * ldc + n;
+            if (*d == *d) continue;
+            float y = ieee_dot(raw, m0 + r, n, 0, K);
+            if (epi) y = epilogue_act(y + bias_n, act);
+            *d = y;
+          }
+        }
       }
     }
     if (c_tma && lane == 0) bulk_wait_group<0>();  // C written
@@ -449,9 +477,18 @@ cudaError_t launch_tf32x3_stream(const Problem& p, int sm_count,
   if (e != cudaSuccess) return e;
   const long long tiles = ((long long)p.M + kTileM - 1) / kTileM;
   const int grid = (int)(tiles < sm_count ? tiles : sm_count);
+  RawOperands raw;
+  raw.A = p.A;
+  raw.lda = p.lda;
+  raw.sA = 0;
+  raw.B = p.B;
+  raw.ldb = p.ldb;
+  raw.sB = 0;
+  raw.transA = 0;
+  raw.transB = 0;
   return launch_pdl(tf32x3_stream_kernel, dim3(grid), dim3(kThreads),
                     kSmemBytes, stream, ta, tb, tc, p.C, p.ldc, p.M, p.N, p.K,
-                    nb, (int)tiles, c_tma, p.bias, p.act, wc);
+                    nb, (int)tiles, c_tma, p.bias, p.act, raw, wc);
 }
 
 }  // namespace gemm_f32_impl

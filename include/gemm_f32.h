@@ -80,8 +80,10 @@ typedef enum {
     GEMM_F32_ALGO_TMA = 2,
     /* Tensor-core kernel (tcgen05, TMEM accumulator) computing each product
      * as three TF32 products of a big/small operand split, accumulated in
-     * fp32; within the single-precision tolerance for finite inputs (an Inf
-     * input may yield NaN where IEEE arithmetic gives ±Inf).  Needs A and B
+     * fp32; within the single-precision tolerance for finite inputs.  NaN
+     * and ±Inf inputs give the IEEE result: outputs the split turns into
+     * NaN (an infinite operand) are recomputed in IEEE single precision
+     * before they are stored, so ±Inf stays ±Inf.  Needs A and B
      * 16-byte aligned, lda and ldb multiples of 4, K >= 1 and an sm_10x GPU.
      * GEMM_F32_ALGO_AUTO picks it whenever these hold. */
     GEMM_F32_ALGO_TF32X3 = 3

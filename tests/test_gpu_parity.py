@@ -301,19 +301,121 @@ def test_nan_and_inf_propagate_simt():
     assert_within_tolerance(c[fin], ref[fin], bound[fin], 64, "finite part")
 
 
-def test_nan_and_inf_tf32x3():
-    """3xTF32: NaN propagates; an Inf input makes its outputs non-finite
-    (NaN where IEEE gives ±Inf, from Inf·0 in a cross term); the outputs
-    that no non-finite input reaches stay within tolerance."""
-    a, b = synth.make_operands(64, 64, 64, seed=3)
-    a[5, 7] = np.nan
-    b[9, 11] = np.inf
-    c = run_gpu(a, b, G.ALGO_TF32X3)
+def _plant_nonfinite(a, b):
+    """NaN and ±Inf in A and B, at places that give every IEEE case: a NaN
+    row, +Inf and -Inf rows and columns, Inf·0 (B holds exact zeros),
+    Inf·Inf, and +Inf meeting -Inf in one sum."""
+    M, K = a.shape
+    N = b.shape[1]
+    a, b = a.copy(), b.copy()
+    a[5 % M, 7 % K] = np.nan
+    b[9 % K, 11 % N] = np.inf
+    a[(M - 3) % M, (K - 2) % K] = -np.inf
+    a[20 % M, 3 % K] = np.inf
+    b[3 % K, 40 % N] = np.inf            # Inf·Inf in C[20, 40]
+    b[(K - 1) % K, 2 % N] = -np.inf       # with a[20, 3]: +Inf and -Inf
+    a[20 % M, (K - 1) % K] = 1.0          #   meet in C[20, 2]
+    return a, b
+
+
+def _check_ieee(c, a, b, what, tol_scale=1.0):
+    """Non-finite outputs exactly where IEEE (the oracle) has them, with the
+    same NaN / ±Inf class; the finite ones within tolerance."""
     ref, bound, _ = oracle.gemm(a, b)
-    assert np.array_equal(np.isfinite(c), np.isfinite(ref))
-    assert np.isnan(c[np.isnan(ref)]).all()
+    K = a.shape[1]
+    assert np.array_equal(np.isnan(c), np.isnan(ref)), what + " NaN set"
+    assert np.array_equal(np.isposinf(c), np.isposinf(ref)), what + " +Inf"
+    assert np.array_equal(np.isneginf(c), np.isneginf(ref)), what + " -Inf"
     fin = np.isfinite(ref)
-    assert_within_tolerance(c[fin], ref[fin], bound[fin], 64, "finite part")
+    assert fin.sum() > c.size // 2
+    assert_within_tolerance(c[fin], ref[fin], tol_scale * bound[fin], K,
+                            what + " finite part")
+
+
+@pytest.mark.parametrize("algo", [G.ALGO_AUTO, G.ALGO_TF32X3],
+                         ids=["auto", "tf32x3"])
+@pytest.mark.parametrize("shape,ws", [
+    ((64, 64, 64), False),            # one 128-row tile
+    ((300, 260, 1000), True),         # 128-row tiles split over K
+    ((512, 384, 2048), True),         # 256-row tiles split over K
+    ((700, 300, 2100), False),        # 256-row tiles, whole
+    ((2100, 2420, 1000), True)],      # whole tiles and a split tail
+    ids=lambda x: "x".join(map(str, x)) if isinstance(x, tuple) else str(x))
+def test_nan_and_inf_ieee_tensor(algo, shape, ws):
+    """The 3xTF32 kernels give IEEE results for NaN and Inf inputs: the
+    outputs the split turns into NaN are recomputed in IEEE arithmetic, so
+    ±Inf comes out as ±Inf and NaN only where IEEE has NaN (Inf·0,
+    Inf − Inf, a NaN operand)."""
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=K, dist_a="uniform",
+                               dist_b="int")
+    a, b = _plant_nonfinite(a, b)
+    if ws:
+        if algo != G.ALGO_AUTO:
+            pytest.skip("scratch goes with the automatic plan")
+        c, need = run_gpu_ws(a, b)
+        assert need > 0
+    else:
+        c = run_gpu(a, b, algo, pad=True)
+    _check_ieee(c, a, b, f"{shape}")
+    assert G.device_status() == 0
+
+
+def test_nan_and_inf_ieee_streaming_kernel():
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    M = 128 * sms + 77
+    assert G.plan(M, 64, 64)["variant"] == "streaming"
+    a, b = synth.make_operands(M, 64, 64, seed=8, dist_b="int")
+    a, b = _plant_nonfinite(a, b)
+    a[M - 1, 0] = np.inf  # the ragged last tile
+    _check_ieee(run_gpu(a, b), a, b, "streaming")
+
+
+@pytest.mark.parametrize("form", ["NT", "TT", "TN"])
+def test_nan_and_inf_ieee_transposed_forms(form):
+    """Operands read transposed in place (NT, TN: the converters transpose
+    A; TT: the swapped product stored transposed)."""
+    M, N, K = 300, 260, 520
+    a, b = synth.make_operands(M, N, K, seed=3, dist_b="int")
+    a, b = _plant_nonfinite(a, b)
+    ta, tb = form[0] == "T", form[1] == "T"
+    sa = torch.from_numpy(a.T.copy() if ta else a).to(DEV)
+    sb = torch.from_numpy(b.T.copy() if tb else b).to(DEV)
+    c = torch.full((M, N), -7.0, device=DEV)
+    # no scratch: Aᵀ·B is read in place too
+    G.gemm_f32_batched_ptr(int(ta), int(tb), M, N, K, sa.data_ptr(),
+                           sa.shape[1], 0, sb.data_ptr(), sb.shape[1], 0,
+                           c.data_ptr(), N, 0, 1,
+                           torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    _check_ieee(c.cpu().numpy(), a, b, form)
+    if form == "TN":  # and through the transposed copy in scratch
+        c2 = G.gemm_f32_batched(sa, sb, trans_a=True)
+        torch.cuda.synchronize()
+        _check_ieee(c2[0].cpu().numpy(), a, b, "TN copy")
+
+
+def test_nan_and_inf_ieee_fused_epilogue():
+    """bias + GELU after the repair: GELU(+Inf) = +Inf, GELU(-Inf) and
+    GELU(NaN) = NaN, as the oracle's float64 epilogue gives."""
+    M, N, K = 300, 260, 1000
+    a, b = synth.make_operands(M, N, K, seed=5, dist_b="int")
+    a, b = _plant_nonfinite(a, b)
+    bias = synth.make_operands(1, N, 1, seed=6)[1][0]
+    c = G.gemm_f32_bias_act(torch.from_numpy(a).to(DEV),
+                            torch.from_numpy(b).to(DEV),
+                            torch.from_numpy(bias).to(DEV), G.ACT_GELU)
+    torch.cuda.synchronize()
+    c = c.cpu().numpy()
+    ref, bound, _ = oracle.gemm(a, b)
+    want = oracle.epilogue(ref, bias, G.ACT_GELU)
+    assert np.array_equal(np.isnan(c), np.isnan(want))
+    assert np.array_equal(np.isposinf(c), np.isposinf(want))
+    assert np.array_equal(np.isneginf(c), np.isneginf(want))
+    fin = np.isfinite(want)
+    tol = 1.2 * oracle.tolerance(bound, K) + 4 * 2.0**-24 * (
+        np.abs(oracle.epilogue(ref, bias, 0)) + np.abs(want))
+    assert (np.abs(c[fin] - want[fin]) <= tol[fin]).all()
 
 
 def test_stream_ordering_on_side_stream():
