@@ -2,7 +2,12 @@
 
 Each CUDA translation unit compiles in parallel to an object file under
 ``_build/``; the objects link into ``libgemm_f32.so`` next to this file.
-``python -m dense_fp32_matrix_02_gb300.build [--verbose-ptxas]``.
+``python -m dense_fp32_matrix_02_gb300.build [--verbose-ptxas] [--checked]``.
+
+``--checked`` (``build(checked=True)``) builds ``libgemm_f32_debug.so``
+instead, with GEMM_F32_BOUNDS_CHECK=1: the FFMA and tensor kernels then test
+every shared-memory, tensor-memory and global index against its extent and
+report a failure through the kernel status word, skipping the access.
 """
 
 from __future__ import annotations
@@ -19,6 +24,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 OUTPUT = os.path.join(HERE, "libgemm_f32.so")
+OUTPUT_CHECKED = os.path.join(HERE, "libgemm_f32_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -44,9 +50,12 @@ def _deps():
         os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
 
 
-def _compile(src: str, ptxas_verbose: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, ptxas_verbose: bool, checked: bool = False) -> str:
+    bdir = os.path.join(BUILD_DIR, "checked") if checked else BUILD_DIR
+    obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    if checked:
+        cmd.append("-DGEMM_F32_BOUNDS_CHECK=1")
     if ptxas_verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -57,24 +66,30 @@ def _compile(src: str, ptxas_verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compiles the library if any source is newer than it; returns its path."""
-    if (not force and not ptxas_verbose and os.path.exists(OUTPUT)
-            and os.path.getmtime(OUTPUT) >= max(os.path.getmtime(p)
+def build(force: bool = False, ptxas_verbose: bool = False,
+          checked: bool = False) -> str:
+    """Compiles the library (the checked one with `checked`) if any source
+    is newer than it; returns its path."""
+    output = OUTPUT_CHECKED if checked else OUTPUT
+    if (not force and not ptxas_verbose and os.path.exists(output)
+            and os.path.getmtime(output) >= max(os.path.getmtime(p)
                                                  for p in _deps())):
-        return OUTPUT
-    os.makedirs(BUILD_DIR, exist_ok=True)
+        return output
+    os.makedirs(os.path.join(BUILD_DIR, "checked") if checked else BUILD_DIR,
+                exist_ok=True)
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, ptxas_verbose), srcs))
-    tmp = OUTPUT + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, ptxas_verbose, checked),
+                           srcs))
+    tmp = output + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, OUTPUT)
-    return OUTPUT
+    os.replace(tmp, output)
+    return output
 
 
 if __name__ == "__main__":
-    print(build(force=True, ptxas_verbose="--verbose-ptxas" in sys.argv))
+    print(build(force=True, ptxas_verbose="--verbose-ptxas" in sys.argv,
+                checked="--checked" in sys.argv))

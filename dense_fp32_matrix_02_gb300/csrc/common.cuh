@@ -14,6 +14,7 @@ enum : unsigned int {
   kStatusTimeoutEmpty = 2u,  // the producer gave up waiting for an empty stage
   kStatusTimeoutDrain = 4u,  // copies still in flight when giving up
   kStatusTimeoutMma = 8u,    // tensor-core completion wait gave up
+  kStatusBounds = 16u,       // checked build: an index out of its extent
 };
 
 // Debug flags passed to the pipelined kernels (tests only).
@@ -42,6 +43,8 @@ struct Problem {
   // fused epilogue: C = act(A·B + bias), bias indexed by column (or NULL)
   const float* bias = nullptr;
   int act = 0;  // 0 identity, 1 GELU
+  // kernel status word (the checked build reports out-of-extent indices)
+  unsigned int* status = nullptr;
 };
 
 enum : int { kActNone = 0, kActGelu = 1 };
@@ -324,6 +327,80 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 __device__ __forceinline__ void record_status(unsigned int* status,
                                               unsigned int bit) {
   if (status) atomicOr(status, bit);
+}
+
+// ------------------------------------------------ checked build
+// Built with GEMM_F32_BOUNDS_CHECK=1 (libgemm_f32_debug.so), the FFMA and
+// tensor kernels check every shared-memory, tensor-memory and global index
+// they compute against the extent it must lie in (the stage buffer, the
+// TMEM allocation, the matrix); a failed check sets kStatusBounds in the
+// status word and the access is skipped, so the kernel neither faults nor
+// touches memory it does not own.  It stands in for a memory checker.  In
+// the normal build every check is the constant true and compiles away.
+#ifndef GEMM_F32_BOUNDS_CHECK
+#define GEMM_F32_BOUNDS_CHECK 0
+#endif
+
+// [p, p + bytes) inside [base, base + extent)?  (generic addresses: global
+// memory, or shared memory through a generic pointer)
+__device__ __forceinline__ bool span_ok(const void* p, long long bytes,
+                                        const void* base, long long extent,
+                                        unsigned int* status) {
+#if GEMM_F32_BOUNDS_CHECK
+  const long long off = reinterpret_cast<const char*>(p) -
+                        reinterpret_cast<const char*>(base);
+  if (off < 0 || off + bytes > extent) {
+    record_status(status, kStatusBounds);
+    return false;
+  }
+#else
+  (void)p, (void)bytes, (void)base, (void)extent, (void)status;
+#endif
+  return true;
+}
+
+// The same for a shared-memory address (state space offset).
+__device__ __forceinline__ bool smem_span_ok(uint32_t addr, int bytes,
+                                             uint32_t base, int extent,
+                                             unsigned int* status) {
+#if GEMM_F32_BOUNDS_CHECK
+  if (addr < base || addr + (uint32_t)bytes > base + (uint32_t)extent) {
+    record_status(status, kStatusBounds);
+    return false;
+  }
+#else
+  (void)addr, (void)bytes, (void)base, (void)extent, (void)status;
+#endif
+  return true;
+}
+
+// A tensor-memory access of `cols` columns at taddr (lane in bits 31..16,
+// column in 15..0) inside an allocation of `alloc_cols` columns at `tmem`,
+// by a warp allowed lanes [32·q, 32·q + 32).
+__device__ __forceinline__ bool tmem_span_ok(uint32_t taddr, int cols,
+                                             uint32_t tmem, int alloc_cols,
+                                             int q, unsigned int* status) {
+#if GEMM_F32_BOUNDS_CHECK
+  const uint32_t col = (taddr & 0xffffu) - (tmem & 0xffffu);
+  const uint32_t lane = taddr >> 16;
+  if ((taddr & 0xffffu) < (tmem & 0xffffu) ||
+      col + (uint32_t)cols > (uint32_t)alloc_cols ||
+      lane != (uint32_t)(32 * q)) {
+    record_status(status, kStatusBounds);
+    return false;
+  }
+#else
+  (void)taddr, (void)cols, (void)tmem, (void)alloc_cols, (void)q,
+      (void)status;
+#endif
+  return true;
+}
+
+// Bytes from the first element of a rows × cols matrix with row stride ld
+// (elements) to one past its last: the extent its elements lie in.
+__host__ __device__ __forceinline__ long long matrix_extent_bytes(
+    long long rows, long long cols, long long ld) {
+  return rows > 0 && cols > 0 ? 4 * ((rows - 1) * ld + cols) : 0;
 }
 
 // Tile order: walks GROUP tile-rows at a time so concurrently running CTAs

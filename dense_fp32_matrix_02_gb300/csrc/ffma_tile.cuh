@@ -58,6 +58,32 @@ __device__ __forceinline__ void fma_f32x2(unsigned long long& d,
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
+// The 16 bytes at p, a float4 inside the `floats`-element buffer at base
+// (checked build: zeros and kStatusBounds when outside it).
+__device__ __forceinline__ float4 lds4_checked(const float* p,
+                                               const float* base, int floats,
+                                               unsigned int* st) {
+  return span_ok(p, 16, base, 4LL * floats, st)
+             ? *reinterpret_cast<const float4*>(p)
+             : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Stores of the 8×8 block: v to C at p (float4 or one float), inside the
+// matrix (checked build: skipped and kStatusBounds when outside it).
+__device__ __forceinline__ void stg4_checked(float* p, float4 v,
+                                             const Problem& pr) {
+  if (span_ok(p, 16, pr.C, matrix_extent_bytes(pr.M, pr.N, pr.ldc),
+              pr.status))
+    *reinterpret_cast<float4*>(p) = v;
+}
+
+__device__ __forceinline__ void stg1_checked(float* p, float v,
+                                             const Problem& pr) {
+  if (span_ok(p, 4, pr.C, matrix_extent_bytes(pr.M, pr.N, pr.ldc),
+              pr.status))
+    *p = v;
+}
+
 template <int BM, int BN, int BK>
 struct FfmaTile {
   static_assert(BM % 64 == 0 && BN % 32 == 0, "warp tile is 64 x 32");
@@ -99,10 +125,12 @@ struct FfmaTile {
     b_col_off = col0;
   }
 
-  // acc += A_stage · B_stage for this thread's 8×8 block.
+  // acc += A_stage · B_stage for this thread's 8×8 block.  `st`: the
+  // status word the checked build reports an out-of-stage index to.
   __device__ __forceinline__ void compute(const float* __restrict__ As,
                                           const float* __restrict__ Bs,
-                                          Acc& acc) const {
+                                          Acc& acc,
+                                          unsigned int* st = nullptr) const {
     const float* a_base = As + a_row_off;
     const float* b_base = Bs + b_col_off;
 #pragma unroll
@@ -110,14 +138,14 @@ struct FfmaTile {
       float4 a[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        a[i] = *reinterpret_cast<const float4*>(a_base + i * 8 * BK +
-                                                a_chunk[q]);
+        a[i] = lds4_checked(a_base + i * 8 * BK + a_chunk[q], As,
+                            kStageFloatsA, st);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int k = 4 * q + kk;
-        const float4 b0 = *reinterpret_cast<const float4*>(b_base + k * BN);
+        const float4 b0 = lds4_checked(b_base + k * BN, Bs, kStageFloatsB, st);
         const float4 b1 =
-            *reinterpret_cast<const float4*>(b_base + k * BN + 16);
+            lds4_checked(b_base + k * BN + 16, Bs, kStageFloatsB, st);
         const unsigned long long bp[4] = {
             pack_f32x2(b0.x, b0.y), pack_f32x2(b0.z, b0.w),
             pack_f32x2(b1.x, b1.y), pack_f32x2(b1.z, b1.w)};
@@ -167,9 +195,11 @@ struct FfmaTile {
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const int c = bn + col0 + 16 * g;
-          *reinterpret_cast<float4*>(crow + 16 * g) =
-              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
-                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
+          stg4_checked(crow + 16 * g,
+                       make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                                   val(i, 4 * g + 2, c + 2),
+                                   val(i, 4 * g + 3, c + 3)),
+                       p);
         }
       }
       return;
@@ -183,13 +213,15 @@ struct FfmaTile {
       for (int g = 0; g < 2; ++g) {
         const int c = bn + col0 + 16 * g;
         if (c_vec && c + 3 < p.N) {
-          *reinterpret_cast<float4*>(crow + c) =
-              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
-                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
+          stg4_checked(crow + c,
+                       make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                                   val(i, 4 * g + 2, c + 2),
+                                   val(i, 4 * g + 3, c + 3)),
+                       p);
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (c + j < p.N) crow[c + j] = val(i, 4 * g + j, c + j);
+            if (c + j < p.N) stg1_checked(crow + c + j, val(i, 4 * g + j, c + j), p);
         }
       }
     }
@@ -273,23 +305,24 @@ struct FfmaTileT {
 
   __device__ __forceinline__ void compute(const float* __restrict__ As,
                                           const float* __restrict__ Bs,
-                                          Acc& acc) const {
+                                          Acc& acc,
+                                          unsigned int* st = nullptr) const {
     const float* b_base = Bs + b_col_off;
 #pragma unroll
     for (int k = 0; k < BK; ++k) {
       const float* a_row = As + k * BM + a_off[k & 7];
-      const float4 a0 = *reinterpret_cast<const float4*>(a_row);
-      const float4 a1 = *reinterpret_cast<const float4*>(a_row + 32);
+      const float4 a0 = lds4_checked(a_row, As, kStageFloatsA, st);
+      const float4 a1 = lds4_checked(a_row + 32, As, kStageFloatsA, st);
       float4 b0, b1;
       if (BSWZ) {
         // col0 / 4 has bit 2 clear, so the second chunk (col0 + 16) sits at
         // the first one's position with bit 2 flipped: offset ^ 16 floats
         const float* b_row = Bs + k * BN;
-        b0 = *reinterpret_cast<const float4*>(b_row + b_off[k & 7]);
-        b1 = *reinterpret_cast<const float4*>(b_row + (b_off[k & 7] ^ 16));
+        b0 = lds4_checked(b_row + b_off[k & 7], Bs, kStageFloatsB, st);
+        b1 = lds4_checked(b_row + (b_off[k & 7] ^ 16), Bs, kStageFloatsB, st);
       } else {
-        b0 = *reinterpret_cast<const float4*>(b_base + k * BN);
-        b1 = *reinterpret_cast<const float4*>(b_base + k * BN + 16);
+        b0 = lds4_checked(b_base + k * BN, Bs, kStageFloatsB, st);
+        b1 = lds4_checked(b_base + k * BN + 16, Bs, kStageFloatsB, st);
       }
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const unsigned long long bp[4] = {
@@ -337,9 +370,11 @@ struct FfmaTileT {
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const int c = bn + col0 + 16 * g;
-          *reinterpret_cast<float4*>(crow + 16 * g) =
-              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
-                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
+          stg4_checked(crow + 16 * g,
+                       make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                                   val(i, 4 * g + 2, c + 2),
+                                   val(i, 4 * g + 3, c + 3)),
+                       p);
         }
       }
       return;
@@ -353,13 +388,15 @@ struct FfmaTileT {
       for (int g = 0; g < 2; ++g) {
         const int c = bn + col0 + 16 * g;
         if (c_vec && c + 3 < p.N) {
-          *reinterpret_cast<float4*>(crow + c) =
-              make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
-                          val(i, 4 * g + 2, c + 2), val(i, 4 * g + 3, c + 3));
+          stg4_checked(crow + c,
+                       make_float4(val(i, 4 * g, c), val(i, 4 * g + 1, c + 1),
+                                   val(i, 4 * g + 2, c + 2),
+                                   val(i, 4 * g + 3, c + 3)),
+                       p);
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (c + j < p.N) crow[c + j] = val(i, 4 * g + j, c + j);
+            if (c + j < p.N) stg1_checked(crow + c + j, val(i, 4 * g + j, c + j), p);
         }
       }
     }

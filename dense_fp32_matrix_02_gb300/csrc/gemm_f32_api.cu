@@ -19,6 +19,13 @@ using namespace gemm_f32_impl;
 // gemm_f32_device_status.
 __device__ unsigned int g_kernel_status;
 
+// The checked build's self-test: the kernels' index check applied to one
+// element past a 4-element extent (the status word itself); nothing is
+// read or written through the index, the check only reports it.
+__global__ void bounds_probe_kernel(unsigned int* status) {
+  (void)span_ok(status + 4, 4, status, 16, status);
+}
+
 namespace {
 
 constexpr long long kDefaultWaitNs = 2000000000LL;  // 2 s
@@ -292,6 +299,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   p.ldc = ldc;
   p.bias = bias;
   p.act = act;
+  p.status = d->status;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (plan.algo) {
     case GEMM_F32_ALGO_SIMT:
@@ -411,6 +419,7 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
   p.batch = static_cast<int>(batch);
   p.transA = ta ? 1 : 0;
   p.transB = tb ? 1 : 0;
+  p.status = d->status;
   const bool vec = aligned16(A) && aligned16(B) && mult4(lda) && mult4(ldb) &&
                    mult4(sA) && mult4(sB);
   const bool c_vec = aligned16(C) && mult4(ldc) && mult4(sC);
@@ -642,6 +651,9 @@ const char* gemm_f32_status_string(int status) {
     case GEMM_F32_ERR_SCRATCH_LIMIT:
       return "the product needs more split-K scratch than the library's "
              "static buffer holds (see gemm_f32_noalloc_scratch_bytes)";
+    case GEMM_F32_ERR_BOUNDS:
+      return "checked build: a kernel's index fell outside its extent (the "
+             "access was skipped)";
     default:
       return "unknown status";
   }
@@ -664,8 +676,22 @@ int gemm_f32_device_status(gemm_f32_stream_t stream) {
     if ((e = cudaMemcpyToSymbol(g_kernel_status, &zero, sizeof(zero))) !=
         cudaSuccess)
       return fail_cuda(e);
-    return GEMM_F32_ERR_TIMEOUT;
+    return (word & kStatusBounds) ? GEMM_F32_ERR_BOUNDS
+                                  : GEMM_F32_ERR_TIMEOUT;
   }
+  return GEMM_F32_OK;
+}
+
+int gemm_f32_bounds_checked(void) { return GEMM_F32_BOUNDS_CHECK ? 1 : 0; }
+
+int gemm_f32_bounds_probe(gemm_f32_stream_t stream) {
+  if (!GEMM_F32_BOUNDS_CHECK) return GEMM_F32_OK;
+  const DeviceInfo* d = nullptr;
+  cudaError_t e = device_info(&d);
+  if (e != cudaSuccess) return fail_cuda(e);
+  bounds_probe_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      d->status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e);
   return GEMM_F32_OK;
 }
 

@@ -27,6 +27,36 @@
 
 namespace gemm_f32_impl {
 
+// cp.async of `bytes` (0..16, or 0 / 4) from src to the shared dst; the
+// checked build first tests dst against its stage buffer [dbase, dbase +
+// dfloats) and, when bytes > 0, src against the operand's extent, and
+// skips (or zero-fills) what falls outside.
+__device__ __forceinline__ void cp16_checked(float* dst, const float* dbase,
+                                             int dfloats, const float* src,
+                                             int bytes, const float* sbase,
+                                             long long sextent,
+                                             unsigned int* st) {
+  if (!span_ok(dst, 16, dbase, 4LL * dfloats, st)) return;
+  if (bytes > 0 && !span_ok(src, bytes, sbase, sextent, st)) {
+    src = sbase;
+    bytes = 0;
+  }
+  cp_async16(smem_u32(dst), src, bytes);
+}
+
+__device__ __forceinline__ void cp4_checked(float* dst, const float* dbase,
+                                            int dfloats, const float* src,
+                                            int bytes, const float* sbase,
+                                            long long sextent,
+                                            unsigned int* st) {
+  if (!span_ok(dst, 4, dbase, 4LL * dfloats, st)) return;
+  if (bytes > 0 && !span_ok(src, bytes, sbase, sextent, st)) {
+    src = sbase;
+    bytes = 0;
+  }
+  cp_async4(smem_u32(dst), src, bytes);
+}
+
 // AKM = true keeps A K-major in shared memory (FfmaTile: 16-byte copies of
 // A, read along K); false stores it transposed (FfmaTileT).
 // TA / TB: A / B stored transposed in global memory (A as K×M, B as N×K).
@@ -48,6 +78,15 @@ struct SimtKernel {
                                                     float* Bs, int bm, int bn,
                                                     int kt, int tid) {
     const int k0 = kt * BK;
+    // the operands' extents (for the checked build)
+    const long long ext_a =
+        TA ? matrix_extent_bytes(p.K, p.M, p.lda)
+           : matrix_extent_bytes(p.M, p.K, p.lda);
+    const long long ext_b =
+        TB ? matrix_extent_bytes(p.N, p.K, p.ldb)
+           : matrix_extent_bytes(p.K, p.N, p.ldb);
+    constexpr int kFA = Tile::kStageFloatsA, kFB = Tile::kStageFloatsB;
+    (void)ext_a, (void)ext_b;
     if constexpr (AKM) {
       // A, K-major: 16-byte chunks (zero-filled past M or K), swizzled
       constexpr int kChunksA = BM * BK / 4;
@@ -61,8 +100,8 @@ struct SimtKernel {
           bytes = 4 * min(4, p.K - gk);
           src = p.A + (long long)gm * p.lda + gk;
         }
-        cp_async16(smem_u32(As + m * BK + ((c ^ a_swizzle<BK>(m)) * 4)), src,
-                   bytes);
+        cp16_checked(As + m * BK + ((c ^ a_swizzle<BK>(m)) * 4), As, kFA, src,
+                     bytes, p.A, ext_a, p.status);
       }
     }
     if constexpr (TA && VEC) {
@@ -78,7 +117,8 @@ struct SimtKernel {
           bytes = 4 * min(4, p.M - gm);
           src = p.A + (long long)gk * p.lda + gm;
         }
-        cp_async16(smem_u32(As + Tile::a_index(k, 4 * c)), src, bytes);
+        cp16_checked(As + Tile::a_index(k, 4 * c), As, kFA, src, bytes, p.A,
+                     ext_a, p.status);
       }
     } else if constexpr (TA) {
       // A stored K×M, any alignment: a warp copies 32 consecutive m of one k
@@ -89,7 +129,8 @@ struct SimtKernel {
         const int gk = k0 + k, gm = bm + m;
         const bool ok = gk < p.K && gm < p.M;
         const float* src = ok ? p.A + (long long)gk * p.lda + gm : p.A;
-        cp_async4(smem_u32(As + Tile::a_index(k, m)), src, ok ? 4 : 0);
+        cp4_checked(As + Tile::a_index(k, m), As, kFA, src, ok ? 4 : 0, p.A,
+                    ext_a, p.status);
       }
     }
     // A, transposed on the way in: single-float copies, a warp covering 4
@@ -104,7 +145,8 @@ struct SimtKernel {
       const int gm = bm + m, gk = k0 + k;
       const bool ok = gm < p.M && gk < p.K;
       const float* src = ok ? p.A + (long long)gm * p.lda + gk : p.A;
-      cp_async4(smem_u32(As + Tile::a_index(k, m)), src, ok ? 4 : 0);
+      cp4_checked(As + Tile::a_index(k, m), As, kFA, src, ok ? 4 : 0, p.A,
+                  ext_a, p.status);
     }
     }
     if constexpr (TB) {
@@ -119,7 +161,8 @@ struct SimtKernel {
         const int gn = bn + n, gk = k0 + k;
         const bool ok = gn < p.N && gk < p.K;
         const float* src = ok ? p.B + (long long)gn * p.ldb + gk : p.B;
-        cp_async4(smem_u32(Bs + Tile::b_index(k, n)), src, ok ? 4 : 0);
+        cp4_checked(Bs + Tile::b_index(k, n), Bs, kFB, src, ok ? 4 : 0, p.B,
+                    ext_b, p.status);
       }
     } else if (VEC) {
       constexpr int kChunksB = BK * BN / 4;
@@ -133,7 +176,8 @@ struct SimtKernel {
           bytes = 4 * min(4, p.N - gn);
           src = p.B + (long long)gk * p.ldb + gn;
         }
-        cp_async16(smem_u32(Bs + k * BN + 4 * c), src, bytes);
+        cp16_checked(Bs + k * BN + 4 * c, Bs, kFB, src, bytes, p.B, ext_b,
+                     p.status);
       }
     } else {
       constexpr int kElemsB = BK * BN;
@@ -143,7 +187,8 @@ struct SimtKernel {
         const int gk = k0 + k, gn = bn + n;
         const bool ok = gk < p.K && gn < p.N;
         const float* src = ok ? p.B + (long long)gk * p.ldb + gn : p.B;
-        cp_async4(smem_u32(Bs + k * BN + n), src, ok ? 4 : 0);
+        cp4_checked(Bs + k * BN + n, Bs, kFB, src, ok ? 4 : 0, p.B, ext_b,
+                    p.status);
       }
     }
   }
@@ -190,7 +235,7 @@ struct SimtKernel {
       cp_async_commit();
       const int slot = kt % STAGES;
       tile.compute(As + slot * Tile::kStageFloatsA,
-                   Bs + slot * Tile::kStageFloatsB, acc);
+                   Bs + slot * Tile::kStageFloatsB, acc, p.status);
     }
     cp_async_wait<0>();
     tile.store(p, bm, bn, c_vec != 0, acc);

@@ -364,6 +364,10 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
       float4* araw = reinterpret_cast<float4*>(smem + s * kStageBytesA);
       float4* asml =
           reinterpret_cast<float4*>(smem + kOffASmall + s * kStageBytesA);
+      // the stage's buffers, for the checked build
+      const unsigned char* bstage = smem + kOffB + s * kStageBytesB;
+      unsigned int* const st = wc.status;
+      (void)bstage, (void)st;
       constexpr int kChunksPerThread = kStageBytesA / 16 / (32 * kConvWarps);
       if constexpr (Cf::kRawBig) {
         float x[8];
@@ -373,23 +377,34 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
           const unsigned char* brow =
               smem + kOffB + s * kStageBytesB + n_loc * 64;
           const int sw = (n_loc >> 1) & 3;
-          const float4 v0 = *reinterpret_cast<const float4*>(
-              brow + (((2 * h) ^ sw) << 4));
-          const float4 v1 = *reinterpret_cast<const float4*>(
-              brow + (((2 * h + 1) ^ sw) << 4));
+          const unsigned char* p0 = brow + (((2 * h) ^ sw) << 4);
+          const unsigned char* p1 = brow + (((2 * h + 1) ^ sw) << 4);
+          const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 v0 = span_ok(p0, 16, bstage, kStageBytesB, st)
+                                ? *reinterpret_cast<const float4*>(p0)
+                                : z4;
+          const float4 v1 = span_ok(p1, 16, bstage, kStageBytesB, st)
+                                ? *reinterpret_cast<const float4*>(p1)
+                                : z4;
           x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
           x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
         } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) x[k] = bcol[k * kTileN];
+          for (int k = 0; k < 8; ++k)
+            x[k] = span_ok(bcol + k * kTileN, 4, bstage, kStageBytesB, st)
+                       ? bcol[k * kTileN]
+                       : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           big[k] = __float_as_uint(x[k]);
           small[k] = tf32_small_of_truncated(x[k]);
         }
-        tmem_st8(tcol, big);
-        tmem_st8(tcol + kBK, small);
+        if (tmem_span_ok(tcol, 8, tmem, kTmemCols, q, st) &&
+            tmem_span_ok(tcol + kBK, 8, tmem, kTmemCols, q, st)) {
+          tmem_st8(tcol, big);
+          tmem_st8(tcol + kBK, small);
+        }
         if constexpr (Cf::kTA) {
           // A row m = n_loc, k in [8h, 8h + 8): read down column m of the
           // staged [k][m] tile, write two 16-byte chunks of row m, raw and
@@ -398,8 +413,13 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                                   smem + Cf::kOffAT + s * kStageBytesA) +
                               n_loc + 8 * h * kTileM;
           float ax[8];
+          const unsigned char* atstage = smem + Cf::kOffAT + s * kStageBytesA;
+          (void)atstage;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) ax[k] = acol[k * kTileM];
+          for (int k = 0; k < 8; ++k)
+            ax[k] = span_ok(acol + k * kTileM, 4, atstage, kStageBytesA, st)
+                        ? acol[k * kTileM]
+                        : 0.f;
           unsigned char* rraw = smem + s * kStageBytesA + n_loc * 64;
           unsigned char* rsml =
               smem + kOffASmall + s * kStageBytesA + n_loc * 64;
@@ -407,10 +427,12 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int pos = ((2 * h + c) ^ sw) << 4;
-            *reinterpret_cast<float4*>(rraw + pos) =
-                make_float4(ax[4 * c], ax[4 * c + 1], ax[4 * c + 2],
-                            ax[4 * c + 3]);
-            *reinterpret_cast<float4*>(rsml + pos) = make_float4(
+            if (span_ok(rraw + pos, 16, araw, kStageBytesA, st))
+              *reinterpret_cast<float4*>(rraw + pos) =
+                  make_float4(ax[4 * c], ax[4 * c + 1], ax[4 * c + 2],
+                              ax[4 * c + 3]);
+            if (span_ok(rsml + pos, 16, asml, kStageBytesA, st))
+              *reinterpret_cast<float4*>(rsml + pos) = make_float4(
                 __uint_as_float(tf32_small_of_truncated(ax[4 * c])),
                 __uint_as_float(tf32_small_of_truncated(ax[4 * c + 1])),
                 __uint_as_float(tf32_small_of_truncated(ax[4 * c + 2])),
@@ -421,6 +443,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll
           for (int j = 0; j < kChunksPerThread; ++j) {
             const int c = t + 32 * kConvWarps * j;
+            if (!span_ok(araw + c, 16, araw, kStageBytesA, st)) continue;
             const float4 v = araw[c];
             asml[c] = make_float4(
                 __uint_as_float(tf32_small_of_truncated(v.x)),
@@ -432,13 +455,20 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          tf32_split(bcol[k * kTileN], big[k], small[k]);
-        tmem_st8(tcol, big);
-        tmem_st8(tcol + kBK, small);
+          tf32_split(span_ok(bcol + k * kTileN, 4, bstage, kStageBytesB, st)
+                         ? bcol[k * kTileN]
+                         : 0.f,
+                     big[k], small[k]);
+        if (tmem_span_ok(tcol, 8, tmem, kTmemCols, q, st) &&
+            tmem_span_ok(tcol + kBK, 8, tmem, kTmemCols, q, st)) {
+          tmem_st8(tcol, big);
+          tmem_st8(tcol + kBK, small);
+        }
         // A: element-wise, position for position (the swizzle is untouched)
 #pragma unroll
         for (int j = 0; j < kChunksPerThread; ++j) {
           const int c = t + 32 * kConvWarps * j;
+          if (!span_ok(araw + c, 16, araw, kStageBytesA, st)) continue;
           const float4 v = araw[c];
           uint32_t b0, b1, b2, b3, s0, s1, s2, s3;
           tf32_split(v.x, b0, s0);
@@ -473,6 +503,14 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         ro.A += za * raw.sA;
         ro.B += zb * raw.sB;
         const int k0 = kb0 * kBK, k1 = min(K, (kb0 + nk) * kBK);
+        // where this CTA's stores may land (for the checked build): its
+        // partial-tile slot, or the stored matrix
+        const long long out_ext =
+            !whole ? 4LL * kTileM * kTileN
+            : Cf::kTStore ? matrix_extent_bytes(N, M, ldo)
+                          : matrix_extent_bytes(M, N, ldo);
+        unsigned int* const st = wc.status;
+        (void)out_ext, (void)st;
         // this lane's column n has one bias value; load it once
         const bool epi = whole && (bias != nullptr || act != 0);
         const float bias_n =
@@ -491,9 +529,15 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll 1
           for (int j = 0; j < kBlocks; ++j) {
             uint32_t v[32];
-            tmem_ld16(tmem + lane_bits + c_begin + 32 * j, v);
-            tmem_ld16(tmem + lane_bits + c_begin + 32 * j + 16, v + 16);
-            tmem_ld_wait();
+            const uint32_t ta = tmem + lane_bits + c_begin + 32 * j;
+            if (tmem_span_ok(ta, 32, tmem, kTmemCols, q, st)) {
+              tmem_ld16(ta, v);
+              tmem_ld16(ta + 16, v + 16);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int r = 0; r < 32; ++r) v[r] = 0u;
+            }
             const bool nan_here = any_nan(v);
             const bool fix = __any_sync(0xffffffffu, nan_here);
             if (epi) {
@@ -505,17 +549,20 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
               }
             }
 #pragma unroll
-            for (int r = 0; r < 32; ++r)
-              *reinterpret_cast<uint32_t*>(
+            for (int r = 0; r < 32; ++r) {
+              unsigned char* sp =
                   stg + j * 4096 + r * 128 +
-                  ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2))) =
-                  v[r];
+                  ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2));
+              if (span_ok(sp, 4, stg, kBlocks * 4096, st))
+                *reinterpret_cast<uint32_t*>(sp) = v[r];
+            }
             if (fix && nan_here && n < N) {
 #pragma unroll 1
               for (int r = 0; r < 32; ++r) {
                 uint32_t* slot = reinterpret_cast<uint32_t*>(
                     stg + j * 4096 + r * 128 +
                     ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2)));
+                if (!span_ok(slot, 4, stg, kBlocks * 4096, st)) continue;
                 const float x = __uint_as_float(*slot);
                 const int m = bm + c_begin + 32 * j + r;
                 if (x == x || m >= M) continue;
@@ -551,8 +598,14 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll 1
         for (int c0 = c_begin; !tma && c0 < c_begin + kAccCols / 2; c0 += 16) {
           uint32_t v[16];
-          tmem_ld16(tmem + lane_bits + c0, v);
-          tmem_ld_wait();
+          if (tmem_span_ok(tmem + lane_bits + c0, 16, tmem, kTmemCols, q,
+                           st)) {
+            tmem_ld16(tmem + lane_bits + c0, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) v[r] = 0u;
+          }
           const bool nan_here = any_nan(v);
           const bool fix = __any_sync(0xffffffffu, nan_here) && nan_here;
           if constexpr (Cf::kTStore) {
@@ -564,18 +617,20 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                   ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
 #pragma unroll
                 for (int i = 0; i < 16; i += 4)
-                  *reinterpret_cast<float4*>(dst + i) = make_float4(
-                      __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                      __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                  if (span_ok(dst + i, 16, out, out_ext, st))
+                    *reinterpret_cast<float4*>(dst + i) = make_float4(
+                        __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
               } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                  if (bm + c0 + i < M) dst[i] = __uint_as_float(v[i]);
+                  if (bm + c0 + i < M && span_ok(dst + i, 4, out, out_ext, st))
+                    dst[i] = __uint_as_float(v[i]);
               }
               if (fix) {
 #pragma unroll 1
                 for (int i = 0; i < 16 && bm + c0 + i < M; ++i)
-                  if (dst[i] != dst[i])
+                  if (span_ok(dst + i, 4, out, out_ext, st) && dst[i] != dst[i])
                     dst[i] = ieee_dot(ro, bm + c0 + i, n, k0, k1);
               }
             }
@@ -592,16 +647,16 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int m = bm + c0 + i;
-              if (m < M)
-                out[(long long)(m - mo) * ldo + (n - no)] =
-                    __uint_as_float(v[i]);
+              float* d = out + (long long)(m - mo) * ldo + (n - no);
+              if (m < M && span_ok(d, 4, out, out_ext, st))
+                *d = __uint_as_float(v[i]);
             }
             if (fix) {
 #pragma unroll 1
               for (int i = 0; i < 16 && bm + c0 + i < M; ++i) {
                 const int m = bm + c0 + i;
                 float* d = out + (long long)(m - mo) * ldo + (n - no);
-                if (*d == *d) continue;
+                if (!span_ok(d, 4, out, out_ext, st) || *d == *d) continue;
                 float y = ieee_dot(ro, m, n, k0, k1);
                 if (epi) {
                   if (bias != nullptr) y += bias_n;

@@ -258,12 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t raw[8], small[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float x = n < nb ? bs[(k0 + j) * nb + n] : 0.f;
+          // B's box (nb × kp floats) in the epilogue staging
+          const float* bp = bs + (k0 + j) * nb + n;
+          const float x =
+              n < nb && span_ok(bp, 4, bs, 4LL * nb * kp, wc.status) ? *bp
+                                                                    : 0.f;
           raw[j] = __float_as_uint(x);
           small[j] = tf32_small_of_truncated(x);
         }
-        tmem_st8(bt_raw + lane_bits + k0, raw);
-        tmem_st8(bt_small + lane_bits + k0, small);
+        if (tmem_span_ok(bt_raw + lane_bits + k0, 8, tmem, kTmemCols, q,
+                         wc.status) &&
+            tmem_span_ok(bt_small + lane_bits + k0, 8, tmem, kTmemCols, q,
+                         wc.status)) {
+          tmem_st8(bt_raw + lane_bits + k0, raw);
+          tmem_st8(bt_small + lane_bits + k0, small);
+        }
       }
     }
     tmem_st_wait();
@@ -291,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < kStageBytes / 16 / (32 * kConvWarps); ++j) {
           const int c = t32 + 32 * kConvWarps * j;
+          if (!span_ok(araw + c, 16, araw, kStageBytes, wc.status)) continue;
           const float4 v = araw[c];
           asml[c] = make_float4(
               __uint_as_float(tf32_small_of_truncated(v.x)),
@@ -333,10 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // issued together, then the accumulator goes back to the MMA
       const int c_begin = hh * (kAccCols / 2);
       uint32_t v[kAccCols / 2];
+      if (tmem_span_ok(tmem + lane_bits + b * kAccCols + c_begin,
+                       kAccCols / 2, tmem, kTmemCols, q, wc.status)) {
 #pragma unroll
-      for (int c = 0; c < kAccCols / 2; c += 16)
-        tmem_ld16(tmem + lane_bits + b * kAccCols + c_begin + c, v + c);
-      tmem_ld_wait();
+        for (int c = 0; c < kAccCols / 2; c += 16)
+          tmem_ld16(tmem + lane_bits + b * kAccCols + c_begin + c, v + c);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int c = 0; c < kAccCols / 2; ++c) v[c] = 0u;
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(b));
@@ -362,16 +378,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           unsigned char* stg = stg0 + sb * kStagingBytes;
 #pragma unroll
-          for (int r = 0; r < 32; ++r)
-            *reinterpret_cast<uint32_t*>(
+          for (int r = 0; r < 32; ++r) {
+            unsigned char* sp =
                 stg + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
-                                 ((lane & 3) << 2))) = v[32 * j + r];
+                                 ((lane & 3) << 2));
+            if (span_ok(sp, 4, stg0, 2 * kStagingBytes, wc.status))
+              *reinterpret_cast<uint32_t*>(sp) = v[32 * j + r];
+          }
           if (fix) {
 #pragma unroll 1
             for (int r = 0; r < 32; ++r) {
               uint32_t* slot = reinterpret_cast<uint32_t*>(
                   stg + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
                                    ((lane & 3) << 2)));
+              if (!span_ok(slot, 4, stg0, 2 * kStagingBytes, wc.status))
+                continue;
               const float x = __uint_as_float(*slot);
               const int m = m0 + 32 * j + r;
               if (x == x || m >= M) continue;
@@ -389,14 +410,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (n < N) {
+        const long long c_ext = matrix_extent_bytes(M, N, ldc);
 #pragma unroll
-        for (int r = 0; r < kAccCols / 2; ++r)
-          if (m0 + r < M) C[(long long)(m0 + r) * ldc + n] = __uint_as_float(v[r]);
+        for (int r = 0; r < kAccCols / 2; ++r) {
+          float* d = C + (long long)(m0 + r) * ldc + n;
+          if (m0 + r < M && span_ok(d, 4, C, c_ext, wc.status))
+            *d = __uint_as_float(v[r]);
+        }
         if (fix) {
 #pragma unroll 1
           for (int r = 0; r < kAccCols / 2 && m0 + r < M; ++r) {
             float* d = C + (long long)(m0 + r) * ldc + n;
-            if (*d == *d) continue;
+            if (!span_ok(d, 4, C, c_ext, wc.status) || *d == *d) continue;
             float y = ieee_dot(raw, m0 + r, n, 0, K);
             if (epi) y = epilogue_act(y + bias_n, act);
             *d = y;

@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile.compute(reinterpret_cast<const float*>(smem + s * kStageBytesA),
                  reinterpret_cast<const float*>(smem + kOffB +
                                                 s * kStageBytesB),
-                 acc);
+                 acc, p.status);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(s));
   }

@@ -90,6 +90,10 @@ def lib() -> ctypes.CDLL:
         L.gemm_f32_set_debug_flags.argtypes = [ctypes.c_uint]
         L.gemm_f32_version.restype = ci
         L.gemm_f32_version.argtypes = []
+        L.gemm_f32_bounds_checked.restype = ci
+        L.gemm_f32_bounds_checked.argtypes = []
+        L.gemm_f32_bounds_probe.restype = ci
+        L.gemm_f32_bounds_probe.argtypes = [vp]
         L.gemm_f32_mixed16.restype = ci
         L.gemm_f32_mixed16.argtypes = [ci, i64, i64, i64, vp, i64, vp, i64,
                                        vp, i64, vp]
@@ -522,6 +526,21 @@ def set_debug_flags(flags: int) -> int:
 
 
 DEBUG_STALL_PRODUCER = 1
+
+
+def bounds_checked() -> bool:
+    """True when the loaded library is the checked build."""
+    return bool(lib().gemm_f32_bounds_checked())
+
+
+def bounds_probe(stream=None):
+    """Checked build: makes the next device_status() report
+    GEMM_F32_ERR_BOUNDS (no memory is touched); no-op otherwise."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    _check(lib().gemm_f32_bounds_probe(handle or None), "gemm_f32_bounds_probe")
 
 
 def version() -> int:

@@ -63,7 +63,12 @@ typedef enum {
     GEMM_F32_ERR_TIMEOUT = 4,
     /* gemm_f32_noalloc: the product needs more split-K scratch than the
      * library's static buffer holds. */
-    GEMM_F32_ERR_SCRATCH_LIMIT = 5
+    GEMM_F32_ERR_SCRATCH_LIMIT = 5,
+    /* Checked build only (gemm_f32_bounds_checked() == 1): a kernel computed
+     * a shared-memory, tensor-memory or global index outside the extent it
+     * must lie in and skipped that access (reported by
+     * gemm_f32_device_status). */
+    GEMM_F32_ERR_BOUNDS = 6
 } gemm_f32_status;
 
 typedef enum {
@@ -418,11 +423,35 @@ GEMM_F32_API int gemm_f32_last_cuda_error(void);
 
 /*
  * Waits for `stream`, then reads and clears the current device's kernel
- * status word.  Returns GEMM_F32_OK, GEMM_F32_ERR_TIMEOUT if a kernel's
- * bounded mbarrier wait gave up since the last call, or
+ * status word.  Returns GEMM_F32_OK; GEMM_F32_ERR_BOUNDS if, in the checked
+ * build, a kernel's index check failed since the last call;
+ * GEMM_F32_ERR_TIMEOUT if a kernel's bounded mbarrier wait gave up; or
  * GEMM_F32_ERR_CUDA.  This is the only entry point that synchronizes.
  */
 GEMM_F32_API int gemm_f32_device_status(gemm_f32_stream_t stream);
+
+/*
+ * The checked build.  libgemm_f32_debug.so (built with
+ * GEMM_F32_BOUNDS_CHECK=1; python -m dense_fp32_matrix_02_gb300.build
+ * --checked) exports the same entry points as libgemm_f32.so, but its FFMA
+ * and tensor kernels test every shared-memory, tensor-memory and global
+ * index they compute against the extent it must lie in (the stage buffer,
+ * the TMEM allocation, the matrix) before the access; a failed test sets a
+ * status bit, reported as GEMM_F32_ERR_BOUNDS by gemm_f32_device_status,
+ * and the access is skipped, so nothing faults.  It is a test build that
+ * stands in for a memory checker (the pages' race and out-of-range
+ * symptoms, "3 · La mémoire partagée" §3.2, §3.3), slower than the normal
+ * one.  The pages have no counterpart to the entries below.
+ *
+ * gemm_f32_bounds_checked: 1 in the checked build, 0 in the normal one.
+ * gemm_f32_bounds_probe: in the checked build, launches one thread that
+ * runs the kernels' check on an index one element past a 4-element extent
+ * (nothing is read or written), so the next gemm_f32_device_status must
+ * return GEMM_F32_ERR_BOUNDS; in the normal build launches nothing.
+ * Returns GEMM_F32_OK or GEMM_F32_ERR_CUDA.
+ */
+GEMM_F32_API int gemm_f32_bounds_checked(void);
+GEMM_F32_API int gemm_f32_bounds_probe(gemm_f32_stream_t stream);
 
 /* The deadline, in nanoseconds of the GPU's global timer, after which an
  * mbarrier wait in the pipelined kernels gives up (<= 0 restores the
