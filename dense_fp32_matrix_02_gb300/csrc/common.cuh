@@ -148,6 +148,14 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Arrive on the mbarrier once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival: .noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(
+                   bar)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- shared loads
 __device__ __forceinline__ float4 lds128(uint32_t addr) {
   float4 v;

@@ -116,11 +116,11 @@ int choose_simt_cfg(int64_t M, int64_t N, const DeviceInfo& d) {
   if (N <= 64) return kSimt128x64x16;
   const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
   if (tiles < d.sm_count) return kSimt128x64x16;
-  // A transposed on its way into shared memory (4-byte copies) measured
-  // ahead of the K-major copy once both tiles issue packed two-lane FMAs:
-  // 4096^3 aligned 46.9 against 44.1 TFLOP/s (unaligned operands take
-  // this tile either way: 41.8)
-  return kSimt128x128x32Occ1;
+  // 16-byte operands: the warp-specialised kernel (a producer warpgroup
+  // issues the copies; 4096^3: 54.4 TFLOP/s against 45.3 for the best
+  // single-role kernel).  Otherwise A transposed on its way into shared
+  // memory by 4-byte copies (4096^3: 41.8).
+  return kSimtWs128x128x32;
 }
 
 int choose_tc_cfg(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {
@@ -302,9 +302,14 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   p.status = d->status;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (plan.algo) {
-    case GEMM_F32_ALGO_SIMT:
-      e = launch_simt(p, plan.simt_cfg, plan.vec, plan.c_vec, s);
+    case GEMM_F32_ALGO_SIMT: {
+      WaitCfg wc;
+      wc.limit = g_wait_ns.load();
+      wc.debug = g_debug_flags.load();
+      wc.status = d->status;
+      e = launch_simt(p, plan.simt_cfg, plan.vec, plan.c_vec, wc, s);
       break;
+    }
     case GEMM_F32_ALGO_TMA: {
       WaitCfg wc;
       wc.limit = g_wait_ns.load();
@@ -478,7 +483,11 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
       cfg = kTc256Raw;
     e = launch_tf32x3(q, cfg, 0, 1, nullptr, wc, s);
   } else {
-    e = launch_simt(p, choose_simt_cfg(M, N, *d), vec, c_vec, s);
+    WaitCfg wc;
+    wc.limit = g_wait_ns.load();
+    wc.debug = g_debug_flags.load();
+    wc.status = d->status;
+    e = launch_simt(p, choose_simt_cfg(M, N, *d), vec, c_vec, wc, s);
   }
   if (e != cudaSuccess) return fail_cuda(e);
   return GEMM_F32_OK;

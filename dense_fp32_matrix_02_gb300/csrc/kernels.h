@@ -45,7 +45,10 @@ enum SimtCfg {
   kSimt128x128x32Occ1 = 3,
   kSimt128x128x16Occ1S6 = 4,
   kSimtKm128x128x32Occ1 = 5,  // A kept K-major (16-byte copies)
-  kSimtCfgCount = 6
+  // warp-specialised: a ninth warp issues every copy (16-byte operands
+  // only; otherwise the same as kSimt128x128x32Occ1)
+  kSimtWs128x128x32 = 6,
+  kSimtCfgCount = 7
 };
 
 // The driver's cuTensorMapEncodeTiled, looked up once (thread-safe); null
@@ -57,6 +60,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t ensure_smem_attr(const void* fn, int bytes);
 
 cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
+                        const WaitCfg& wc,
                         cudaStream_t stream);
 
 // 3xTF32 tcgen05 kernel configurations: 256 x 128 tiles at one CTA per SM,

@@ -251,7 +251,182 @@ __global__ void __launch_bounds__(FfmaTileT<BM, BN, BK>::kThreads, MINB)
                                                         c_vec);
 }
 
+// ------------------------------------------------- warp-specialised
+// The same 8×8 K-major tile (FfmaTile, 128 × 128 × 32 stages), with the
+// copies taken off the threads that multiply: warps 0-7 only wait, compute
+// and release; warps 8-11 (one warpgroup) issue every cp.async of the ring.  The pages' two
+// __syncthreads per tile ("3 · La mémoire partagée", §3.2-§3.3) become two
+// mbarrier phases per ring slot, as in the TMA-fed kernel:
+//   full[s]   expects one arrival from each of the 128 producer threads,
+//             made by cp.async.mbarrier.arrive.noinc once that thread's
+//             copies into slot s have landed;
+//   empty[s]  one arrival per compute warp after it has read slot s; the
+//             producer waits on it before refilling the slot.
+// Compute warps no longer meet at a CTA barrier every stage, and none of
+// them spends issue slots on copies or waits on its own copies.  Operands
+// must be 16-byte aligned with leading dimensions multiples of 4 (16-byte
+// copies, zero-filled past M, N and K).  Every wait is bounded (the status
+// word and a CTA abort flag, as in the other pipelined kernels).
+namespace simt_ws {
+
+constexpr int kBM = 128, kBN = 128, kBK = 32, kStages = 4;
+using Tile = FfmaTile<kBM, kBN, kBK>;
+constexpr int kComputeThreads = Tile::kThreads;        // 256: warpgroups 0, 1
+constexpr int kProducers = 128;                        // warpgroup 2
+constexpr int kThreads = kComputeThreads + kProducers;
+// Registers: the CTA is launched with 168 a thread (384 × 168 = 64,512 of
+// the SM's 65,536); the producer warpgroup then gives up all but 88 and the
+// two compute warpgroups take 208: 256 × 208 + 128 × 88 = 64,512, exactly
+// the launch's allocation (an increase beyond what the decrease frees would
+// wait forever).  With 56 or fewer for the producers their code spills.
+constexpr int kLaunchRegs = 168, kComputeRegs = 208, kProducerRegs = 88;
+static_assert(kComputeThreads * kComputeRegs + kProducers * kProducerRegs <=
+                  kThreads * kLaunchRegs,
+              "register split within the launch's allocation");
+constexpr int kStageFloatsA = Tile::kStageFloatsA;     // 128 × 32
+constexpr int kStageFloatsB = Tile::kStageFloatsB;     // 32 × 128
+constexpr int kOffB = kStages * kStageFloatsA * 4;
+constexpr int kOffBar = kOffB + kStages * kStageFloatsB * 4;
+constexpr int kSmemBytes = kOffBar + 2 * kStages * 8 + 16 + 1024;
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute the same one).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    simt_ws_kernel(Problem p, int tiles_m, int tiles_n, int c_vec,
+                   WaitCfg wc) {
+  griddep_wait();  // A, B and C may belong to the kernel before
+  p.A += blockIdx.z * p.sA;
+  p.B += blockIdx.z * p.sB;
+  p.C += blockIdx.z * p.sC;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* As = reinterpret_cast<float*>(smem);
+  float* Bs = reinterpret_cast<float*>(smem + kOffB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 2 * kStages);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[kStages + s]); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int tm, tn;
+  tile_coords<8>(blockIdx.x, tiles_m, tiles_n, tm, tn);
+  const int bm = tm * kBM, bn = tn * kBN;
+  const int nk = (p.K + kBK - 1) / kBK;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), kProducers);
+      mbar_init(empty(s), kComputeThreads / 32);
+    }
+    *abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (tid >= kComputeThreads) {
+    // ---------------------------------------------------------- producers
+    setmaxnreg_dec<kProducerRegs>();
+    // per stage each of the 128 producer threads copies 8 chunks of A
+    // (rows pt/8 + 16i, chunk pt % 8 of the row's 8, swizzled as FfmaTile
+    // reads) and 8 of B (row pt/32 + 4i, chunk pt % 32 of the row's 32)
+    const int pt = tid - kComputeThreads;
+    const long long ext_a = matrix_extent_bytes(p.M, p.K, p.lda);
+    const long long ext_b = matrix_extent_bytes(p.K, p.N, p.ldb);
+    (void)ext_a, (void)ext_b;
+    const int ca = pt & 7, ra = pt >> 3;
+    const int cb = pt & 31, rb = pt >> 5;
+    if (!(wc.debug & kDebugStallProducer)) {
+      for (int kt = 0; kt < nk; ++kt) {
+        const int s = kt % kStages;
+        if (kt >= kStages &&
+            !bounded_wait(empty(s), ((kt / kStages) - 1) & 1, wc.limit, abort,
+                          0u)) {
+          *abort = 1;
+          if (pt == 0) record_status(wc.status, kStatusTimeoutEmpty);
+          break;
+        }
+        const int k0 = kt * kBK;
+        float* as = As + s * kStageFloatsA;
+        float* bs = Bs + s * kStageFloatsB;
+        const int gk = k0 + 4 * ca;
+        const int abytes = gk < p.K ? 4 * min(4, p.K - gk) : 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int m = ra + 16 * i, gm = bm + m;
+          const int bytes = gm < p.M ? abytes : 0;
+          const float* src = bytes ? p.A + (long long)gm * p.lda + gk : p.A;
+          cp16_checked(as + m * kBK + ((ca ^ a_swizzle<kBK>(m)) * 4), as,
+                       kStageFloatsA, src, bytes, p.A, ext_a, p.status);
+        }
+        const int gn = bn + 4 * cb;
+        const int bcols = gn < p.N ? 4 * min(4, p.N - gn) : 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int k = rb + 4 * i;
+          const int bytes = k0 + k < p.K ? bcols : 0;
+          const float* src =
+              bytes ? p.B + (long long)(k0 + k) * p.ldb + gn : p.B;
+          cp16_checked(bs + k * kBN + 4 * cb, bs, kStageFloatsB, src, bytes,
+                       p.B, ext_b, p.status);
+        }
+        cp_async_mbar_arrive_noinc(full(s));
+      }
+    }
+    cp_async_wait<0>();  // this thread's copies land before it leaves
+  } else {
+    // ---------------------------------------------------------- compute
+    setmaxnreg_inc<kComputeRegs>();
+    Tile tile;
+    tile.init(tid);
+    Tile::Acc acc;
+    Tile::zero(acc);
+    bool ok = true;
+    for (int kt = 0; kt < nk; ++kt) {
+      const int s = kt % kStages;
+      if (!bounded_wait(full(s), (kt / kStages) & 1, wc.limit, abort, 0u)) {
+        *abort = 1;
+        record_status(wc.status, kStatusTimeoutFull);
+        ok = false;
+        break;
+      }
+      tile.compute(As + s * kStageFloatsA, Bs + s * kStageFloatsB, acc,
+                   p.status);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(s));
+    }
+    if (ok && !*abort) tile.store(p, bm, bn, c_vec != 0, acc);
+  }
+}
+
+}  // namespace simt_ws
+
 namespace {
+
+cudaError_t launch_ws(const Problem& p, bool c_vec, const WaitCfg& wc,
+                      cudaStream_t stream) {
+  using namespace simt_ws;
+  auto fn = simt_ws_kernel;
+  cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(fn), kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int tiles_m = (p.M + kBM - 1) / kBM, tiles_n = (p.N + kBN - 1) / kBN;
+  const long long grid = (long long)tiles_m * tiles_n;
+  if (grid > 0x7fffffffLL || p.batch < 1 || p.batch > 65535)
+    return cudaErrorInvalidConfiguration;
+  return launch_pdl(fn, dim3((unsigned)grid, 1, (unsigned)p.batch),
+                    dim3(kThreads), kSmemBytes, stream, p, tiles_m, tiles_n,
+                    (int)c_vec, wc);
+}
 
 template <int BM, int BN, int BK, int STAGES, bool VEC, int MINB,
           bool AKM = false, bool TA = false, bool TB = false>
@@ -285,7 +460,7 @@ cudaError_t launch_trans(const Problem& p, bool c_vec, cudaStream_t stream) {
 
 template <bool VEC>
 cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
-                       cudaStream_t stream) {
+                       const WaitCfg& wc, cudaStream_t stream) {
   switch (cfg) {
     case kSimt128x64x16:
       return launch_cfg<128, 64, 16, 4, VEC, 3>(p, c_vec, stream);
@@ -301,6 +476,9 @@ cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
       // 16-byte copies of A need VEC (aligned A, lda % 4 == 0)
       return VEC ? launch_cfg<128, 128, 32, 4, true, 1, true>(p, c_vec, stream)
                  : launch_cfg<128, 128, 32, 4, false, 1>(p, c_vec, stream);
+    case kSimtWs128x128x32:
+      return VEC ? launch_ws(p, c_vec, wc, stream)
+                 : launch_cfg<128, 128, 32, 4, false, 1>(p, c_vec, stream);
     default:
       return cudaErrorInvalidValue;
   }
@@ -310,12 +488,12 @@ cudaError_t launch_vec(const Problem& p, int cfg, bool c_vec,
 
 
 cudaError_t launch_simt(const Problem& p, int cfg, bool vec, bool c_vec,
-                        cudaStream_t stream) {
+                        const WaitCfg& wc, cudaStream_t stream) {
   if (p.transA || p.transB)
     return vec ? launch_trans<true>(p, c_vec, stream)
                : launch_trans<false>(p, c_vec, stream);
-  return vec ? launch_vec<true>(p, cfg, c_vec, stream)
-             : launch_vec<false>(p, cfg, c_vec, stream);
+  return vec ? launch_vec<true>(p, cfg, c_vec, wc, stream)
+             : launch_vec<false>(p, cfg, c_vec, wc, stream);
 }
 
 }  // namespace gemm_f32_impl

@@ -24,7 +24,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 from dense_fp32_matrix_02_gb300 import gemm as G  # noqa: E402
 
 DEV = torch.device("cuda:0")
-SIMT_CFGS = list(range(6))  # kSimtCfgCount
+SIMT_CFGS = list(range(7))  # kSimtCfgCount
 
 
 def _env(name, value):
@@ -913,6 +913,45 @@ def test_tma_ffma_timeout_path_reports_and_recovers():
         G.set_debug_flags(old_f)
         G.set_wait_timeout_ns(old_t)
     check_full(a, b, run_gpu(a, b, G.ALGO_TMA, pad=True), what="tma after")
+    assert G.device_status() == 0
+
+
+def test_simt_ws_timeout_path_reports_and_recovers():
+    """The warp-specialised cp.async kernel: a producer that issues no
+    copies makes the compute warps' bounded waits run out."""
+    a, b = synth.make_operands(300, 200, 100, seed=2)
+    old_t = G.set_wait_timeout_ns(2_000_000)
+    old_f = G.set_debug_flags(G.DEBUG_STALL_PRODUCER)
+    try:
+        with _forced(G.ALGO_SIMT, 6):
+            run_gpu(a, b, G.ALGO_SIMT, pad=True)
+        assert G.device_status() == 4
+    finally:
+        G.set_debug_flags(old_f)
+        G.set_wait_timeout_ns(old_t)
+    with _forced(G.ALGO_SIMT, 6):
+        check_full(a, b, run_gpu(a, b, G.ALGO_SIMT, pad=True),
+                   what="simt ws after")
+    assert G.device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1000, 1000, 1000),
+                                   (300, 260, 77), (129, 65, 33)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_simt_ws_kernel(shape):
+    """The warp-specialised cp.async kernel (aligned operands, padded
+    leading dimensions): every element against the oracle, integers exact,
+    the full-size case included."""
+    M, N, K = shape
+    a, b = synth.make_operands(M, N, K, seed=M + 7)
+    with _forced(G.ALGO_SIMT, 6):
+        check_full(a, b, run_gpu(a, b, G.ALGO_SIMT, pad=True),
+                   what=f"simt ws {shape}")
+    ai, bi = synth.make_operands(M, N, K, seed=M + 8, dist_a="int",
+                                 dist_b="int")
+    with _forced(G.ALGO_SIMT, 6):
+        check_full(ai, bi, run_gpu(ai, bi, G.ALGO_SIMT, pad=True), exact=True,
+                   what=f"simt ws {shape} int")
     assert G.device_status() == 0
 
 
