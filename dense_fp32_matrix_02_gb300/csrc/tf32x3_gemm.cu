@@ -673,6 +673,9 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
 
   griddep_launch_dependents();
   tc_fence_before_sync();
+  // the roles ran on one lane of warps 0 and 1: reconverge each warp before
+  // the CTA barrier (a barrier reached by part of a warp does not hold it)
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();

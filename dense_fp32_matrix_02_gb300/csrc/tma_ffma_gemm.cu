@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       nullptr))
         record_status(wc.status, kStatusTimeoutDrain);
   }
+  __syncwarp();  // warp 0 reconverges after thread 0's drain
   __syncthreads();
   if (ok && !*abort) tile.store(p, bm, bn, c_vec != 0, acc);
 }
