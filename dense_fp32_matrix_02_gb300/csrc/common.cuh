@@ -250,6 +250,53 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------ thread-block clusters
+// This CTA's rank within its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+
+// Barrier over every thread of every CTA in the cluster: shared-memory
+// writes made before it (release) are visible to the cluster's threads
+// after it (acquire).  Each warp must reach it converged.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;\n" ::
+          : "memory");
+}
+
+// The shared::cluster address of this CTA's shared address `addr` as seen
+// in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
+               : "=r"(r)
+               : "r"(addr), "r"(rank));
+  return r;
+}
+
+// (volatile, so it stays after the cluster barrier before it; no memory
+// clobber, so the arithmetic between such loads does not order them)
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];\n"
+               : "=r"(v)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // ------------------------------------------------ programmatic launch
 // A kernel launched with programmatic stream serialization may start while
 // the kernel before it in the stream is still running; griddep_wait blocks

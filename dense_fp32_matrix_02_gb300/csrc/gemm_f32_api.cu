@@ -91,6 +91,7 @@ struct Plan {
   int tc_cfg;    // for ALGO_TF32X3
   int splits;    // split-K factor for ALGO_TF32X3 (1 = none)
   int full_tiles;  // tiles computed whole before the split ones
+  bool cluster;    // every tile split, reduced within thread-block clusters
   bool tc_stream;  // ALGO_TF32X3 on the streaming kernel (narrow B)
   long long ws_bytes;  // scratch the plan needs (0 = none)
   bool vec;      // 16-byte operand copies
@@ -147,7 +148,11 @@ int choose_tc_cfg(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {
 //    tile costs about as long as a full round);
 // at least 8 k stages per split, at most 16 splits.  GEMM_F32_SPLITS forces
 // every tile to split that many ways; GEMM_F32_TAIL_SPLIT=0 keeps the last
-// round whole.
+// round whole.  When every tile is split at most kMaxClusterSplits ways,
+// the splits of a tile run as one thread-block cluster and add their
+// partial tiles in distributed shared memory: no scratch, no second kernel
+// (GEMM_F32_CLUSTER_REDUCE=0 takes the scratch and the reduction kernel
+// instead).  Tail splits of a partly filled last round keep the scratch.
 void choose_splits(int64_t M, int64_t N, int64_t K, int tile_m,
                    const DeviceInfo& d, Plan* plan) {
   const int forced = env_int("GEMM_F32_SPLITS", 0);
@@ -172,7 +177,11 @@ void choose_splits(int64_t M, int64_t N, int64_t K, int tile_m,
   }
   plan->splits = (int)s;
   plan->full_tiles = (int)full;
-  plan->ws_bytes = tf32x3_partials_bytes(tile_m, tiles - full, (int)s);
+  plan->cluster = s >= 2 && full == 0 && s <= kMaxClusterSplits &&
+                  env_int("GEMM_F32_CLUSTER_REDUCE", 1) != 0;
+  plan->ws_bytes = plan->cluster
+                       ? 0
+                       : tf32x3_partials_bytes(tile_m, tiles - full, (int)s);
 }
 
 // Decides which kernel runs.  Returns a status; fills *plan on success.
@@ -187,6 +196,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   plan->tc_cfg = choose_tc_cfg(M, N, K, d);
   plan->splits = 1;
   plan->full_tiles = 0;
+  plan->cluster = false;
   plan->tc_stream = false;
   plan->ws_bytes = 0;
   const bool tcgen05_ok = d.cc_major == 10 && vec && K >= 1;
@@ -326,9 +336,10 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       e = plan.tc_stream
               ? launch_tf32x3_stream(p, d->sm_count, wc, s)
               : launch_tf32x3(p, plan.tc_cfg, plan.full_tiles, plan.splits,
-                              plan.splits > 1 ? static_cast<float*>(ws)
-                                              : nullptr,
-                              wc, s);
+                              plan.splits > 1 && !plan.cluster
+                                  ? static_cast<float*>(ws)
+                                  : nullptr,
+                              plan.cluster, wc, s);
       break;
     }
     default:
@@ -481,7 +492,7 @@ int run_batched(int opA, int opB, int64_t M, int64_t N, int64_t K,
       cfg = forced;
     else if (forced < 0 && K >= 2048 && !q.transA)
       cfg = kTc256Raw;
-    e = launch_tf32x3(q, cfg, 0, 1, nullptr, wc, s);
+    e = launch_tf32x3(q, cfg, 0, 1, nullptr, false, wc, s);
   } else {
     WaitCfg wc;
     wc.limit = g_wait_ns.load();

@@ -33,6 +33,29 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block,
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// The same with thread-block clusters of `cluster_x` consecutive CTAs
+// (along x).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(Params...), dim3 grid,
+                               dim3 block, size_t smem, cudaStream_t stream,
+                               unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // SIMT tile configurations (BM x BN x BK).  "Occ1" variants let a thread
 // use up to 255 registers at one 256-thread CTA per SM; the 128 x 64 and
 // 64 x 64 tiles run 128-thread CTAs, three and four per SM.  Every one
@@ -91,11 +114,16 @@ long long tf32x3_partials_bytes(int tile_m, long long split_tiles,
 // `partials` buffer of tf32x3_partials_bytes for the tiles past the first
 // full_tiles (grouped order), each of those tiles' K range is split over
 // `splits` CTAs and a second kernel sums the partial tiles into C in split
-// order (deterministic); full_tiles = 0 splits every tile.  splits is
-// reduced so no split is empty.  Single products only.
+// order (deterministic); full_tiles = 0 splits every tile.  With `cluster`
+// (full_tiles = 0, 2 <= splits <= kMaxClusterSplits, no buffer needed) the
+// splits of a tile form a thread-block cluster instead and add their
+// partial tiles through distributed shared memory, in the same split order
+// (bit-identical results), with no second kernel.  splits is reduced so no
+// split is empty.  Single products only.
+constexpr int kMaxClusterSplits = 8;  // the portable cluster size
 cudaError_t launch_tf32x3(const Problem& p, int cfg, int full_tiles,
-                          int splits, float* partials, const WaitCfg& wc,
-                          cudaStream_t stream);
+                          int splits, float* partials, bool cluster,
+                          const WaitCfg& wc, cudaStream_t stream);
 
 // Whether the streaming 3xTF32 kernel takes an N × K B (N <= 128,
 // K <= 128: B lives in TMEM).

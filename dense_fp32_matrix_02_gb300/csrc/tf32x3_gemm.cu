@@ -124,6 +124,8 @@ struct Cfg {
                 "transposed A: raw split, 128-row tiles, plain B and store");
   // the epilogue stages 8 warps × TILE_M / 64 blocks of 4 KB in the ring
   static_assert(8 * (TILE_M / 64) * 4096 <= kOffCtl, "epilogue staging");
+  // a cluster-reduced split keeps its whole partial tile in the ring
+  static_assert(TILE_M * 128 * 4 <= kOffCtl, "partial tile in the ring");
 };
 
 constexpr int kMaxStages = 8;
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                        long long ldc, int M, int N, int K, int tiles_m,
                        int tiles_n, int full_tiles, int tail_splits,
                        int kb_per_split, float* partials, long long sC,
-                       int batched_ab, int store_tma,
+                       int batched_ab, int store_tma, int cluster_reduce,
                        const float* bias, int act, RawOperands raw,
                        WaitCfg wc) {
   // batch: matrix blockIdx.z; tensor-map batch coordinates are z for a
@@ -521,7 +523,46 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
         // staged in the ring, idle now that every MMA has completed, row by
         // row in the 128-byte swizzle, and stored by one bulk tensor copy
         // that skips what lies past M or N
-        const bool tma = !Cf::kTStore && ((whole ? store_tma : store_tma >> 1) & 1);
+        const bool tma = !cluster_reduce && !Cf::kTStore &&
+                         ((whole ? store_tma : store_tma >> 1) & 1);
+        if (cluster_reduce) {
+          // this split's partial tile, row-major TILE_M × 128 fp32 at the
+          // start of the idle ring, for the cluster's reduction at the end
+          float* part = reinterpret_cast<float*>(smem);
+          constexpr long long kPartBytes = 4LL * kTileM * kTileN;
+#pragma unroll 1
+          for (int j = 0; j < kAccCols / 2 / 32; ++j) {
+            uint32_t v[32];
+            const uint32_t ta = tmem + lane_bits + c_begin + 32 * j;
+            if (tmem_span_ok(ta, 32, tmem, kTmemCols, q, st)) {
+              tmem_ld16(ta, v);
+              tmem_ld16(ta + 16, v + 16);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int r = 0; r < 32; ++r) v[r] = 0u;
+            }
+            const bool nan_here = any_nan(v);
+            const bool fix = __any_sync(0xffffffffu, nan_here);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+              float* d = part + (c_begin + 32 * j + r) * kTileN + n_loc;
+              if (span_ok(d, 4, part, kPartBytes, st))
+                *d = __uint_as_float(v[r]);
+            }
+            if (fix && nan_here && n < N) {
+#pragma unroll 1
+              for (int r = 0; r < 32; ++r) {
+                float* d = part + (c_begin + 32 * j + r) * kTileN + n_loc;
+                const int m = bm + c_begin + 32 * j + r;
+                if (!span_ok(d, 4, part, kPartBytes, st) || *d == *d ||
+                    m >= M)
+                  continue;
+                *d = ieee_dot(ro, m, n, k0, k1);
+              }
+            }
+          }
+        }
         if (tma) {
           constexpr int kBlocks = kAccCols / 2 / 32;
           unsigned char* stg = smem + (warp - 2) * kBlocks * 4096;
@@ -596,7 +637,9 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
           __syncwarp();
         }
 #pragma unroll 1
-        for (int c0 = c_begin; !tma && c0 < c_begin + kAccCols / 2; c0 += 16) {
+        for (int c0 = c_begin; !tma && !cluster_reduce &&
+                               c0 < c_begin + kAccCols / 2;
+             c0 += 16) {
           uint32_t v[16];
           if (tmem_span_ok(tmem + lane_bits + c0, 16, tmem, kTmemCols, q,
                            st)) {
@@ -677,6 +720,69 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   // the CTA barrier (a barrier reached by part of a warp does not hold it)
   __syncwarp();
   __syncthreads();
+  if (cluster_reduce) {
+    // The splits of this tile are the CTAs of this cluster (rank = split).
+    // Once every partial tile is in its CTA's shared memory (barrier 1),
+    // CTA `split` adds rows [split·TILE_M/S, (split+1)·TILE_M/S) of the S
+    // partials, read through distributed shared memory in split order
+    // 0, 1, …, S−1 (the order of the reduction kernel: identical results),
+    // applies the fused epilogue and stores those rows of C; barrier 2
+    // keeps every CTA's partial in place until all have read it.
+    cluster_sync_all();
+    if (warp >= 2) {
+      const int S = tail_splits;
+      bool any_abort = false;
+      for (int s2 = 0; s2 < S; ++s2)
+        any_abort |=
+            ld_cluster_s32(cluster_map(smem_u32(&ctl->abort), s2)) != 0;
+      if (!any_abort) {
+        const int r0 = split * kTileM / S, r1 = (split + 1) * kTileM / S;
+        const int t = threadIdx.x - 64;
+        const bool cvec = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 &&
+                          (ldc & 3) == 0;
+        const bool epi = bias != nullptr || act != 0;
+        const long long c_ext = matrix_extent_bytes(M, N, ldc);
+        unsigned int* const st = wc.status;
+        (void)c_ext, (void)st;
+        for (int g = t; g < (r1 - r0) * (kTileN / 4); g += 32 * kConvWarps) {
+          const int ml = r0 + g / (kTileN / 4), c4 = (g % (kTileN / 4)) * 4;
+          const int m = bm + ml, n = bn + c4;
+          if (m >= M || n >= N) continue;
+          const uint32_t off = sbase + (uint32_t)(ml * kTileN + c4) * 4u;
+          if (!smem_span_ok(off, 16, sbase, 4 * kTileM * kTileN, st)) continue;
+          // every split's four values in flight at once, then the sum in
+          // split order
+          float4 v[kMaxClusterSplits];
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+            if (s2 < S) v[s2] = ld_cluster_v4(cluster_map(off, s2));
+          float4 acc = v[0];
+#pragma unroll
+          for (int s2 = 1; s2 < kMaxClusterSplits; ++s2) {
+            if (s2 >= S) break;
+            acc.x += v[s2].x;
+            acc.y += v[s2].y;
+            acc.z += v[s2].z;
+            acc.w += v[s2].w;
+          }
+          float a[4] = {acc.x, acc.y, acc.z, acc.w};
+          if (epi)
+            for (int e = 0; e < 4; ++e)
+              a[e] = apply_epilogue(a[e], bias, act, n + e);
+          float* dst = C + (long long)m * ldc + n;
+          if (cvec && n + 3 < N) {
+            if (span_ok(dst, 16, C, c_ext, st))
+              *reinterpret_cast<float4*>(dst) =
+                  make_float4(a[0], a[1], a[2], a[3]);
+          } else {
+            for (int e = 0; e < 4 && n + e < N; ++e)
+              if (span_ok(dst + e, 4, C, c_ext, st)) dst[e] = a[e];
+          }
+        }
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while another reads its partial
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
@@ -768,7 +874,7 @@ bool encode_3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m,
 
 template <class Cf>
 cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
-                       float* partials, const WaitCfg& wc,
+                       float* partials, bool cluster, const WaitCfg& wc,
                        cudaStream_t stream) {
   using namespace tf32x3;
   auto encode = tensor_map_encoder();
@@ -822,20 +928,27 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
   const long long tiles = (long long)tiles_m * tiles_n;
   int ts = tail_splits;
   long long full = full_tiles;
-  if (ts < 2 || !partials || p.batch > 1 || full < 0 || full >= tiles) {
+  // every tile split, its splits one cluster: no partial-tile buffer
+  bool use_cluster = cluster && full == 0 && p.batch == 1 && ts >= 2 &&
+                     ts <= kMaxClusterSplits;
+  if (!use_cluster &&
+      (ts < 2 || !partials || p.batch > 1 || full < 0 || full >= tiles)) {
     ts = 1;
     full = tiles;
   }
   const int kb_per_split = (nk + ts - 1) / ts;
   ts = (nk + kb_per_split - 1) / kb_per_split;  // no empty split
-  if (ts < 2) full = tiles;
+  if (ts < 2) {
+    full = tiles;
+    use_cluster = false;
+  }
   const long long tail = tiles - full;
   const long long grid = full + tail * ts;
   if (grid > 0x7fffffffLL || p.batch < 1 || p.batch > 65535)
     return cudaErrorInvalidConfiguration;
   const int batched_ab =
       (p.batch > 1 && p.sA != 0 ? 1 : 0) | (p.batch > 1 && p.sB != 0 ? 2 : 0);
-  if (tail > 0 && env_store_tma()) {
+  if (tail > 0 && !use_cluster && env_store_tma()) {
     const cuuint64_t dims[2] = {128, (cuuint64_t)(tail * ts * Cf::kTileM)};
     const cuuint64_t strides[1] = {128 * 4};
     const cuuint32_t box[2] = {32, 32};
@@ -855,11 +968,17 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
   raw.sB = p.sB;
   raw.transA = Cf::kTA ? 1 : 0;
   raw.transB = Cf::kTB ? 1 : 0;
+  if (use_cluster)
+    return launch_pdl_cluster(
+        fn, dim3((unsigned)grid, 1, 1), dim3(Cf::kThreads), kSmem, stream,
+        (unsigned)ts, ta, tb, tc, tp, p.C, p.ldc, p.M, p.N, p.K, tiles_m,
+        tiles_n, 0, ts, kb_per_split, (float*)nullptr, p.sC, batched_ab,
+        store_tma, 1, p.bias, p.act, raw, wc);
   e = launch_pdl(fn, dim3((unsigned)grid, 1, (unsigned)p.batch),
                  dim3(Cf::kThreads), kSmem, stream, ta, tb, tc, tp, p.C,
                  p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, (int)full, ts,
-                 kb_per_split, partials, p.sC, batched_ab, store_tma, p.bias,
-                 p.act, raw, wc);
+                 kb_per_split, partials, p.sC, batched_ab, store_tma, 0,
+                 p.bias, p.act, raw, wc);
   if (e != cudaSuccess || tail == 0) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&
                    p.ldc % 4 == 0)
@@ -887,40 +1006,43 @@ long long tf32x3_partials_bytes(int tile_m, long long split_tiles,
 }
 
 cudaError_t launch_tf32x3(const Problem& p, int cfg, int full_tiles,
-                          int splits, float* partials, const WaitCfg& wc,
-                          cudaStream_t stream) {
+                          int splits, float* partials, bool cluster,
+                          const WaitCfg& wc, cudaStream_t stream) {
   using namespace tf32x3;
   switch (cfg) {
     case kTc256:
       return launch_cfg<Cfg<256, 5, false>>(p, full_tiles, splits, partials,
-                                            wc, stream);
+                                            cluster, wc, stream);
     case kTc128:
       return launch_cfg<Cfg<128, 4, false>>(p, full_tiles, splits, partials,
-                                            wc, stream);
+                                            cluster, wc, stream);
     case kTc128Raw:
       if (p.transB)  // A·Bᵀ with B stored N×K
         return launch_cfg<Cfg<128, 4, true, true>>(p, full_tiles, splits,
-                                                   partials, wc, stream);
+                                                   partials, cluster, wc,
+                                                   stream);
       if (p.storeT)  // caller passed (B, A) swapped: store the transpose
         return launch_cfg<Cfg<128, 4, true, false, true>>(p, full_tiles, splits,
-                                                          partials, wc, stream);
+                                                          partials, cluster,
+                                                          wc, stream);
       if (p.transA)  // Aᵀ·B with A stored K×M: A transposed by the converters
         return launch_cfg<Cfg<128, 3, true, false, false, true>>(
-            p, full_tiles, splits, partials, wc, stream);
+            p, full_tiles, splits, partials, cluster, wc, stream);
       return launch_cfg<Cfg<128, 4, true>>(p, full_tiles, splits, partials,
-                                           wc, stream);
+                                           cluster, wc, stream);
     case kTc256Raw:
       if (p.transB)
         return launch_cfg<Cfg<256, 5, true, true>>(p, full_tiles, splits,
-                                                   partials, wc, stream);
+                                                   partials, cluster, wc,
+                                                   stream);
       if (p.storeT)
         return launch_cfg<Cfg<256, 5, true, false, true>>(
-            p, full_tiles, splits, partials, wc, stream);
+            p, full_tiles, splits, partials, cluster, wc, stream);
       if (p.transA)  // the transposed-A staging exists for 128-row tiles
-        return launch_tf32x3(p, kTc128Raw, full_tiles, splits, partials, wc,
-                             stream);
+        return launch_tf32x3(p, kTc128Raw, full_tiles, splits, partials,
+                             cluster, wc, stream);
       return launch_cfg<Cfg<256, 5, true>>(p, full_tiles, splits, partials,
-                                           wc, stream);
+                                           cluster, wc, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -353,8 +353,12 @@ def test_nan_and_inf_ieee_tensor(algo, shape, ws):
     if ws:
         if algo != G.ALGO_AUTO:
             pytest.skip("scratch goes with the automatic plan")
-        c, need = run_gpu_ws(a, b)
+        c, _ = run_gpu_ws(a, b)
+        # splits added in the cluster or by the reduction kernel
+        with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+            c2, need = run_gpu_ws(a, b)
         assert need > 0
+        _check_ieee(c2, a, b, f"{shape} reduction kernel")
     else:
         c = run_gpu(a, b, algo, pad=True)
     _check_ieee(c, a, b, f"{shape}")
@@ -672,9 +676,15 @@ def test_workspace_size_policy():
     slots = _slots()
     sms = slots // 2
     tile = 128 * 128 * 4
-    # few tiles: all split, slots // tiles ways (at least 8 k stages each)
+    # few tiles: all split, slots // tiles ways (at least 8 k stages each);
+    # up to 8 ways the splits reduce within a cluster (no scratch), else
+    # (or with GEMM_F32_CLUSTER_REDUCE=0) in scratch
     assert G.plan(1024, 1024, 1024)["tile_rows"] == 128
-    assert G.workspace_size(1024, 1024, 1024) == 64 * min(slots // 64, 8) * tile
+    s1024 = min(slots // 64, 8)
+    assert G.workspace_size(1024, 1024, 1024) == (0 if s1024 <= 8 else
+                                                  64 * s1024 * tile)
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        assert G.workspace_size(1024, 1024, 1024) == 64 * s1024 * tile
     # a partly filled last round of 256 x 128 tiles: its tiles split
     # sms // tail ways
     p = G.plan(4096, 4096, 4096)
@@ -691,7 +701,11 @@ def test_workspace_size_policy():
     p = G.plan(1024, 1024, 4096)
     assert p["tile_rows"] == 256
     assert p["splits"] == min(sms // 32, 4096 // 16 // 8, 16)
-    assert G.workspace_size(1024, 1024, 4096) == 32 * p["splits"] * 2 * tile
+    assert G.workspace_size(1024, 1024, 4096) == (
+        0 if p["splits"] <= 8 else 32 * p["splits"] * 2 * tile)
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        assert G.workspace_size(1024, 1024, 4096) == \
+            32 * p["splits"] * 2 * tile
     # whole rounds: nothing to split
     assert G.workspace_size(128 * (slots // 19), 128 * 19, 4096) == 0
     assert G.workspace_size(64, 64, 64) == 0               # K too short
@@ -710,25 +724,43 @@ def test_splitk_256_row_tiles(shape):
     assert p["tile_rows"] == 256 and p["splits"] > 1, p
     a, b = synth.make_operands(M, N, K, seed=K, dist_a="normal")
     c, need = run_gpu_ws(a, b)
-    assert need > 0
+    assert (need > 0) == (p["splits"] > 8)   # clusters up to 8 splits
     check_full(a, b, c, what=f"256 split {shape}")
     ai, bi = synth.make_operands(M, N, K, seed=K + 1, dist_a="int",
                                  dist_b="int")
     ci, _ = run_gpu_ws(ai, bi)
     check_full(ai, bi, ci, exact=True, what=f"256 split {shape} int")
+    # the reduction kernel adds the same partials in the same order
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        c2, need2 = run_gpu_ws(a, b)
+    assert need2 > 0
+    assert np.array_equal(c.view(np.uint32), c2.view(np.uint32))
 
 
 @pytest.mark.parametrize("name", ["sq1024", "rag1000"])
 def test_splitk_workloads(name):
+    """Every tile split 4 ways: the splits of a tile run as one cluster and
+    add their partial tiles in distributed shared memory (no scratch, also
+    through gemm_f32 itself); with GEMM_F32_CLUSTER_REDUCE=0 they go
+    through scratch and the reduction kernel instead, with the same bits."""
     w = synth.WORKLOADS[name]
     a, b = w.operands()
+    assert G.plan(w.M, w.N, w.K)["splits"] > 1
     c, need = run_gpu_ws(a, b)
-    assert need > 0
+    assert need == 0
     check_full(a, b, c, what=f"{name} split-K")
+    assert np.array_equal(c.view(np.uint32), run_gpu(a, b).view(np.uint32))
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        c2, need2 = run_gpu_ws(a, b)
+    assert need2 > 0
+    assert np.array_equal(c.view(np.uint32), c2.view(np.uint32))
     wi = w.integer_variant()
     ai, bi = wi.operands()
     ci, _ = run_gpu_ws(ai, bi)
     check_full(ai, bi, ci, exact=True, what=f"{wi.name} split-K")
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        ci2, _ = run_gpu_ws(ai, bi)
+    check_full(ai, bi, ci2, exact=True, what=f"{wi.name} split-K kernel")
     assert G.device_status() == 0
 
 
@@ -742,19 +774,28 @@ def test_splitk_forced(splits, shape):
         need = G.workspace_size(M, N, K)
         s = min(splits, (K + 15) // 16, 16)
         tiles = ((M + 127) // 128) * ((N + 127) // 128)
-        assert need == (tiles * s * 128 * 128 * 4 if s > 1 else 0)
+        cluster = 2 <= s <= 8
+        assert need == (tiles * s * 128 * 128 * 4 if s > 1 and not cluster
+                        else 0)
         c, _ = run_gpu_ws(a, b)
         check_full(a, b, c, what=f"split {splits} {shape}")
         ai, bi = synth.make_operands(M, N, K, seed=splits, dist_a="int",
                                      dist_b="int")
         ci, _ = run_gpu_ws(ai, bi)
         check_full(ai, bi, ci, exact=True, what=f"split {splits} {shape} int")
+        if cluster:  # the reduction kernel gives the same bits
+            with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+                c2, need2 = run_gpu_ws(a, b)
+            assert need2 == tiles * s * 128 * 128 * 4
+            assert np.array_equal(c.view(np.uint32), c2.view(np.uint32))
 
 
 def test_splitk_small_workspace_falls_back():
     a, b = synth.WORKLOADS["sq1024"].operands()
-    need = G.workspace_size(1024, 1024, 1024)
-    c, _ = run_gpu_ws(a, b, ws_bytes=need - 4)
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        need = G.workspace_size(1024, 1024, 1024)
+        assert need > 0
+        c, _ = run_gpu_ws(a, b, ws_bytes=need - 4)
     check_full(a, b, c, what="too-small workspace")
 
 

@@ -18,6 +18,7 @@ from dense_fp32_matrix_02_gb300 import gemm as G
 
 SMS = 152  # GB300
 KNOBS = ["GEMM_F32_TC_CFG", "GEMM_F32_SPLITS", "GEMM_F32_TAIL_SPLIT",
+         "GEMM_F32_CLUSTER_REDUCE",
          "GEMM_F32_STREAM", "GEMM_F32_AUTO_SIMT", "GEMM_F32_SIMT_CFG",
          "GEMM_F32_MIXED_NARROW", "GEMM_F32_MIXED_BM"]
 

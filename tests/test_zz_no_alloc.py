@@ -7,9 +7,9 @@ The entry point is called through the C ABI, twice in a row, and its
 output is checked three ways: against the float64 oracle within the
 tolerance the other tests use (bit for bit on small-integer inputs), and
 bit for bit against gemm_f32_ws (the same product with caller-owned
-scratch, which runs the same deterministic split).  The shapes used are
-ones whose plan splits over K, so the static buffer is really written and
-read.  This file sorts last so that a run stopping at the first failure
+scratch, which runs the same deterministic split).  Most shapes used are
+ones whose plan splits the last round of tiles over K, so the static
+buffer is really written and read.  This file sorts last so that a run stopping at the first failure
 has already run every other test; it also passes on its own in a fresh
 process.
 """
@@ -42,15 +42,35 @@ def _noalloc(ta, tb, tc):
                            torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("name", ["sq1024", "rag1000", "rag1000_int",
-                                  "sq64"])
-def test_noalloc_matches_oracle_and_workspace_entry_point_twice(name):
-    w = (synth.WORKLOADS[name[:-4]].integer_variant() if name.endswith("_int")
-         else synth.WORKLOADS[name])
-    a, b = w.operands()
-    need = G.workspace_size(w.M, w.N, w.K)
-    # 1024^3 and 1000^3 are split over K: the static scratch is used
-    assert (need > 0) == (name != "sq64")
+# (name, M, N, K, integer): the transformer-MLP workload and two shapes
+# whose last, partly filled round of tiles is split over K through the
+# scratch (17 x 19 = 323 tiles of 128 x 128 on 304 CTA slots of 152 SMs),
+# one of them ragged and integer-valued; 1024^3 splits inside clusters and
+# needs no scratch at all; 64^3 does not split
+CASES = [("mlp", 8192, 3072, 768, False),
+         ("tail", 17 * 128, 19 * 128, 512, False),
+         ("tail_int", 2100, 2420, 1000, True),
+         ("sq1024", 1024, 1024, 1024, False),
+         ("sq64", 64, 64, 64, False)]
+
+
+@pytest.mark.parametrize("name,M,N,K,integer", CASES,
+                         ids=[c[0] for c in CASES])
+def test_noalloc_matches_oracle_and_workspace_entry_point_twice(
+        name, M, N, K, integer):
+    if name == "mlp":
+        a, b = synth.WORKLOADS["mlp"].operands()
+    else:
+        dist = "int" if integer else "uniform"
+        a, b = synth.make_operands(M, N, K, seed=M + K, dist_a=dist,
+                                   dist_b=dist)
+    need = G.workspace_size(M, N, K)
+    p = G.plan(M, N, K)
+    # the static scratch is used where the plan splits a partly filled
+    # last round of tiles (whole tiles before the split ones)
+    assert (need > 0) == (p["splits"] > 1 and p["whole_tiles"] > 0)
+    if name in ("mlp", "tail", "tail_int"):
+        assert need > 0, p
     assert need <= G.noalloc_scratch_bytes()
     ta = torch.from_numpy(a).to(DEV)
     tb = torch.from_numpy(b).to(DEV)
@@ -60,7 +80,7 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_twice(name):
     torch.cuda.synchronize()
     c_ws = c_ws.cpu().numpy()
     ref, bound, _ = oracle.gemm(a, b)
-    tc = torch.empty(w.M, w.N, device=DEV)
+    tc = torch.empty(M, N, device=DEV)
     free_after = []
     for call in range(2):
         tc.fill_(float("nan"))
@@ -68,11 +88,11 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_twice(name):
         torch.cuda.synchronize()
         free_after.append(torch.cuda.mem_get_info(DEV)[0])
         c = tc.cpu().numpy()
-        what = f"{w.name} call {call}"
-        if w.dist_a == "int":
+        what = f"{name} call {call}"
+        if integer:
             assert_bitexact(c, ref, what)
         else:
-            assert_within_tolerance(c, ref, bound, w.K, what)
+            assert_within_tolerance(c, ref, bound, K, what)
         # same plan, same split, same summation order as gemm_f32_ws
         assert np.array_equal(c.view(np.uint32), c_ws.view(np.uint32)), what
     # the second call took no device memory
@@ -81,12 +101,16 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_twice(name):
 
 
 def test_noalloc_rejects_products_beyond_its_scratch():
+    """A split whose partial tiles need more than the static buffer holds
+    is refused with GEMM_F32_ERR_SCRATCH_LIMIT and nothing runs (256-row
+    tiles, a last round of half the SMs split two ways: about 20 MB on 152
+    SMs)."""
     cap = G.noalloc_scratch_bytes()
     shape = None
-    for n in (1536, 1600, 1700, 1800, 1900):
-        need = G.workspace_size(n, n, 4096)
+    for rows in range(8, 64):
+        need = G.workspace_size(256 * rows, 1536, 4096)
         if need > cap:
-            shape = (n, n, 4096)
+            shape = (256 * rows, 1536, 4096)
             break
     if shape is None:
         pytest.skip("no candidate shape needs more scratch on this GPU")
