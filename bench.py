@@ -654,7 +654,9 @@ def sub_record(w, ms, steps, clocks, kernel, entry, peaks, tf32_peak,
            "entry": entry, "kernel": kernel, "value": tflops,
            "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
            "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_min_mhz",
-                                                 "samples", "reasons")}}
+                                                 "samples", "reasons")},
+           "traffic": recorded_traffic(kernel, w.name),
+           "algorithmic_bytes": w.bytes}
     bw_roof = w.flops / w.bytes * peaks["hbm_gbs"] / 1e3
     if kernel.startswith("tf32x3"):
         if bw_roof < tf32_peak / 3.0:
