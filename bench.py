@@ -126,6 +126,18 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
+def product_launches(plan, ws_bytes):
+    """Kernel launches of one automatic product: a split plan adds the
+    reduction kernel when the partial tiles go through scratch, or, when
+    its split tiles reduce within clusters, a launch of their own after the
+    whole tiles (if any)."""
+    if plan["algo"] != 3 or plan["splits"] < 2:
+        return 1
+    if ws_bytes:
+        return 2
+    return 2 if plan["whole_tiles"] > 0 else 1
+
+
 def hbm_roofline(flops, nbytes, kernel_ms, peaks, peaks_src, tensor_peak,
                  achieved):
     """Roofline entry of a memory-bound launch: algorithmic bytes per
@@ -778,7 +790,8 @@ def run_ours(args, w, config):
     # on grids too small to fill the GPU); a forced kernel through gemm_f32_ex
     ws_bytes = G.workspace_size(w.M, w.N, w.K) if algo == 0 else 0
     ws = torch.empty(max(ws_bytes // 4, 1), device=dev) if ws_bytes else None
-    launches_per_step = 2 if ws_bytes else 1
+    launches_per_step = product_launches(G.plan(w.M, w.N, w.K), ws_bytes) \
+        if algo == 0 else 1
 
     batched = args.op != "nn" or args.batch > 1
     if batched:

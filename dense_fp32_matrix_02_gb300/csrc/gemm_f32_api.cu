@@ -148,11 +148,11 @@ int choose_tc_cfg(int64_t M, int64_t N, int64_t K, const DeviceInfo& d) {
 //    tile costs about as long as a full round);
 // at least 8 k stages per split, at most 16 splits.  GEMM_F32_SPLITS forces
 // every tile to split that many ways; GEMM_F32_TAIL_SPLIT=0 keeps the last
-// round whole.  When every tile is split at most kMaxClusterSplits ways,
-// the splits of a tile run as one thread-block cluster and add their
-// partial tiles in distributed shared memory: no scratch, no second kernel
-// (GEMM_F32_CLUSTER_REDUCE=0 takes the scratch and the reduction kernel
-// instead).  Tail splits of a partly filled last round keep the scratch.
+// round whole.  Up to kMaxClusterSplits ways, the splits of a tile run as
+// one thread-block cluster and add their partial tiles in distributed
+// shared memory: no scratch and no reduction kernel (a split tail runs as
+// a second launch after the whole tiles'; GEMM_F32_CLUSTER_REDUCE=0 takes
+// the scratch and the reduction kernel instead).
 void choose_splits(int64_t M, int64_t N, int64_t K, int tile_m,
                    const DeviceInfo& d, Plan* plan) {
   const int forced = env_int("GEMM_F32_SPLITS", 0);
@@ -177,7 +177,7 @@ void choose_splits(int64_t M, int64_t N, int64_t K, int tile_m,
   }
   plan->splits = (int)s;
   plan->full_tiles = (int)full;
-  plan->cluster = s >= 2 && full == 0 && s <= kMaxClusterSplits &&
+  plan->cluster = s >= 2 && s <= kMaxClusterSplits &&
                   env_int("GEMM_F32_CLUSTER_REDUCE", 1) != 0;
   plan->ws_bytes = plan->cluster
                        ? 0

@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
                        int tiles_n, int full_tiles, int tail_splits,
                        int kb_per_split, float* partials, long long sC,
                        int batched_ab, int store_tma, int cluster_reduce,
-                       const float* bias, int act, RawOperands raw,
-                       WaitCfg wc) {
+                       int cta_base, int pdl_flags, const float* bias,
+                       int act, RawOperands raw, WaitCfg wc) {
   // batch: matrix blockIdx.z; tensor-map batch coordinates are z for a
   // batched operand and 0 for one shared by every product (batched_ab bits
   // 0 = A, 1 = B); C advances by sC per product.
@@ -217,12 +217,14 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   // stages [s·kb_per_split, min(nk, (s+1)·kb_per_split)) of tail tile j and
   // stores that partial tile, TILE_M × 128 row-major, to workspace slot
   // j·tail_splits + s; a second kernel adds the slots in split order.
-  const bool whole = (int)blockIdx.x < full_tiles;
-  const int jt = whole ? 0 : ((int)blockIdx.x - full_tiles) / tail_splits;
-  const int split = whole ? 0 : ((int)blockIdx.x - full_tiles) % tail_splits;
+  // (cta_base: the index of this launch's first CTA in that numbering —
+  // a launch of only the split tail tiles starts at full_tiles)
+  const int cta = (int)blockIdx.x + cta_base;
+  const bool whole = cta < full_tiles;
+  const int jt = whole ? 0 : (cta - full_tiles) / tail_splits;
+  const int split = whole ? 0 : (cta - full_tiles) % tail_splits;
   int tm, tn;
-  tile_coords<8>(whole ? (int)blockIdx.x : full_tiles + jt, tiles_m, tiles_n,
-                 tm, tn);
+  tile_coords<8>(whole ? cta : full_tiles + jt, tiles_m, tiles_n, tm, tn);
   const int bm = tm * kTileM, bn = tn * kTileN;
   const int nk_total = (K + kBK - 1) / kBK;
   const int kb0 = split * kb_per_split;
@@ -268,7 +270,13 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
-  griddep_wait();  // A, B, C and the scratch may belong to the kernel before
+  // pdl_flags bit 1: the launch of the split tail tiles that follows a
+  // launch of the whole tiles; it needs nothing from that kernel (other
+  // tiles of C), which let it be scheduled once past its own wait (bit 0),
+  // so it starts at once and waits for it only before it ends
+  if (!(pdl_flags & 2))
+    griddep_wait();  // A, B, C and the scratch may belong to the kernel before
+  if (pdl_flags & 1) griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -787,6 +795,9 @@ __global__ void __launch_bounds__(Cf::kThreads, Cf::kMinBlocks)
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // the kernel the next one in the stream waits for must not end before
+  // the whole-tile launch it overlapped
+  if (pdl_flags & 2) griddep_wait();
 }
 
 // Tail tile j (tile full_tiles + j in the grouped order): C = the sum over
@@ -928,9 +939,9 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
   const long long tiles = (long long)tiles_m * tiles_n;
   int ts = tail_splits;
   long long full = full_tiles;
-  // every tile split, its splits one cluster: no partial-tile buffer
-  bool use_cluster = cluster && full == 0 && p.batch == 1 && ts >= 2 &&
-                     ts <= kMaxClusterSplits;
+  // the split tiles' splits as clusters: no partial-tile buffer
+  bool use_cluster = cluster && p.batch == 1 && ts >= 2 &&
+                     ts <= kMaxClusterSplits && full >= 0 && full < tiles;
   if (!use_cluster &&
       (ts < 2 || !partials || p.batch > 1 || full < 0 || full >= tiles)) {
     ts = 1;
@@ -968,16 +979,30 @@ cudaError_t launch_cfg(const Problem& p, int full_tiles, int tail_splits,
   raw.sB = p.sB;
   raw.transA = Cf::kTA ? 1 : 0;
   raw.transB = Cf::kTB ? 1 : 0;
-  if (use_cluster)
+  if (use_cluster) {
+    // whole tiles first (if any), in a launch of their own that lets the
+    // next one be scheduled once past its wait for the kernel before; then
+    // the split tiles, one cluster per tile, which overlap its last round
+    // and wait for it only before they end
+    if (full > 0) {
+      e = launch_pdl(fn, dim3((unsigned)full, 1, 1), dim3(Cf::kThreads),
+                     kSmem, stream, ta, tb, tc, tp, p.C, p.ldc, p.M, p.N,
+                     p.K, tiles_m, tiles_n, (int)full, ts, kb_per_split,
+                     (float*)nullptr, p.sC, batched_ab, store_tma, 0, 0, 1,
+                     p.bias, p.act, raw, wc);
+      if (e != cudaSuccess) return e;
+    }
     return launch_pdl_cluster(
-        fn, dim3((unsigned)grid, 1, 1), dim3(Cf::kThreads), kSmem, stream,
-        (unsigned)ts, ta, tb, tc, tp, p.C, p.ldc, p.M, p.N, p.K, tiles_m,
-        tiles_n, 0, ts, kb_per_split, (float*)nullptr, p.sC, batched_ab,
-        store_tma, 1, p.bias, p.act, raw, wc);
+        fn, dim3((unsigned)(tail * ts), 1, 1), dim3(Cf::kThreads), kSmem,
+        stream, (unsigned)ts, ta, tb, tc, tp, p.C, p.ldc, p.M, p.N, p.K,
+        tiles_m, tiles_n, (int)full, ts, kb_per_split, (float*)nullptr, p.sC,
+        batched_ab, store_tma, 1, (int)full, full > 0 ? 2 : 0, p.bias, p.act,
+        raw, wc);
+  }
   e = launch_pdl(fn, dim3((unsigned)grid, 1, (unsigned)p.batch),
                  dim3(Cf::kThreads), kSmem, stream, ta, tb, tc, tp, p.C,
                  p.ldc, p.M, p.N, p.K, tiles_m, tiles_n, (int)full, ts,
-                 kb_per_split, partials, p.sC, batched_ab, store_tma, 0,
+                 kb_per_split, partials, p.sC, batched_ab, store_tma, 0, 0, 0,
                  p.bias, p.act, raw, wc);
   if (e != cudaSuccess || tail == 0) return e;
   const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 &&

@@ -96,11 +96,13 @@ typedef enum {
 
 /*
  * C = A·B.  M, N, K >= 0.  M == 0 or N == 0: returns OK and launches
- * nothing.  K == 0: C[0:M, 0:N] is set to 0 (the empty sum).  Products
- * whose tiles would leave most of the GPU idle (on the tensor path) split
- * K over up to 8 CTAs per tile, which run as one thread-block cluster and
- * add their partial tiles in distributed shared memory in a fixed order:
- * no scratch is needed and results are deterministic.
+ * nothing.  K == 0: C[0:M, 0:N] is set to 0 (the empty sum).  On the
+ * tensor path, tiles that would leave SMs idle — every tile of a product
+ * too small to fill the GPU, or the tiles of a larger product's last,
+ * partly filled round — split K over up to 8 CTAs each, which run as one
+ * thread-block cluster and add their partial tiles in distributed shared
+ * memory in a fixed order: no scratch is needed and results are
+ * deterministic.
  */
 GEMM_F32_API int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
              const float *B, int64_t ldb, float *C, int64_t ldc,
@@ -290,11 +292,10 @@ GEMM_F32_API int64_t gemm_f32_ffma_peak_flops(int64_t iters);
 
 /*
  * As gemm_f32 (automatic kernel choice), with caller-owned device scratch
- * that the library may use to split K over several CTAs per tile where a
- * cluster cannot hold the split: the tiles of the last, partly filled
- * round of a larger product (spread over the whole GPU instead of one per
- * SM), or more than 8 splits per tile.  A second kernel then sums the
- * partial tiles in a fixed order, so results stay deterministic.
+ * that the library may use where a cluster cannot hold a tile's splits:
+ * more than 8 splits per tile (a few tiles with a long K).  A second
+ * kernel then sums the partial tiles in a fixed order, so results stay
+ * deterministic.  gemm_f32_workspace_size is 0 for every other product.
  * `workspace` must be 16-byte aligned device memory of `workspace_bytes`
  * bytes (NULL with 0 is allowed); if it is smaller than
  * gemm_f32_workspace_size(M, N, K) the call runs without splitting.  The
@@ -381,10 +382,10 @@ GEMM_F32_API int gemm_f32_select_algo(int64_t M, int64_t N, int64_t K, const flo
  * out[1]: tensor-kernel variant, 0 tiled, 1 streaming (B held in tensor
  * memory: N <= 128, K <= 128 and at least one 128-row tile per SM; the
  * environment variable GEMM_F32_STREAM=0 turns it off); out[2]: split-K
- * ways of the split tiles (1: none); out[3]: tiles computed whole before
- * the split ones (0 with 2..8 splits: every tile split, reduced within
- * thread-block clusters, no scratch; GEMM_F32_CLUSTER_REDUCE=0 takes the
- * scratch instead); out[4]: rows of C per tensor tile (256 when K >= 2048,
+ * ways of the split tiles (1: none; 2..8 reduce within thread-block
+ * clusters, more through scratch; GEMM_F32_CLUSTER_REDUCE=0 takes the
+ * scratch for every split); out[3]: tiles computed whole before the split
+ * ones; out[4]: rows of C per tensor tile (256 when K >= 2048,
  * else 128; 0 for the FFMA kernels).  Returns a status
  * (GEMM_F32_ERR_INVALID_ARG also for out == NULL).
  */

@@ -178,13 +178,21 @@ def test_workload_large_full(name, integer):
     if want is not None:
         assert (p["tile_rows"], p["splits"], p["whole_tiles"]) == want, p
     c, need = run_like_bench(a, b)
-    assert (need > 0) == (p["splits"] > 1)
+    # up to 8 splits a tile reduce within thread-block clusters: no scratch
+    assert (need > 0) == (p["splits"] > 8)
     plain = run_gpu(a, b)
     for got, path in ((c, "bench path"), (plain, "gemm_f32")):
         if integer:
             assert_bitexact(got, ref, f"{w.name} {path}")
         else:
             assert_within_tolerance(got, ref, bound, w.K, f"{w.name} {path}")
+    if p["splits"] > 1:
+        # the partial tiles through scratch and the reduction kernel: the
+        # same sums in the same order, the same bits
+        with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+            c2, need2 = run_like_bench(a, b)
+        assert need2 > 0
+        assert np.array_equal(c.view(np.uint32), c2.view(np.uint32))
     assert G.device_status() == 0
 
 
@@ -692,7 +700,10 @@ def test_workspace_size_policy():
     tail = 512 % sms
     s = min(sms // tail, 4096 // 16 // 8, 16)
     assert G.workspace_size(4096, 4096, 4096) == (tail * s * 2 * tile
-                                                  if s > 1 else 0)
+                                                  if s > 8 else 0)
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        assert G.workspace_size(4096, 4096, 4096) == (tail * s * 2 * tile
+                                                      if s > 1 else 0)
     assert p["splits"] == (s if s > 1 else 1)
     assert p["whole_tiles"] == (512 - tail if s > 1 else 0)
     # K below 2048: 128-row tiles; few 256-row tiles are split over K
@@ -812,14 +823,26 @@ def test_tail_split_shapes(shape):
     if ((M + 127) // 128) * ((N + 127) // 128) <= _slots():
         pytest.skip("this GPU fills the tiles in one round")
     a, b = synth.make_operands(M, N, K, seed=M + K)
+    p = G.plan(M, N, K)
+    assert p["splits"] > 1 and p["whole_tiles"] > 0, p
+    # the split tail tiles as thread-block clusters (no scratch) ...
     c, need = run_gpu_ws(a, b)
-    assert need > 0
+    assert need == 0
     check_full(a, b, c, what=f"tail split {shape}")
     ai, bi = synth.make_operands(M, N, K, seed=N, dist_a="int", dist_b="int")
     ci, _ = run_gpu_ws(ai, bi)
     check_full(ai, bi, ci, exact=True, what=f"tail split {shape} int")
     c2, _ = run_gpu_ws(a, b)
     assert np.array_equal(c.view(np.uint32), c2.view(np.uint32))
+    assert np.array_equal(c.view(np.uint32), run_gpu(a, b, pad=True).view(
+        np.uint32))
+    # ... and through scratch and the reduction kernel: the same bits
+    with _env("GEMM_F32_CLUSTER_REDUCE", 0):
+        c3, need3 = run_gpu_ws(a, b)
+        ci3, _ = run_gpu_ws(ai, bi)
+    assert need3 > 0
+    assert np.array_equal(c.view(np.uint32), c3.view(np.uint32))
+    check_full(ai, bi, ci3, exact=True, what=f"tail split {shape} int kernel")
     assert G.device_status() == 0
 
 
@@ -833,7 +856,7 @@ def test_tail_split_256_row_tiles():
     rows = -(-(sms + 16) // 8)
     M, N, K = rows * 256 - 77, 8 * 128 - 50, 2048 + 13
     p = G.plan(M, N, K)
-    assert p["tile_rows"] == 256 and p["splits"] > 1, p
+    assert p["tile_rows"] == 256 and p["splits"] > 8, p  # scratch, kernel
     assert p["whole_tiles"] == sms, p
     assert (p["tile_rows"], p["splits"], p["whole_tiles"]) == \
         expected_tail_plan(M, N, K)

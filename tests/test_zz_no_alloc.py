@@ -42,14 +42,15 @@ def _noalloc(ta, tb, tc):
                            torch.cuda.current_stream().cuda_stream)
 
 
-# (name, M, N, K, integer): the transformer-MLP workload and two shapes
-# whose last, partly filled round of tiles is split over K through the
-# scratch (17 x 19 = 323 tiles of 128 x 128 on 304 CTA slots of 152 SMs),
-# one of them ragged and integer-valued; 1024^3 splits inside clusters and
-# needs no scratch at all; 64^3 does not split
-CASES = [("mlp", 8192, 3072, 768, False),
-         ("tail", 17 * 128, 19 * 128, 512, False),
-         ("tail_int", 2100, 2420, 1000, True),
+# (name, M, N, K, integer): products whose tiles split more than 8 ways
+# (few 256 x 128 tiles, long K), the one case a plan still needs scratch,
+# one of them ragged and one integer-valued; the transformer-MLP workload
+# (its last round split 6 ways), 1024^3 (every tile split 4 ways) and 64^3
+# (no split) need none: their splits reduce within thread-block clusters
+CASES = [("split16", 256, 256, 4096, False),
+         ("split16_ragged", 300, 260, 2100, False),
+         ("split16_int", 512, 384, 2048, True),
+         ("mlp", 8192, 3072, 768, False),
          ("sq1024", 1024, 1024, 1024, False),
          ("sq64", 64, 64, 64, False)]
 
@@ -66,10 +67,9 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_twice(
                                    dist_b=dist)
     need = G.workspace_size(M, N, K)
     p = G.plan(M, N, K)
-    # the static scratch is used where the plan splits a partly filled
-    # last round of tiles (whole tiles before the split ones)
-    assert (need > 0) == (p["splits"] > 1 and p["whole_tiles"] > 0)
-    if name in ("mlp", "tail", "tail_int"):
+    # the static scratch is used where a tile splits more than 8 ways
+    assert (need > 0) == (p["splits"] > 8)
+    if name.startswith("split16"):
         assert need > 0, p
     assert need <= G.noalloc_scratch_bytes()
     ta = torch.from_numpy(a).to(DEV)
@@ -102,15 +102,17 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_twice(
 
 def test_noalloc_rejects_products_beyond_its_scratch():
     """A split whose partial tiles need more than the static buffer holds
-    is refused with GEMM_F32_ERR_SCRATCH_LIMIT and nothing runs (256-row
-    tiles, a last round of half the SMs split two ways: about 20 MB on 152
-    SMs)."""
+    is refused with GEMM_F32_ERR_SCRATCH_LIMIT and nothing runs (nine
+    256 x 128 tiles split 16 ways: about 19 MB on 152 SMs)."""
     cap = G.noalloc_scratch_bytes()
     shape = None
-    for rows in range(8, 64):
-        need = G.workspace_size(256 * rows, 1536, 4096)
-        if need > cap:
-            shape = (256 * rows, 1536, 4096)
+    for rows in range(1, 9):
+        for cols in range(1, 9):
+            need = G.workspace_size(256 * rows, 128 * cols, 4096)
+            if need > cap:
+                shape = (256 * rows, 128 * cols, 4096)
+                break
+        if shape:
             break
     if shape is None:
         pytest.skip("no candidate shape needs more scratch on this GPU")
