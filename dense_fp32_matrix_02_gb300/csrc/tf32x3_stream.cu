@@ -6,20 +6,27 @@
 // fp32; a·b ≈ a_big·b_big + a_big·b_small + a_small·b_big), computed as
 // Cᵀ = Bᵀ·Aᵀ tile by tile: TMEM lane n holds column n of C.
 //
-// One persistent CTA per SM (576 threads) walks 128-row tiles of C:
+// One persistent CTA per SM (608 threads) walks 128-row tiles of C:
 //   warp 0       TMA producer: A in 16-deep k stages (128 rows × 64 bytes,
 //                64-byte swizzle) into a 10-stage ring that runs on across
 //                tiles, so the loads of the next tiles are in flight while
 //                this one is multiplied and stored;
-//   warp 1       TMEM allocator (all 512 columns) and MMA issuer: per stage
-//                2 k-steps × 3 tcgen05.mma kind::tf32 (M 128 = columns of
-//                C, N 128 = rows, K 8) into one of two accumulators;
-//   warps 2-9    converters: once, Bᵀ (raw and small parts, zero past N and
+//   warps 1-2    MMA issuers (warp 1 also allocates all 512 TMEM columns),
+//                taking the tiles in turn, each into its own accumulator:
+//                per stage 2 k-steps × 3 tcgen05.mma kind::tf32 (M 128 =
+//                columns of C, N 128 = rows, K 8).  One issuing thread gets
+//                through about one such instruction per 80 ns, under half
+//                the tensor core's rate for this shape, so one issuer alone
+//                left the tensor core idle more than half the time and
+//                bounded the kernel (a second issuer: 106.7 -> 83.5 us at
+//                1048576 × 64 × 64, 12.8 -> 11.1 us at 65536 × 64 × 64);
+//   warps 3-10   converters: once, Bᵀ (raw and small parts, zero past N and
 //                K) into TMEM from B, which the producer's first copy puts
 //                in the epilogue's staging buffers (free until the first
 //                tile is stored); then per stage the small part of the A
-//                tile into its own shared buffer;
-//   warps 10-17  epilogue: two per TMEM lane quarter, each reading half of
+//                tile into its own shared buffer, signalling the barrier of
+//                the tile's issuer;
+//   warps 11-18  epilogue: two per TMEM lane quarter, each reading half of
 //                the accumulator's columns (64 rows of C) in one go and
 //                releasing it at once, so the tile after next accumulates
 //                into it while this one is stored.  With the fused bias /
@@ -53,7 +60,12 @@ constexpr int kTileN = 128;  // columns of C (the MMA's M, TMEM lanes)
 constexpr int kBK = 16;      // k per stage: 64-byte rows
 constexpr int kStages = 10;
 constexpr int kConvWarps = 8, kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * (kConvWarps + kEpiWarps);  // 576
+// MMA issuers: warps 1 .. kIssuers; issuer w takes the tiles i (this CTA's
+// count) with i mod kIssuers = w, accumulator i mod 2
+constexpr int kIssuers = 2;
+constexpr int kConvBase = 1 + kIssuers;                // first converter warp
+constexpr int kEpiBase = kConvBase + kConvWarps;       // first epilogue warp
+constexpr int kThreads = 32 * (kEpiBase + kEpiWarps);  // 608
 constexpr int kStageBytes = kTileM * kBK * 4;                  // 8 KB
 constexpr int kOffSmall = kStages * kStageBytes;
 constexpr int kStagingBytes = 32 * 32 * 4;  // one 32×32 fp32 block
@@ -68,7 +80,7 @@ constexpr uint32_t kSleepNs = 100000;
 
 struct __align__(8) Control {
   uint64_t full[kStages];   // TMA -> converters (transaction bytes)
-  uint64_t conv[kStages];   // converters -> MMA (one arrival per warp)
+  uint64_t conv[kIssuers][kStages];  // converters -> the tile's issuer
   uint64_t empty[kStages];  // MMA completion -> producer
   uint64_t acc_full[2];     // last MMA of a tile -> epilogue
   uint64_t acc_empty[2];    // epilogue warps -> MMA (one arrival per warp)
@@ -95,6 +107,30 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
                                             true));
 }
 
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+
+// Recomputes, in IEEE arithmetic (see ieee_dot), every NaN in column n of C,
+// rows [m_lo, m_hi) (the split product gives NaN where an operand is
+// infinite), with the fused bias / activation.  Kept out of line so the
+// epilogue's usual path carries none of it.
+__device__ __noinline__ void repair_nan_rows(float* C, long long ldc, int M,
+                                             int N, int K, int m_lo,
+                                             int m_hi, int n, float bias_n,
+                                             int act, bool epi,
+                                             RawOperands raw,
+                                             unsigned int* status) {
+  const long long c_ext = matrix_extent_bytes(M, N, ldc);
+  for (int m = m_lo; m < m_hi && m < M; ++m) {
+    float* d = C + (long long)m * ldc + n;
+    if (!span_ok(d, 4, C, c_ext, status) || *d == *d) continue;
+    float y = ieee_dot(raw, m, n, 0, K);
+    if (epi) y = epilogue_act(y + bias_n, act);
+    *d = y;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_stream_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
@@ -109,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Control* ctl = reinterpret_cast<Control*>(smem + kOffCtl);
   volatile int* abort = &ctl->abort;
   auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
-  auto conv = [&](int s) { return smem_u32(&ctl->conv[s]); };
+  auto conv = [&](int w, int s) { return smem_u32(&ctl->conv[w][s]); };
   auto empty = [&](int s) { return smem_u32(&ctl->empty[s]); };
   auto acc_full = [&](int b) { return smem_u32(&ctl->acc_full[b]); };
   auto acc_empty = [&](int b) { return smem_u32(&ctl->acc_empty[b]); };
@@ -124,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(conv(s), kConvWarps);
+      for (int w = 0; w < kIssuers; ++w) mbar_init(conv(w, s), kConvWarps);
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -133,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(b_full, 1);
     mbar_init(b_ready, kConvWarps);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, kIssuers);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -190,16 +226,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_status(wc.status, kStatusTimeoutDrain);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp < kConvBase) {
+    // ----------------------------------------------------------- MMA issuers
     if (lane == 0) {
+      const int w = warp - 1;
       bool ok = wait_phase(b_ready, 0, wc.limit, abort, false);
       if (!ok) {
         *abort = 1;
         record_status(wc.status, kStatusTimeoutFull);
       }
-      int it = 0;
+      // bit s: parity of this issuer's next wait on conv(w, s); its own
+      // uses of ring slot s complete that barrier's phases in order
+      uint32_t conv_par = 0;
       for (int t = blockIdx.x, i = 0; ok && t < tiles; t += gridDim.x, ++i) {
+        if (i % kIssuers != w) continue;
+        int it = i * nks;  // the tile's first stage, over all tiles
         const int b = i & 1;
         if (i >= 2 && !wait_phase(acc_empty(b), ((i >> 1) - 1) & 1, wc.limit,
                                   abort, false)) {
@@ -211,8 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem + b * kAccCols;
         for (int kb = 0; kb < nks; ++kb, ++it) {
           const int s = it % kStages;
-          if (!wait_phase(conv(s), (it / kStages) & 1, wc.limit, abort,
-                          false)) {
+          const uint32_t par = (conv_par >> s) & 1u;
+          conv_par ^= 1u << s;
+          if (!wait_phase(conv(w, s), par, wc.limit, abort, false)) {
             *abort = 1;
             record_status(wc.status, kStatusTimeoutFull);
             ok = false;
@@ -240,10 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_phase(mma_done, 0, kDrainNs, nullptr, false))
         record_status(wc.status, kStatusTimeoutDrain);
     }
-  } else if (warp < 2 + kConvWarps) {
+  } else if (warp < kEpiBase) {
     // ------------------------------------------------------------ converters
     const int q = warp & 3;         // TMEM lane quarter
-    const int h = (warp - 2) >> 2;  // half of Bᵀ's k range
+    const int h = (warp - kConvBase) >> 2;  // half of Bᵀ's k range
     const int n = q * 32 + lane;    // column of C = TMEM lane
     const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
     // Bᵀ, k in [h·kp/2, (h+1)·kp/2) (a multiple of 8 wide): column n of
@@ -280,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(b_ready);
 
-    const int t32 = threadIdx.x - 64;  // 0..255
+    const int t32 = threadIdx.x - 32 * kConvBase;  // 0..255
     int it = 0;
-    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+    for (int t = blockIdx.x, i = 0; ok && t < tiles; t += gridDim.x, ++i) {
       for (int kb = 0; kb < nks; ++kb, ++it) {
         const int s = it % kStages;
         if (!warp_wait(full(s), (it / kStages) & 1, wc.limit, abort)) {
@@ -310,12 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(conv(s));
+        if (lane == 0) mbar_arrive(conv(i % kIssuers, s));
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 2 - kConvWarps;  // 0..7
+    const int e = warp - kEpiBase;        // 0..7
     const int q = warp & 3;               // TMEM lane quarter
     const int hh = e >> 2;                // half of the accumulator columns
     const int n = q * 32 + lane;
@@ -357,10 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(b));
       const int m0 = t * kTileM + c_begin;
-      // NaN outputs (an infinite operand) are recomputed in IEEE
-      // arithmetic after staging or storing (see ieee_dot)
       const bool nan_here = any_nan(v);
-      const bool fix = __any_sync(0xffffffffu, nan_here) && nan_here && n < N;
       if (epi) {
 #pragma unroll
         for (int r = 0; r < kAccCols / 2; ++r)
@@ -385,22 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (span_ok(sp, 4, stg0, 2 * kStagingBytes, wc.status))
               *reinterpret_cast<uint32_t*>(sp) = v[32 * j + r];
           }
-          if (fix) {
-#pragma unroll 1
-            for (int r = 0; r < 32; ++r) {
-              uint32_t* slot = reinterpret_cast<uint32_t*>(
-                  stg + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
-                                   ((lane & 3) << 2)));
-              if (!span_ok(slot, 4, stg0, 2 * kStagingBytes, wc.status))
-                continue;
-              const float x = __uint_as_float(*slot);
-              const int m = m0 + 32 * j + r;
-              if (x == x || m >= M) continue;
-              float y = ieee_dot(raw, m, n, 0, K);
-              if (epi) y = epilogue_act(y + bias_n, act);
-              *slot = __float_as_uint(y);
-            }
-          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && m0 + 32 * j < M) {
@@ -417,16 +440,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (m0 + r < M && span_ok(d, 4, C, c_ext, wc.status))
             *d = __uint_as_float(v[r]);
         }
-        if (fix) {
-#pragma unroll 1
-          for (int r = 0; r < kAccCols / 2 && m0 + r < M; ++r) {
-            float* d = C + (long long)(m0 + r) * ldc + n;
-            if (!span_ok(d, 4, C, c_ext, wc.status) || *d == *d) continue;
-            float y = ieee_dot(raw, m0 + r, n, 0, K);
-            if (epi) y = epilogue_act(y + bias_n, act);
-            *d = y;
-          }
+      }
+      // NaN outputs (an infinite operand) are recomputed in IEEE arithmetic
+      // once this warp's stores of the tile have landed; out of line, so
+      // the common case pays only for the test
+      if (__any_sync(0xffffffffu, nan_here)) {
+        if (c_tma) {
+          if (lane == 0) bulk_wait_group<0>();
+          __syncwarp();
+          fence_proxy_async_global();
         }
+        if (nan_here && n < N)
+          repair_nan_rows(C, ldc, M, N, K, m0, m0 + kAccCols / 2, n, bias_n,
+                          act, epi, raw, wc.status);
+        __syncwarp();
       }
     }
     if (c_tma && lane == 0) bulk_wait_group<0>();  // C written
