@@ -555,10 +555,11 @@ def _stream_shapes():
             (r, 1, 1),
             (2 * r + 5, 100, 77),    # ragged N and K, a partial last tile
             (r + 1, 33, 16),
-            (3 * r - 3, 65, 120)]
+            (3 * r - 3, 65, 120),
+            (9 * r + 77, 64, 64)]    # > 8 tiles a CTA: the 10-stage ring
 
 
-@pytest.mark.parametrize("case", range(6))
+@pytest.mark.parametrize("case", range(7))
 def test_stream_kernel_shapes(case):
     """N <= 128, K <= 128 and a tile per SM: the persistent kernel that
     keeps Bᵀ in TMEM; every element against the oracle, and integers
