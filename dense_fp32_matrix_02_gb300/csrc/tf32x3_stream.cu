@@ -107,6 +107,21 @@ constexpr int smem_bytes(int stages) {
 }
 static_assert(smem_bytes(kMaxStages) <= 227 * 1024, "shared memory budget");
 
+// Tiles of A per CTA prefetched into L2 before the wait for the kernel
+// before (see the prologue).
+constexpr int kPrefetchTiles = 2;
+
+// Asks the TMA unit to bring the box at (x, y) of a tensor map into L2
+// (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x,
+                                                   int y) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::
+          "l"(tmap),
+      "r"(x), "r"(y)
+      : "memory");
+}
+
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            long long limit_ns,
                                            volatile int* abort, bool sleep) {
@@ -196,6 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
     if (c_tma) prefetch_tmap(&tmap_c);
+    // While the kernel before ends, bring this CTA's first tiles of A and
+    // all of B into L2.  A prefetch only warms L2 (the point of coherence,
+    // so nothing stale can be read later): the copies that use the data
+    // still wait for that kernel first.
+    for (int t = blockIdx.x, j = 0; j < kPrefetchTiles && t < tiles;
+         t += gridDim.x, ++j)
+      for (int kb = 0; kb < nks; ++kb)
+        tma_prefetch_l2_2d(&tmap_a, kb * kBK, t * kTileM);
+    tma_prefetch_l2_2d(&tmap_b, 0, 0);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
