@@ -383,6 +383,44 @@ def test_nan_and_inf_ieee_streaming_kernel():
     _check_ieee(run_gpu(a, b), a, b, "streaming")
 
 
+@pytest.mark.parametrize("epilogue", [False, True], ids=["plain", "gelu"])
+def test_nan_and_inf_ieee_streaming_lane_stores(epilogue):
+    """The streaming kernel with C that no tensor map describes (odd row
+    stride: per-lane stores), with more than 8 tiles a CTA (the 10-stage
+    ring) and, optionally, bias + GELU: non-finite outputs exactly where
+    IEEE has them, recomputed after the stores."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    M, N, K = 9 * 128 * sms + 77, 60, 40
+    assert G.plan(M, N, K)["variant"] == "streaming"
+    a, b = synth.make_operands(M, N, K, seed=18, dist_b="int")
+    a, b = _plant_nonfinite(a, b)
+    a[M - 1, 0] = -np.inf
+    store = torch.full((M, N + 1), -5.0, device=DEV)
+    bias = synth.make_operands(1, N, 1, seed=19)[1][0]
+    if epilogue:
+        G.gemm_f32_bias_act(_padded(a), _padded(b),
+                            torch.from_numpy(bias).to(DEV), G.ACT_GELU,
+                            c=store[:, :N])
+    else:
+        G.gemm_f32_ex(_padded(a), _padded(b), store[:, :N])
+    torch.cuda.synchronize()
+    host = store.cpu().numpy()
+    assert (host[:, N] == -5.0).all()
+    c = host[:, :N]
+    if not epilogue:
+        _check_ieee(c, a, b, "streaming, lane stores")
+        return
+    ref, bound, _ = oracle.gemm(a, b)
+    want = oracle.epilogue(ref, bias, G.ACT_GELU)
+    assert np.array_equal(np.isnan(c), np.isnan(want))
+    assert np.array_equal(np.isposinf(c), np.isposinf(want))
+    assert np.array_equal(np.isneginf(c), np.isneginf(want))
+    fin = np.isfinite(want)
+    tol = 1.2 * oracle.tolerance(bound, K) + 4 * 2.0**-24 * (
+        np.abs(oracle.epilogue(ref, bias, 0)) + np.abs(want))
+    assert (np.abs(c[fin] - want[fin]) <= tol[fin]).all()
+
+
 @pytest.mark.parametrize("form", ["NT", "TT", "TN"])
 def test_nan_and_inf_ieee_transposed_forms(form):
     """Operands read transposed in place (NT, TN: the converters transpose
