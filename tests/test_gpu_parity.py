@@ -594,10 +594,11 @@ def _stream_shapes():
             (2 * r + 5, 100, 77),    # ragged N and K, a partial last tile
             (r + 1, 33, 16),
             (3 * r - 3, 65, 120),
-            (9 * r + 77, 64, 64)]    # > 8 tiles a CTA: the 10-stage ring
+            (9 * r + 77, 64, 64),    # > 8 tiles a CTA: the 10-stage ring
+            (9 * r + 5, 128, 128)]   # the same with B at the limits
 
 
-@pytest.mark.parametrize("case", range(7))
+@pytest.mark.parametrize("case", range(8))
 def test_stream_kernel_shapes(case):
     """N <= 128, K <= 128 and a tile per SM: the persistent kernel that
     keeps Bᵀ in TMEM; every element against the oracle, and integers
